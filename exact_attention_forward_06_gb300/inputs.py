@@ -1,0 +1,152 @@
+"""Seeded synthetic inputs for attention prefill and paged decode.
+
+This module only draws random numbers and arranges them into the shapes the
+workloads use; it holds none of the attention arithmetic.  Both sides of a
+parity check (the CUDA library and the CPU oracle) receive the same bf16
+bytes from here.
+
+Recipe (the same for every workload):
+  * values are drawn with ``torch.randn`` in fp32 from a CPU
+    ``torch.Generator`` seeded per workload, in the order q, k, v, then cast
+    to bf16 (round to nearest even);
+  * tensors are generated in BSHD order ``[B, S, H, d]``; the BHSD form is a
+    permuted copy, so an element (b, s, h, c) has the same value in both;
+  * the long-sequence MQA workload scales 1% of the key positions
+    (``ceil(0.01 * Sk)`` positions from a seeded permutation) by 8 in fp32
+    before the cast, which makes some softmax rows sharply peaked;
+  * paged decode draws per-sequence lengths uniformly from [lo, hi], gives each
+    sequence ceil(L / 16) pages, assigns physical page ids by a seeded random
+    permutation of the whole pool, and pads block-table rows with -1.
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+
+import torch
+
+
+@dataclasses.dataclass(frozen=True)
+class PrefillWorkload:
+    name: str
+    B: int
+    Hq: int
+    Hkv: int
+    Sq: int
+    Sk: int
+    d: int = 128
+    layout: str = "bshd"
+    causal: bool = False
+    seed: int = 0
+    spike_frac: float = 0.0
+    spike_scale: float = 8.0
+
+    @property
+    def scale(self) -> float:
+        """Softmax scale 1/sqrt(d), rounded once to fp32."""
+        return float(torch.tensor(1.0 / math.sqrt(self.d), dtype=torch.float32).item())
+
+    @property
+    def flops(self) -> float:
+        """Matmul flops 4*B*Hq*Sq*Sk*d, halved for causal (the usual convention)."""
+        f = 4.0 * self.B * self.Hq * self.Sq * self.Sk * self.d
+        return f / 2 if self.causal else f
+
+    def with_(self, **kw) -> "PrefillWorkload":
+        return dataclasses.replace(self, **kw)
+
+
+@dataclasses.dataclass(frozen=True)
+class DecodeWorkload:
+    name: str
+    B: int = 32
+    Hq: int = 32
+    Hkv: int = 8
+    d: int = 128
+    page_size: int = 16
+    max_blocks: int = 512
+    len_lo: int = 1024
+    len_hi: int = 8192
+    seed: int = 5
+
+    @property
+    def scale(self) -> float:
+        return float(torch.tensor(1.0 / math.sqrt(self.d), dtype=torch.float32).item())
+
+    def with_(self, **kw) -> "DecodeWorkload":
+        return dataclasses.replace(self, **kw)
+
+
+# The five workloads: a tiny BHSD case, GQA causal, long MQA causal with
+# peaked rows, ragged non-causal self- and cross-attention, and paged decode.
+TINY_BHSD = PrefillWorkload("tiny_bhsd_1x2x256", 1, 2, 2, 256, 256, layout="bhsd", seed=1)
+GQA_CAUSAL = PrefillWorkload("gqa_causal_4x32q8kv_4096", 4, 32, 8, 4096, 4096, causal=True, seed=2)
+MQA_CAUSAL = PrefillWorkload("mqa_causal_1x32q1kv_16384", 1, 32, 1, 16384, 16384, causal=True,
+                             seed=3, spike_frac=0.01)
+RAGGED_SELF = PrefillWorkload("ragged_self_2x12_32760", 2, 12, 12, 32760, 32760, seed=4)
+RAGGED_CROSS = PrefillWorkload("ragged_cross_2x12_32760x512", 2, 12, 12, 32760, 512, seed=40)
+PAGED_DECODE = DecodeWorkload("paged_decode_32seq_32q8kv")
+
+PREFILL_WORKLOADS = {w.name: w for w in (TINY_BHSD, GQA_CAUSAL, MQA_CAUSAL, RAGGED_SELF, RAGGED_CROSS)}
+
+
+def _randn_bf16(shape, gen: torch.Generator) -> torch.Tensor:
+    return torch.randn(shape, generator=gen, dtype=torch.float32).to(torch.bfloat16)
+
+
+def make_prefill(w: PrefillWorkload):
+    """(q, k, v) as CPU bf16 tensors in w.layout: BSHD [B,S,H,d] or BHSD [B,H,S,d]."""
+    gen = torch.Generator().manual_seed(w.seed)
+    q = torch.randn((w.B, w.Sq, w.Hq, w.d), generator=gen, dtype=torch.float32)
+    k = torch.randn((w.B, w.Sk, w.Hkv, w.d), generator=gen, dtype=torch.float32)
+    v = torch.randn((w.B, w.Sk, w.Hkv, w.d), generator=gen, dtype=torch.float32)
+    if w.spike_frac > 0:
+        n = math.ceil(w.spike_frac * w.Sk)
+        pos = torch.randperm(w.Sk, generator=gen)[:n]
+        k[:, pos] *= w.spike_scale
+    q, k, v = (t.to(torch.bfloat16) for t in (q, k, v))
+    if w.layout == "bhsd":
+        q, k, v = (t.permute(0, 2, 1, 3).contiguous() for t in (q, k, v))
+    elif w.layout != "bshd":
+        raise ValueError(f"unknown layout {w.layout!r}")
+    return q, k, v
+
+
+def to_layout(t: torch.Tensor, src: str, dst: str) -> torch.Tensor:
+    """Re-arrange a [B,S,H,d] / [B,H,S,d] tensor between layouts (a plain permute)."""
+    if src == dst:
+        return t
+    return t.permute(0, 2, 1, 3).contiguous()
+
+
+def make_decode(w: DecodeWorkload, seqlens=None):
+    """(q [B,Hq,d], k_pages, v_pages [P,page,Hkv,d], block_table [B,max_blocks] int32, seqlens [B] int32).
+
+    `seqlens` overrides the drawn lengths (for edge cases); the pool still gets
+    ceil(L/page) pages per sequence, with permuted physical ids.
+    """
+    gen = torch.Generator().manual_seed(w.seed)
+    if seqlens is None:
+        lens = torch.randint(w.len_lo, w.len_hi + 1, (w.B,), generator=gen, dtype=torch.int64)
+    else:
+        lens = torch.as_tensor(seqlens, dtype=torch.int64)
+        assert lens.numel() == w.B
+    if int(lens.max()) > w.page_size * w.max_blocks:
+        raise ValueError("a sequence is longer than the block table allows")
+    npages = [(int(L) + w.page_size - 1) // w.page_size for L in lens]
+    total = max(1, sum(npages))
+    perm = torch.randperm(total, generator=gen).to(torch.int32)
+    table = torch.full((w.B, w.max_blocks), -1, dtype=torch.int32)
+    off = 0
+    for b, n in enumerate(npages):
+        table[b, :n] = perm[off:off + n]
+        off += n
+    q = _randn_bf16((w.B, w.Hq, w.d), gen)
+    k_pages = _randn_bf16((total, w.page_size, w.Hkv, w.d), gen)
+    v_pages = _randn_bf16((total, w.page_size, w.Hkv, w.d), gen)
+    return q, k_pages, v_pages, table, lens.to(torch.int32)
+
+
+def decode_kv_bytes(seqlens, Hkv: int, d: int) -> int:
+    """Algorithmic K+V bytes one decode pass must read: 2 tensors * 2 B * Hkv * d per token."""
+    return int(sum(int(L) for L in seqlens)) * Hkv * d * 2 * 2

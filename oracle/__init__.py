@@ -1,0 +1,228 @@
+"""Plain fp64 CPU oracle for exact attention and paged decode.
+
+TEST INFRASTRUCTURE ONLY.  The test suite, ``__graft_entry__.smoke()`` and the
+benchmark's CPU-baseline leg are the only callers.  The product path (the CUDA
+library and its Python binding) never imports this package, and this package
+never imports the product: they share no code.
+
+The arithmetic lives in ``attn_oracle.c`` (plain C, double precision,
+OpenMP over rows); this module compiles it with gcc on first use and wraps it
+with numpy.  Inputs are bf16 bit patterns (``numpy.uint16``), widened to
+double exactly inside the C code.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "attn_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+_i64 = ctypes.c_int64
+_int = ctypes.c_int
+_dbl = ctypes.c_double
+_p = ctypes.c_void_p
+
+
+class use_library:
+    """Temporarily route every oracle call to another compiled copy (tests only).
+
+    The mutation tests compile deliberately broken copies of attn_oracle.c and
+    check that the pins notice; this swaps the loaded library for the duration
+    of a ``with`` block.
+    """
+
+    def __init__(self, path: str):
+        self.path = path
+        self.saved = None
+
+    def __enter__(self):
+        global _lib
+        _load()
+        self.saved = _lib
+        lib = ctypes.CDLL(self.path)
+        for name in dir(self.saved):
+            if name.startswith("oracle_"):
+                f, g = getattr(self.saved, name), getattr(lib, name)
+                g.argtypes, g.restype = f.argtypes, f.restype
+        _lib = lib
+        return self
+
+    def __exit__(self, *exc):
+        global _lib
+        _lib = self.saved
+        return False
+
+
+def build(force: bool = False) -> str:
+    """Compile attn_oracle.c into liboracle.so next to it (gcc, -fopenmp)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        cmd = ["gcc", "-O2", "-fopenmp", "-shared", "-fPIC", "-std=c11", "-o", tmp, _SRC, "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            lib = ctypes.CDLL(_LIB)
+            lib.oracle_num_threads.restype = _int
+            lib.oracle_attention.argtypes = [_p, _p, _p, _i64, _i64, _i64, _i64, _i64, _i64,
+                                             _int, _int, _dbl, _p, _p]
+            lib.oracle_attention_rows.argtypes = [_p, _p, _p, _i64, _i64, _i64, _i64, _i64, _i64,
+                                                  _int, _int, _dbl, _i64, _p, _i64, _i64, _p, _p]
+            lib.oracle_attention_probs_row.argtypes = [_p, _p, _i64, _i64, _i64, _i64, _i64, _i64,
+                                                       _int, _int, _dbl, _i64, _i64, _i64, _p]
+            lib.oracle_attention_tiled_rows.argtypes = [_p, _p, _p, _i64, _i64, _i64, _i64, _i64, _i64,
+                                                        _int, _int, _dbl, _i64, _i64, _p, _p, _p]
+            lib.oracle_lse_merge.argtypes = [_i64, _i64, _i64, _p, _p, _p, _p]
+            lib.oracle_decode_paged.argtypes = [_p, _p, _p, _p, _p, _i64, _i64, _i64, _i64,
+                                                _i64, _i64, _i64, _dbl, _p, _p]
+            lib.oracle_round_bf16_rtne.argtypes = [_dbl]
+            lib.oracle_round_bf16_rtne.restype = ctypes.c_uint16
+            for name in ("oracle_attention", "oracle_attention_rows", "oracle_attention_probs_row",
+                         "oracle_attention_tiled_rows", "oracle_lse_merge", "oracle_decode_paged"):
+                getattr(lib, name).restype = _int
+            _lib = lib
+    return _lib
+
+
+LAYOUTS = {"bshd": 0, "bhsd": 1}
+
+
+def _bits(a) -> np.ndarray:
+    """bf16 data as a C-contiguous uint16 bit array (accepts torch bf16 or uint16 numpy)."""
+    if hasattr(a, "view") and hasattr(a, "dtype") and str(a.dtype) == "torch.bfloat16":
+        import torch  # local: only needed when handed a torch tensor
+        a = a.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+    a = np.ascontiguousarray(a)
+    if a.dtype != np.uint16:
+        raise TypeError(f"expected bf16 bit patterns (uint16), got {a.dtype}")
+    return a
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _check(rc: int, what: str):
+    if rc != 0:
+        raise ValueError(f"{what}: oracle rejected its arguments (code {rc})")
+
+
+def num_threads() -> int:
+    """OpenMP threads the oracle runs on."""
+    return _load().oracle_num_threads()
+
+
+def attention(q, k, v, *, B, Hq, Hkv, Sq, Sk, d=128, layout="bshd", causal=False, scale):
+    """Full softmax(Q K^T * scale [+causal]) V in fp64.
+
+    Returns (out, lse): out in q's layout as float64, lse as [B, Hq, Sq] float64.
+    """
+    lib = _load()
+    qb, kb, vb = _bits(q), _bits(k), _bits(v)
+    lay = LAYOUTS[layout]
+    shape = (B, Sq, Hq, d) if lay == 0 else (B, Hq, Sq, d)
+    out = np.empty(shape, np.float64)
+    lse = np.empty((B, Hq, Sq), np.float64)
+    _check(lib.oracle_attention(_ptr(qb), _ptr(kb), _ptr(vb), B, Hq, Hkv, Sq, Sk, d, lay,
+                                int(bool(causal)), float(scale), _ptr(out), _ptr(lse)), "attention")
+    return out, lse
+
+
+def attention_rows(q, k, v, rows, *, B, Hq, Hkv, Sq, Sk, d=128, layout="bshd", causal=False,
+                   scale, key_range=None):
+    """Selected rows (an [n, 3] array of (b, h, i)), optionally over keys [lo, hi).
+
+    Returns (out [n, d], lse [n]) in float64.
+    """
+    lib = _load()
+    qb, kb, vb = _bits(q), _bits(k), _bits(v)
+    rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64).reshape(-1, 3))
+    n = rows.shape[0]
+    lo, hi = (0, Sk) if key_range is None else key_range
+    out = np.empty((n, d), np.float64)
+    lse = np.empty((n,), np.float64)
+    _check(lib.oracle_attention_rows(_ptr(qb), _ptr(kb), _ptr(vb), B, Hq, Hkv, Sq, Sk, d,
+                                     LAYOUTS[layout], int(bool(causal)), float(scale), n,
+                                     _ptr(rows), int(lo), int(hi), _ptr(out), _ptr(lse)),
+           "attention_rows")
+    return out, lse
+
+
+def attention_probs_row(q, k, b, h, i, *, B, Hq, Hkv, Sq, Sk, d=128, layout="bshd",
+                        causal=False, scale):
+    """The softmax probabilities of one query row over all Sk keys (0 where masked)."""
+    lib = _load()
+    qb, kb = _bits(q), _bits(k)
+    probs = np.empty((Sk,), np.float64)
+    _check(lib.oracle_attention_probs_row(_ptr(qb), _ptr(kb), B, Hq, Hkv, Sq, Sk, d,
+                                          LAYOUTS[layout], int(bool(causal)), float(scale),
+                                          b, h, i, _ptr(probs)), "attention_probs_row")
+    return probs
+
+
+def attention_tiled_rows(q, k, v, rows, *, tile, B, Hq, Hkv, Sq, Sk, d=128, layout="bshd",
+                         causal=False, scale):
+    """The online-softmax recurrence over key tiles of `tile` keys, for selected rows."""
+    lib = _load()
+    qb, kb, vb = _bits(q), _bits(k), _bits(v)
+    rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64).reshape(-1, 3))
+    n = rows.shape[0]
+    out = np.empty((n, d), np.float64)
+    lse = np.empty((n,), np.float64)
+    _check(lib.oracle_attention_tiled_rows(_ptr(qb), _ptr(kb), _ptr(vb), B, Hq, Hkv, Sq, Sk, d,
+                                           LAYOUTS[layout], int(bool(causal)), float(scale),
+                                           int(tile), n, _ptr(rows), _ptr(out), _ptr(lse)),
+           "attention_tiled_rows")
+    return out, lse
+
+
+def lse_merge(lse_parts, o_parts):
+    """Merge key-range partials: lse_parts [S, n], o_parts [S, n, d] -> (out [n, d], lse [n])."""
+    lib = _load()
+    lse_parts = np.ascontiguousarray(lse_parts, dtype=np.float64)
+    o_parts = np.ascontiguousarray(o_parts, dtype=np.float64)
+    S, n = lse_parts.shape
+    d = o_parts.shape[2]
+    out = np.empty((n, d), np.float64)
+    lse = np.empty((n,), np.float64)
+    _check(lib.oracle_lse_merge(S, n, d, _ptr(lse_parts), _ptr(o_parts), _ptr(out), _ptr(lse)),
+           "lse_merge")
+    return out, lse
+
+
+def decode_paged(q, k_pages, v_pages, block_table, seqlens, *, scale, page_size=16):
+    """Paged-KV decode.  q [B, Hq, d]; pools [num_pages, page_size, Hkv, d];
+    block_table [B, max_blocks] int32; seqlens [B] int32.  Returns (out [B, Hq, d], lse [B, Hq])."""
+    lib = _load()
+    qb, kb, vb = _bits(q), _bits(k_pages), _bits(v_pages)
+    bt = np.ascontiguousarray(np.asarray(block_table, dtype=np.int32))
+    sl = np.ascontiguousarray(np.asarray(seqlens, dtype=np.int32))
+    B, Hq, d = qb.shape
+    num_pages, ps, Hkv, d2 = kb.shape
+    if ps != page_size or d2 != d or vb.shape != kb.shape:
+        raise ValueError("page pool shape mismatch")
+    out = np.empty((B, Hq, d), np.float64)
+    lse = np.empty((B, Hq), np.float64)
+    _check(lib.oracle_decode_paged(_ptr(qb), _ptr(kb), _ptr(vb), _ptr(bt), _ptr(sl), B, Hq, Hkv, d,
+                                   page_size, num_pages, bt.shape[1], float(scale), _ptr(out),
+                                   _ptr(lse)), "decode_paged")
+    return out, lse
+
+
+def round_bf16_rtne(x: float) -> int:
+    """Bit pattern of the bf16 nearest to x, ties to even."""
+    return int(_load().oracle_round_bf16_rtne(float(x)))

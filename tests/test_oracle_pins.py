@@ -1,0 +1,383 @@
+"""Pins for the CPU oracle: closed forms, invariants, brute force and a library routine.
+
+None of these re-types the oracle's formula.  Each checks the oracle against
+something fixed from outside it: a hand-worked example, a closed form that a
+special input reduces to, an invariance the definition implies, torch's own
+scaled-dot-product attention in fp64 (an independent library routine), or a
+different algorithm (the tiled online-softmax recurrence, the log-sum-exp
+merge) that the pages say reaches the same result.  The mutation tests at
+the bottom plant plausible mistakes in a copy of the oracle's C source and
+check that at least one pin fails for each.
+"""
+import json
+import math
+import os
+import shutil
+import subprocess
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from exact_attention_forward_06_gb300 import inputs
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+
+
+def bf16(x) -> torch.Tensor:
+    return torch.as_tensor(np.asarray(x, dtype=np.float32)).to(torch.bfloat16)
+
+
+def rand_bf16(shape, seed, std=1.0):
+    g = torch.Generator().manual_seed(seed)
+    return (torch.randn(shape, generator=g) * std).to(torch.bfloat16)
+
+
+def f64(t: torch.Tensor) -> np.ndarray:
+    return t.to(torch.float64).numpy()
+
+
+def _scalar(s: str) -> float:
+    table = {"ln3": math.log(3.0), "ln4": math.log(4.0), "1": 1.0, "0": 0.0,
+             "1+ln3": 1.0 + math.log(3.0)}
+    return table[s]
+
+
+# ---------------------------------------------------------------- golden, hand-worked
+
+def test_golden_hand_worked():
+    data = json.load(open(os.path.join(HERE, "golden", "hand_worked.json")))
+    for case in data["cases"]:
+        q = bf16(case["q"])[None, :, None, :]   # [B=1, Sq, H=1, d]
+        k = bf16(case["k"])[None, :, None, :]
+        v = bf16(case["v"])[None, :, None, :]
+        Sq, Sk, d = q.shape[1], k.shape[1], q.shape[3]
+        out, lse = oracle.attention(q, k, v, B=1, Hq=1, Hkv=1, Sq=Sq, Sk=Sk, d=d,
+                                    causal=case["causal"], scale=_scalar(case["scale"]))
+        np.testing.assert_allclose(out[0, :, 0, :], np.array(case["out"]), rtol=0, atol=1e-12,
+                                   err_msg=case["name"])
+        np.testing.assert_allclose(lse[0, 0], [_scalar(s) for s in case["lse"]], rtol=0, atol=1e-12,
+                                   err_msg=case["name"])
+
+
+# ---------------------------------------------------------------- library routine
+
+def _sdpa_reference(q, k, v, causal, scale, layout="bshd"):
+    """torch.nn.functional.scaled_dot_product_attention in fp64, bottom-right causal mask."""
+    if layout == "bshd":
+        q, k, v = (t.permute(0, 2, 1, 3) for t in (q, k, v))
+    q, k, v = (t.to(torch.float64) for t in (q, k, v))
+    Hq, Hkv = q.shape[1], k.shape[1]
+    k = k.repeat_interleave(Hq // Hkv, dim=1)
+    v = v.repeat_interleave(Hq // Hkv, dim=1)
+    Sq, Sk = q.shape[2], k.shape[2]
+    mask = None
+    if causal:
+        i = torch.arange(Sq)[:, None]
+        j = torch.arange(Sk)[None, :]
+        mask = j <= i + (Sk - Sq)
+    o = torch.nn.functional.scaled_dot_product_attention(q, k, v, attn_mask=mask, scale=scale)
+    if layout == "bshd":
+        o = o.permute(0, 2, 1, 3)
+    return o.numpy()
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,Sq,Sk,causal,layout", [
+    (1, 2, 2, 17, 17, False, "bshd"),
+    (2, 4, 2, 33, 33, True, "bshd"),
+    (1, 4, 1, 5, 40, False, "bhsd"),
+    (1, 6, 3, 24, 31, True, "bhsd"),   # Sk > Sq causal: bottom-right
+])
+def test_matches_torch_sdpa_fp64(B, Hq, Hkv, Sq, Sk, causal, layout):
+    d = 32
+    w = inputs.PrefillWorkload("t", B, Hq, Hkv, Sq, Sk, d=d, layout=layout, causal=causal, seed=11)
+    q, k, v = inputs.make_prefill(w)
+    scale = 1.0 / math.sqrt(d)
+    out, _ = oracle.attention(q, k, v, B=B, Hq=Hq, Hkv=Hkv, Sq=Sq, Sk=Sk, d=d, layout=layout,
+                              causal=causal, scale=scale)
+    ref = _sdpa_reference(q, k, v, causal, scale, layout)
+    np.testing.assert_allclose(out, ref, rtol=1e-10, atol=1e-12)
+
+
+# ---------------------------------------------------------------- closed forms
+
+def test_identical_keys_give_mean_of_v():
+    B, H, S, d = 1, 2, 37, 16
+    q = rand_bf16((B, S, H, d), 1)
+    k0 = rand_bf16((1, 1, H, d), 2)
+    k = k0.expand(B, S, H, d).contiguous()
+    v = rand_bf16((B, S, H, d), 3)
+    scale = 0.3
+    out, lse = oracle.attention(q, k, v, B=B, Hq=H, Hkv=H, Sq=S, Sk=S, d=d, scale=scale)
+    mean_v = f64(v).mean(axis=1)                       # [B, H, d]
+    np.testing.assert_allclose(out, np.broadcast_to(mean_v[:, None], out.shape), rtol=0, atol=1e-12)
+    s = scale * np.einsum("bihc,hc->bhi", f64(q), f64(k0)[0, 0])
+    np.testing.assert_allclose(lse, s + math.log(S), rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("causal,Sq,Sk", [(False, 9, 13), (True, 13, 13), (True, 5, 13)])
+def test_zero_scale_counts_visible_keys(causal, Sq, Sk):
+    d = 8
+    q, k, v = rand_bf16((1, Sq, 1, d), 4), rand_bf16((1, Sk, 1, d), 5), rand_bf16((1, Sk, 1, d), 6)
+    out, lse = oracle.attention(q, k, v, B=1, Hq=1, Hkv=1, Sq=Sq, Sk=Sk, d=d, causal=causal, scale=0.0)
+    vv = f64(v)[0, :, 0, :]
+    for i in range(Sq):
+        n = min(Sk, i + 1 + Sk - Sq) if causal else Sk
+        np.testing.assert_allclose(out[0, i, 0], vv[:n].mean(axis=0), rtol=0, atol=1e-12)
+        assert abs(lse[0, 0, i] - math.log(n)) < 1e-12
+
+
+def test_dominant_score_selects_its_value_row():
+    d, Sk = 16, 20
+    q = bf16(np.eye(1, d, 0))[None, :, None, :]                # q = e0
+    k = np.zeros((Sk, d), np.float32)
+    k[:, 1] = 1.0
+    jstar = 7
+    k[jstar, 0] = 64.0                                          # score gap of 64 * scale
+    v = rand_bf16((1, Sk, 1, d), 7)
+    scale = 1.0
+    out, lse = oracle.attention(q, bf16(k)[None, :, None, :], v, B=1, Hq=1, Hkv=1, Sq=1, Sk=Sk,
+                                d=d, scale=scale)
+    np.testing.assert_allclose(out[0, 0, 0], f64(v)[0, jstar, 0], rtol=0, atol=1e-20)
+    assert abs(lse[0, 0, 0] - 64.0) < 1e-12
+
+
+def test_causal_row_zero_is_first_value():
+    B, H, S, d = 2, 3, 19, 16
+    q, k, v = rand_bf16((B, S, H, d), 8), rand_bf16((B, S, H, d), 9), rand_bf16((B, S, H, d), 10)
+    scale = 0.25
+    out, lse = oracle.attention(q, k, v, B=B, Hq=H, Hkv=H, Sq=S, Sk=S, d=d, causal=True, scale=scale)
+    np.testing.assert_array_equal(out[:, 0], f64(v)[:, 0])
+    s00 = scale * np.einsum("bhc,bhc->bh", f64(q)[:, 0], f64(k)[:, 0])
+    np.testing.assert_allclose(lse[:, :, 0], s00, rtol=0, atol=1e-12)
+
+
+def test_single_key_returns_it_for_every_row():
+    Sq, d = 11, 16
+    q, k, v = rand_bf16((1, Sq, 2, d), 11), rand_bf16((1, 1, 2, d), 12), rand_bf16((1, 1, 2, d), 13)
+    out, _ = oracle.attention(q, k, v, B=1, Hq=2, Hkv=2, Sq=Sq, Sk=1, d=d, scale=0.7)
+    np.testing.assert_array_equal(out, np.broadcast_to(f64(v)[:, :1], out.shape))
+
+
+def test_constant_value_vector_is_returned():
+    S, d = 23, 16
+    q, k = rand_bf16((1, S, 2, d), 14, std=3.0), rand_bf16((1, S, 2, d), 15, std=3.0)
+    c = rand_bf16((d,), 16)
+    v = c.expand(1, S, 2, d).contiguous()
+    out, _ = oracle.attention(q, k, v, B=1, Hq=2, Hkv=2, Sq=S, Sk=S, d=d, causal=True, scale=0.5)
+    np.testing.assert_allclose(out, np.broadcast_to(f64(c), out.shape), rtol=1e-14, atol=0)
+
+
+def test_probability_rows_sum_to_one():
+    S, d = 29, 16
+    q, k = rand_bf16((1, S, 1, d), 17, std=4.0), rand_bf16((1, S, 1, d), 18, std=4.0)
+    for i in (0, 5, 28):
+        for causal in (False, True):
+            p = oracle.attention_probs_row(q, k, 0, 0, i, B=1, Hq=1, Hkv=1, Sq=S, Sk=S, d=d,
+                                           causal=causal, scale=0.5)
+            assert abs(p.sum() - 1.0) < 1e-12
+            assert (p >= 0).all()
+            if causal:
+                assert (p[i + 1:] == 0).all()
+
+
+def test_fully_masked_rows_are_zero_with_minus_inf_lse():
+    Sq, Sk, d = 10, 4, 8          # causal with Sq > Sk: rows i < Sq - Sk see no key
+    q, k, v = rand_bf16((1, Sq, 1, d), 19), rand_bf16((1, Sk, 1, d), 20), rand_bf16((1, Sk, 1, d), 21)
+    out, lse = oracle.attention(q, k, v, B=1, Hq=1, Hkv=1, Sq=Sq, Sk=Sk, d=d, causal=True, scale=1.0)
+    for i in range(Sq):
+        if i < Sq - Sk:
+            assert (out[0, i, 0] == 0).all() and lse[0, 0, i] == -math.inf
+        else:
+            assert np.isfinite(lse[0, 0, i])
+    # the last row sees every key: equals the non-causal last row
+    ref, _ = oracle.attention(q, k, v, B=1, Hq=1, Hkv=1, Sq=Sq, Sk=Sk, d=d, causal=False, scale=1.0)
+    np.testing.assert_array_equal(out[0, -1], ref[0, -1])
+
+
+# ---------------------------------------------------------------- invariants
+
+def test_gqa_equals_replicated_kv_heads():
+    B, Hq, Hkv, S, d = 2, 8, 2, 21, 16
+    w = inputs.PrefillWorkload("g", B, Hq, Hkv, S, S, d=d, causal=True, seed=22)
+    q, k, v = inputs.make_prefill(w)
+    out, lse = oracle.attention(q, k, v, B=B, Hq=Hq, Hkv=Hkv, Sq=S, Sk=S, d=d, causal=True, scale=0.2)
+    G = Hq // Hkv
+    kr, vr = k.repeat_interleave(G, dim=2), v.repeat_interleave(G, dim=2)
+    out2, lse2 = oracle.attention(q, kr, vr, B=B, Hq=Hq, Hkv=Hq, Sq=S, Sk=S, d=d, causal=True, scale=0.2)
+    np.testing.assert_allclose(out, out2, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse, lse2, rtol=0, atol=1e-12)
+
+
+def test_layouts_agree_after_permute():
+    B, Hq, Hkv, Sq, Sk, d = 2, 4, 2, 13, 17, 16
+    w = inputs.PrefillWorkload("l", B, Hq, Hkv, Sq, Sk, d=d, layout="bshd", causal=True, seed=23)
+    q, k, v = inputs.make_prefill(w)
+    q2, k2, v2 = inputs.make_prefill(w.with_(layout="bhsd"))
+    assert torch.equal(q.permute(0, 2, 1, 3), q2)
+    o1, l1 = oracle.attention(q, k, v, B=B, Hq=Hq, Hkv=Hkv, Sq=Sq, Sk=Sk, d=d, layout="bshd",
+                              causal=True, scale=0.3)
+    o2, l2 = oracle.attention(q2, k2, v2, B=B, Hq=Hq, Hkv=Hkv, Sq=Sq, Sk=Sk, d=d, layout="bhsd",
+                              causal=True, scale=0.3)
+    np.testing.assert_array_equal(o1, o2.transpose(0, 2, 1, 3))
+    np.testing.assert_array_equal(l1, l2)
+
+
+def test_key_permutation_invariance_noncausal():
+    S, Sk, d = 7, 31, 16
+    q, k, v = rand_bf16((1, S, 2, d), 24), rand_bf16((1, Sk, 2, d), 25), rand_bf16((1, Sk, 2, d), 26)
+    perm = torch.randperm(Sk, generator=torch.Generator().manual_seed(27))
+    o1, l1 = oracle.attention(q, k, v, B=1, Hq=2, Hkv=2, Sq=S, Sk=Sk, d=d, scale=0.4)
+    o2, l2 = oracle.attention(q, k[:, perm].contiguous(), v[:, perm].contiguous(), B=1, Hq=2, Hkv=2,
+                              Sq=S, Sk=Sk, d=d, scale=0.4)
+    np.testing.assert_allclose(o1, o2, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(l1, l2, rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("Sq,Sk", [(1, 1), (3, 3), (17, 17), (128, 128), (130, 130), (3, 17), (17, 130)])
+@pytest.mark.parametrize("tile", [1, 5, 64])
+def test_tiled_online_softmax_equals_full(Sq, Sk, tile):
+    d = 16
+    causal = Sq == Sk and Sq % 2 == 1
+    q, k, v = rand_bf16((1, Sq, 1, d), 30, 2.0), rand_bf16((1, Sk, 1, d), 31, 2.0), rand_bf16((1, Sk, 1, d), 32)
+    rows = [(0, 0, i) for i in range(Sq)]
+    kw = dict(B=1, Hq=1, Hkv=1, Sq=Sq, Sk=Sk, d=d, causal=causal, scale=0.6)
+    o_full, l_full = oracle.attention_rows(q, k, v, rows, **kw)
+    o_tile, l_tile = oracle.attention_tiled_rows(q, k, v, rows, tile=tile, **kw)
+    np.testing.assert_allclose(o_tile, o_full, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(l_tile, l_full, rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("nsplit", [1, 2, 3, 7])
+def test_split_and_merge_equals_unsplit(nsplit):
+    Sq, Sk, d = 9, 50, 16
+    q, k, v = rand_bf16((1, Sq, 2, d), 33, 2.0), rand_bf16((1, Sk, 2, d), 34, 2.0), rand_bf16((1, Sk, 2, d), 35)
+    rows = [(0, h, i) for h in range(2) for i in range(Sq)]
+    kw = dict(B=1, Hq=2, Hkv=2, Sq=Sq, Sk=Sk, d=d, causal=True, scale=0.5)
+    o_full, l_full = oracle.attention_rows(q, k, v, rows, **kw)
+    bounds = np.linspace(0, Sk, nsplit + 1).astype(int)
+    parts = [oracle.attention_rows(q, k, v, rows, key_range=(bounds[s], bounds[s + 1]), **kw)
+             for s in range(nsplit)]
+    o_m, l_m = oracle.lse_merge(np.stack([p[1] for p in parts]), np.stack([p[0] for p in parts]))
+    np.testing.assert_allclose(o_m, o_full, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(l_m, l_full, rtol=0, atol=1e-12)
+
+
+def test_merge_of_empty_partials():
+    lse_s = np.array([[-np.inf], [-np.inf]])
+    o_s = np.zeros((2, 1, 4))
+    o, l = oracle.lse_merge(lse_s, o_s)
+    assert l[0] == -np.inf and (o == 0).all()
+
+
+# ---------------------------------------------------------------- paged decode
+
+def _gather_contiguous(k_pages, v_pages, table, seqlens, b):
+    L = int(seqlens[b])
+    ids = [int(table[b, t // 16]) for t in range(L)]
+    slots = [t % 16 for t in range(L)]
+    k = k_pages[ids, slots][None]   # [1, L, Hkv, d]
+    v = v_pages[ids, slots][None]
+    return k.contiguous(), v.contiguous()
+
+
+def test_paged_decode_equals_contiguous_prefill_oracle():
+    w = inputs.DecodeWorkload("small", B=3, Hq=8, Hkv=2, d=16, max_blocks=8, len_lo=1, len_hi=120, seed=40)
+    q, kp, vp, table, lens = inputs.make_decode(w, seqlens=[1, 17, 128])
+    out, lse = oracle.decode_paged(q, kp, vp, table, lens, scale=0.3)
+    for b in range(w.B):
+        k, v = _gather_contiguous(kp, vp, table, lens, b)
+        L = int(lens[b])
+        qb = q[b][None, None]             # [1, Sq=1, Hq, d]
+        o2, l2 = oracle.attention(qb, k, v, B=1, Hq=w.Hq, Hkv=w.Hkv, Sq=1, Sk=L, d=w.d, scale=0.3)
+        np.testing.assert_array_equal(out[b], o2[0, 0])
+        np.testing.assert_array_equal(lse[b], l2[0, :, 0])
+
+
+def test_paged_decode_zero_length_and_padding():
+    w = inputs.DecodeWorkload("z", B=2, Hq=4, Hkv=4, d=16, max_blocks=4, seed=41)
+    q, kp, vp, table, lens = inputs.make_decode(w, seqlens=[0, 16])
+    assert (table[0] == -1).all() and (table[1, 1:] == -1).all()
+    out, lse = oracle.decode_paged(q, kp, vp, table, lens, scale=0.3)
+    assert (out[0] == 0).all() and (lse[0] == -np.inf).all()
+    assert np.isfinite(lse[1]).all()
+
+
+def test_paged_decode_rejects_bad_block_table():
+    w = inputs.DecodeWorkload("z", B=1, Hq=4, Hkv=4, d=16, max_blocks=4, seed=42)
+    q, kp, vp, table, lens = inputs.make_decode(w, seqlens=[20])
+    table[0, 1] = kp.shape[0]           # one past the pool
+    with pytest.raises(ValueError):
+        oracle.decode_paged(q, kp, vp, table, lens, scale=0.3)
+
+
+# ---------------------------------------------------------------- bf16 rounding
+
+def test_bf16_rtne_matches_torch_on_float_values():
+    g = torch.Generator().manual_seed(50)
+    x = torch.randn(20000, generator=g, dtype=torch.float32) * torch.exp(torch.randn(20000, generator=g) * 8)
+    want = x.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    got = np.array([oracle.round_bf16_rtne(float(t)) for t in x], dtype=np.uint16)
+    np.testing.assert_array_equal(got, want)
+
+
+def test_bf16_rtne_ties_go_to_even():
+    assert oracle.round_bf16_rtne(1.0) == 0x3F80
+    assert oracle.round_bf16_rtne(1.0 + 2.0 ** -8) == 0x3F80          # tie, even stays
+    assert oracle.round_bf16_rtne(1.0 + 3 * 2.0 ** -8) == 0x3F82      # tie, rounds up to even
+    assert oracle.round_bf16_rtne(1.0 + 2.0 ** -8 + 2.0 ** -30) == 0x3F81   # just above the tie
+    assert oracle.round_bf16_rtne(-2.0) == 0xC000
+    assert oracle.round_bf16_rtne(float("inf")) == 0x7F80
+
+
+# ---------------------------------------------------------------- mutation tests
+
+MUTATIONS = {
+    # wrong GQA head map
+    "head_map_modulo": ("const int64_t g = h / (p->Hq / p->Hkv);", "const int64_t g = h % p->Hkv;"),
+    # top-left causal alignment instead of bottom-right
+    "causal_top_left": ("int64_t lim = i + Sk - Sq;", "int64_t lim = i;"),
+    # sign error in the exponent
+    "exp_sign": ("double w = exp(scores[j] - M);", "double w = exp(M - scores[j]);"),
+    # dropped normalisation
+    "no_normalise": ("for (int64_t c = 0; c < d; ++c) o[c] /= L;", ";"),
+    # lse off by the log term
+    "lse_sign": ("*lse = M + log(L);", "*lse = M - log(L);"),
+    # transposed operand: key index used for the value row
+    "value_from_query_row": ("o[c] += w * bf16_to_double(p->v[offset_of(p->layout, b, j, g, c, p->Sk, p->Hkv, d)]);",
+                             "o[c] += w * bf16_to_double(p->v[offset_of(p->layout, b, i < p->Sk ? i : 0, g, c, p->Sk, p->Hkv, d)]);"),
+}
+
+
+def _pin_suite():
+    """The pins that exercise the whole-row path, run against whichever oracle is loaded."""
+    failures = []
+    for fn in (test_golden_hand_worked,
+               lambda: test_matches_torch_sdpa_fp64(1, 6, 3, 24, 31, True, "bhsd"),
+               lambda: test_matches_torch_sdpa_fp64(2, 4, 2, 33, 33, True, "bshd"),
+               test_identical_keys_give_mean_of_v,
+               lambda: test_zero_scale_counts_visible_keys(True, 5, 13),
+               test_gqa_equals_replicated_kv_heads):
+        try:
+            fn()
+        except AssertionError:
+            failures.append(fn)
+    return failures
+
+
+@pytest.mark.skipif(shutil.which("gcc") is None, reason="needs gcc")
+@pytest.mark.parametrize("name", sorted(MUTATIONS))
+def test_planted_mistake_is_caught(name, tmp_path):
+    src = open(os.path.join(os.path.dirname(oracle.__file__), "attn_oracle.c")).read()
+    old, new = MUTATIONS[name]
+    assert old in src, f"mutation anchor for {name} not found"
+    bad = tmp_path / "bad.c"
+    bad.write_text(src.replace(old, new, 1))
+    so = tmp_path / "libbad.so"
+    subprocess.run(["gcc", "-O1", "-fopenmp", "-shared", "-fPIC", "-o", str(so), str(bad), "-lm"], check=True)
+    with oracle.use_library(str(so)):
+        failures = _pin_suite()
+    assert failures, f"no pin caught the planted mistake {name}"
+    # and the real oracle passes the same suite
+    assert not _pin_suite()
