@@ -1,0 +1,440 @@
+"""Benchmark: attention forward TFLOPS and paged-decode HBM GB/s on one GB300.
+
+One step = one pass of the whole hot path: the fused prefill forward on the
+GQA causal workload (B=4, Hq=32, Hkv=8, Sq=Sk=4096, d=128, bf16, BSHD) followed
+by one paged-KV decode step (32 sequences, Hq=32, Hkv=8, lengths U[1024, 8192],
+16-token pages).  `value` is the prefill TFLOPS (4*B*Hq*Sq*Sk*d / 2 flops per
+launch, causal) over the timed steps; the decode GB/s (algorithmic K+V bytes
+per launch / time) is reported beside it.  Inputs are seeded synthetic data of
+those shapes, resident in HBM when the timed region starts, and larger than
+L2 (no flush needed).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
+
+Under torchrun (N > 1) every rank runs its own replica of the step (weak
+scaling, no collective on the data path); timing is bracketed by a barrier and
+the max over ranks is reported.  `--impl reference` times the fp64 CPU oracle
+on bounded samples of the same workload instead (the slow reference arm).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from exact_attention_forward_06_gb300 import inputs  # noqa: E402
+
+PEAKS_PATH = os.path.join(ROOT, "MEASURED_PEAKS.json")
+TRAFFIC_PATH = os.path.join(ROOT, "profiles", "dram_traffic.json")
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+PREFILL_KERNEL_SRC = os.path.join(ROOT, "exact_attention_forward_06_gb300", "csrc", "prefill_tc.cu")
+DECODE_KERNEL_SRC = os.path.join(ROOT, "exact_attention_forward_06_gb300", "csrc", "decode.cu")
+
+
+# ---------------------------------------------------------------------------- helpers
+
+def load_peaks():
+    try:
+        with open(PEAKS_PATH) as f:
+            d = json.load(f)
+        return d, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def source_hash(path):
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def traffic_for(kernel_key, src_path, units_per_launch):
+    """DRAM bytes per launch from the committed ncu summary, or None if stale/absent.
+
+    The summary stores bytes per unit of work measured on one capture; the
+    kernel source hash recorded with it must match the current source.
+    """
+    try:
+        with open(TRAFFIC_PATH) as f:
+            t = json.load(f)[kernel_key]
+    except (OSError, ValueError, KeyError):
+        return None
+    if t.get("source_sha256_16") != source_hash(src_path):
+        return None
+    return t["bytes_per_unit"] * units_per_launch
+
+
+def reduce_max_over_ranks(x: float) -> float:
+    """Max of a host scalar over all ranks (identity without a process group)."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return x
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason sampling during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            if self.thread is not None:
+                self.thread.join(timeout=2)
+        return False
+
+    def summary(self):
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+        sm_sorted = sorted(sm)
+        return {"sm_mhz": sm_sorted[len(sm_sorted) // 2], "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------- our arm
+
+def run_ours(args, rank, world, local_rank):
+    import exact_attention_forward_06_gb300 as A
+    A.load()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    peaks, peak_src = load_peaks()
+    wp = inputs.PREFILL_WORKLOADS[args.workload]
+    wd = inputs.PAGED_DECODE
+
+    # Inputs (seeded, synthetic), resident on the device.
+    q_h, k_h, v_h = inputs.make_prefill(wp)
+    q, k, v = (t.to(dev) for t in (q_h, k_h, v_h))
+    out = torch.empty_like(q)
+    lse = torch.empty((wp.B, wp.Hq, wp.Sq), device=dev, dtype=torch.float32)
+    dq_h, kp_h, vp_h, table_h, lens_h = inputs.make_decode(wd)
+    dq, kp, vp, table, lens = (t.to(dev) for t in (dq_h, kp_h, vp_h, table_h, lens_h))
+    dout = torch.empty_like(dq)
+    dlse = torch.empty((wd.B, wd.Hq), device=dev, dtype=torch.float32)
+    ws = torch.empty(A.decode_workspace_bytes(wd.B, wd.Hq, wd.d, wd.max_blocks), device=dev, dtype=torch.uint8)
+    stream = torch.cuda.current_stream(dev)
+
+    def prefill():
+        A.fwd(q, k, v, causal=wp.causal, scale=wp.scale, layout=wp.layout, out=out, lse=lse, stream=stream)
+
+    def decode():
+        A.decode_paged(dq, kp, vp, table, lens, scale=wd.scale, out=dout, lse=dlse, workspace=ws, stream=stream)
+
+    for _ in range(args.warmup):
+        prefill()
+        decode()
+    torch.cuda.synchronize(dev)
+    code, site = A.device_status()
+    if code != 0:
+        raise RuntimeError(f"device status {code} at site {site} after warm-up")
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(dev.index if dev.index is not None else 0) as clocks:
+        start.record(stream)
+        for i in range(K):
+            ev[i][0].record(stream)
+            prefill()
+            ev[i][1].record(stream)
+            decode()
+            ev[i][2].record(stream)
+        stop.record(stream)
+        torch.cuda.synchronize(dev)
+    barrier()
+    code, site = A.device_status()
+    if code != 0:
+        raise RuntimeError(f"device status {code} at site {site} after the timed steps")
+    total_ms = start.elapsed_time(stop)
+    prefill_ms = sum(e[0].elapsed_time(e[1]) for e in ev) / K
+    decode_ms = sum(e[1].elapsed_time(e[2]) for e in ev) / K
+    total_ms = reduce_max_over_ranks(total_ms)
+    prefill_ms = reduce_max_over_ranks(prefill_ms)
+    decode_ms = reduce_max_over_ranks(decode_ms)
+
+    # End to end through the public API: pinned host inputs -> device -> result back to pinned host.
+    e2e = run_e2e(A, wp, q_h, k_h, v_h, dev, stream, args)
+
+    if rank != 0:
+        return None
+    flops = wp.flops
+    tflops = world * flops / (prefill_ms * 1e-3) / 1e12
+    per_launch_tflops = flops / (prefill_ms * 1e-3) / 1e12
+    kv_bytes = inputs.decode_kv_bytes(lens_h.tolist(), wd.Hkv, wd.d)
+    dec_gbs_launch = kv_bytes / (decode_ms * 1e-3) / 1e9
+    n_units = prefill_units(wp)
+    traffic = traffic_for("prefill_kernel", PREFILL_KERNEL_SRC, n_units)
+    dec_traffic = traffic_for("decode_split_kernel", DECODE_KERNEL_SRC, sum(int(x) for x in lens_h.tolist()))
+    clk = clocks.summary()
+    line = {
+        "metric": "attn fwd TFLOPS (bf16, d=128) and % of GB300 bf16 peak; paged decode HBM GB/s",
+        "value": round(tflops, 2),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": round(total_ms / K, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded randn, bf16)",
+        "config": {"workload": wp.name, "B": wp.B, "Hq": wp.Hq, "Hkv": wp.Hkv, "Sq": wp.Sq, "Sk": wp.Sk,
+                   "d": wp.d, "layout": wp.layout, "causal": wp.causal,
+                   "decode_workload": wd.name, "decode_B": wd.B, "decode_Hq": wd.Hq, "decode_Hkv": wd.Hkv,
+                   "decode_lengths": f"U[{wd.len_lo},{wd.len_hi}] seed {wd.seed}, sum {int(lens_h.sum())}",
+                   "page_size": wd.page_size, "l2": "inputs larger than L2 (no flush)",
+                   "parallelism": f"replicas x{world}"},
+        "prefill_ms_per_launch": round(prefill_ms, 4),
+        "roofline": {"bound": "tensor", "achieved": round(per_launch_tflops, 2),
+                     "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                     "frac": round(per_launch_tflops / peaks["bf16_tflops"], 4),
+                     "traffic": traffic, "peak_source": f"{peak_src} bf16_tflops (burst)",
+                     "kernel": "attn::g1::prefill_kernel",
+                     "algorithmic": f"{flops:.4g} flop per launch (4*B*Hq*Sq*Sk*d/2)"},
+        "decode": {"value": round(dec_gbs_launch * world, 1), "unit": "GB/s", "ms_per_launch": round(decode_ms, 4),
+                   "roofline": {"bound": "hbm", "achieved": round(dec_gbs_launch, 1), "peak": peaks["hbm_gbs"],
+                                "unit": "GB/s", "frac": round(dec_gbs_launch / peaks["hbm_gbs"], 4),
+                                "traffic": dec_traffic, "peak_source": f"{peak_src} hbm_gbs",
+                                "kernel": "attn::dec::split_kernel + merge_kernel",
+                                "algorithmic": f"{kv_bytes} B K+V per launch (4096 B per token)"}},
+        "e2e": e2e,
+        "gpu_launches": 3 * K,
+        "clocks": clk,
+    }
+    if not args.no_cpu_baseline and world == 1:
+        line["cpu_baseline"] = cpu_baseline(wp, q_h, k_h, v_h, seconds=args.cpu_seconds)
+    return line
+
+
+def prefill_units(w):
+    """Work units (two 128-row Q tiles) one prefill launch processes."""
+    G = w.Hq // w.Hkv
+    n_m = (w.Sq + 127) // 128
+    if G % 2 == 0:
+        return w.B * w.Hkv * (G // 2) * n_m
+    return w.B * w.Hq * ((n_m + 1) // 2)
+
+
+def run_e2e(A, w, q_h, k_h, v_h, dev, stream, args):
+    qp, kp, vp = (t.pin_memory() for t in (q_h, k_h, v_h))
+    q = torch.empty_like(qp, device=dev)
+    k = torch.empty_like(kp, device=dev)
+    v = torch.empty_like(vp, device=dev)
+    out_h = torch.empty_like(qp).pin_memory()
+    lse_h = torch.empty((w.B, w.Hq, w.Sq), dtype=torch.float32).pin_memory()
+    out = torch.empty_like(q)
+    lse = torch.empty((w.B, w.Hq, w.Sq), device=dev, dtype=torch.float32)
+
+    def step():
+        q.copy_(qp, non_blocking=True)
+        k.copy_(kp, non_blocking=True)
+        v.copy_(vp, non_blocking=True)
+        A.fwd(q, k, v, causal=w.causal, scale=w.scale, layout=w.layout, out=out, lse=lse, stream=stream)
+        out_h.copy_(out, non_blocking=True)
+        lse_h.copy_(lse, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        step()
+    torch.cuda.synchronize(dev)
+    n = max(1, args.steps // 2)
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    s.record(stream)
+    for _ in range(n):
+        step()
+    e.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = reduce_max_over_ranks(s.elapsed_time(e) / n)
+    world = _world()
+    h2d = sum(t.numel() * t.element_size() for t in (qp, kp, vp))
+    d2h = out_h.numel() * out_h.element_size() + lse_h.numel() * lse_h.element_size()
+    return {"value": round(world * w.flops / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 4),
+            "api": "exact_attention_forward_06_gb300.fwd (C ABI attn_fwd) with pinned host copies"}
+
+
+# ---------------------------------------------------------------------------- CPU oracle arms
+
+def _row_flops(w, rows):
+    """Matmul flops of the sampled rows: 4*d per visible key."""
+    tot = 0
+    for _, _, i in rows:
+        n = min(w.Sk, i + 1 + w.Sk - w.Sq) if w.causal else w.Sk
+        tot += 4 * w.d * max(0, n)
+    return tot
+
+
+def _oracle_sample(w, q_h, k_h, v_h, seconds, seed):
+    import numpy as np
+    import oracle
+    rng = np.random.default_rng(seed)
+
+    def rows_of(n):
+        return np.stack([rng.integers(0, w.B, n), rng.integers(0, w.Hq, n), rng.integers(0, w.Sq, n)], 1)
+
+    kw = dict(B=w.B, Hq=w.Hq, Hkv=w.Hkv, Sq=w.Sq, Sk=w.Sk, d=w.d, layout=w.layout, causal=w.causal,
+              scale=w.scale)
+    # calibrate on a small batch, then size the sample to about `seconds`
+    probe = rows_of(max(8, oracle.num_threads()))
+    t0 = time.perf_counter()
+    oracle.attention_rows(q_h, k_h, v_h, probe, **kw)
+    dt = time.perf_counter() - t0
+    n = max(len(probe), int(len(probe) * seconds / max(dt, 1e-3)))
+    rows = rows_of(n)
+    t0 = time.perf_counter()
+    oracle.attention_rows(q_h, k_h, v_h, rows, **kw)
+    dt = time.perf_counter() - t0
+    return _row_flops(w, rows), dt, n
+
+
+def cpu_baseline(w, q_h, k_h, v_h, seconds):
+    import oracle
+    flops, dt, n = _oracle_sample(w, q_h, k_h, v_h, seconds, seed=1)
+    return {"value": round(flops / dt / 1e12, 6), "unit": "TFLOP/s", "cores": oracle.num_threads(),
+            "kind": "oracle",
+            "sample": f"{n} uniformly drawn query rows of {w.name} (fp64 C oracle, OpenMP), {dt:.1f} s"}
+
+
+def run_reference(args, rank, world):
+    import oracle
+    if rank != 0:
+        return None
+    w = inputs.PREFILL_WORKLOADS[args.workload]
+    q_h, k_h, v_h = inputs.make_prefill(w)
+    per_step = max(1.0, min(6.0, 60.0 / max(1, args.steps + args.warmup)))
+    for i in range(args.warmup):
+        _oracle_sample(w, q_h, k_h, v_h, per_step / 2, seed=100 + i)
+    tot_flops, tot_t, tot_rows = 0, 0.0, 0
+    for i in range(args.steps):
+        f, dt, n = _oracle_sample(w, q_h, k_h, v_h, per_step, seed=i)
+        tot_flops += f
+        tot_t += dt
+        tot_rows += n
+    value = tot_flops / tot_t / 1e12
+    return {
+        "impl": "reference",
+        "metric": "attn fwd TFLOPS (bf16, d=128) and % of GB300 bf16 peak; paged decode HBM GB/s",
+        "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(1e3 * tot_t / args.steps, 2), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded randn, bf16 inputs)",
+        "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "Sq": w.Sq, "Sk": w.Sk, "d": w.d,
+                   "layout": w.layout, "causal": w.causal},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": oracle.num_threads(),
+                         "kind": "oracle",
+                         "sample": f"{tot_rows} uniformly drawn query rows of {w.name} over {args.steps} steps"},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+
+
+# ---------------------------------------------------------------------------- main
+
+def _world():
+    return int(os.environ.get("WORLD_SIZE", "1"))
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=inputs.GQA_CAUSAL.name, choices=sorted(inputs.PREFILL_WORKLOADS))
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = _world()
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "gloo" if args.impl == "reference" else "nccl"
+        if backend == "nccl":
+            torch.cuda.set_device(local_rank)
+        dist.init_process_group(backend=backend)
+    try:
+        if args.impl == "reference":
+            line = run_reference(args, rank, world)
+        else:
+            line = run_ours(args, rank, world, local_rank)
+        if rank == 0 and line is not None:
+            print(json.dumps(line), flush=True)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            if dist.is_initialized():
+                dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

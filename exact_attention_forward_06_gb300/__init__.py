@@ -1,0 +1,13 @@
+"""GB300-native (sm_103a) exact attention: fused prefill forward and paged-KV decode.
+
+The computation lives in the CUDA library ``libattn.so`` (C ABI, include/attn.h);
+this package is its thin Python binding.  Importing the package does not load
+the library; the first call does, and raises if it has not been built.
+"""
+from ._binding import (AttnError, LIBRARY_PATH, debug_inject, decode_paged, decode_workspace_bytes,
+                       device_status, fwd, fwd_simple, load, lse_merge, selftest_umma, set_wait_budget_ns,
+                       status_string, version)
+
+__all__ = ["AttnError", "LIBRARY_PATH", "debug_inject", "decode_paged", "decode_workspace_bytes", "device_status",
+           "fwd", "fwd_simple", "load", "lse_merge", "selftest_umma", "set_wait_budget_ns", "status_string",
+           "version"]

@@ -1,0 +1,226 @@
+"""ctypes binding of libattn.so (the C ABI in include/attn.h).
+
+Argument marshalling only: every step of the computation runs in the CUDA
+library.  PyTorch owns the device memory and the stream; tensors are passed by
+``data_ptr()`` and the current stream by handle.  If the compiled library is
+missing this module raises immediately -- there is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIBRARY_PATH = os.path.join(_PKG, "libattn.so")
+
+ATTN_OK = 0
+STATUS_NAMES = {0: "ATTN_OK", 1: "ATTN_ERR_INVALID_ARG", 2: "ATTN_ERR_UNSUPPORTED", 3: "ATTN_ERR_CUDA",
+                4: "ATTN_ERR_TIMEOUT", 5: "ATTN_ERR_WORKSPACE", 6: "ATTN_ERR_DEVICE_BOUNDS"}
+LAYOUTS = {"bshd": 0, "bhsd": 1}
+
+_lock = threading.Lock()
+_lib = None
+
+_p = ctypes.c_void_p
+_i = ctypes.c_int
+_f = ctypes.c_float
+_sz = ctypes.c_size_t
+_u64 = ctypes.c_uint64
+
+
+class AttnError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        self.code = code
+        super().__init__(f"{what}: {STATUS_NAMES.get(code, code)}")
+
+
+def load():
+    """Load libattn.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIBRARY_PATH):
+                raise RuntimeError(
+                    f"{LIBRARY_PATH} is missing: build the CUDA library first "
+                    "(python -c 'import __graft_entry__ as g; g.build()')")
+            lib = ctypes.CDLL(LIBRARY_PATH)
+            fwd_args = [_p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _i, _f, _p]
+            lib.attn_fwd.argtypes = fwd_args
+            lib.attn_fwd_simple.argtypes = fwd_args
+            lib.attn_decode_workspace_bytes.argtypes = [_i, _i, _i, _i]
+            lib.attn_decode_workspace_bytes.restype = _sz
+            lib.attn_decode_paged.argtypes = [_p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _f, _p,
+                                              _sz, _p]
+            lib.attn_lse_merge.argtypes = [_p, _p, _p, _p, _i, _i, _i, _p]
+            lib.attn_get_device_status.argtypes = [_p, ctypes.POINTER(_i)]
+            lib.attn_set_wait_budget_ns.argtypes = [_u64]
+            lib.attn_debug_inject.argtypes = [_i]
+            lib.attn_selftest_umma.argtypes = [_p, _p, _p, _i, _p]
+            lib.attn_status_string.argtypes = [_i]
+            lib.attn_status_string.restype = ctypes.c_char_p
+            lib.attn_version.restype = _i
+            for name in ("attn_fwd", "attn_fwd_simple", "attn_decode_paged", "attn_lse_merge",
+                         "attn_get_device_status", "attn_set_wait_budget_ns", "attn_debug_inject",
+                         "attn_selftest_umma"):
+                getattr(lib, name).restype = _i
+            _lib = lib
+    return _lib
+
+
+def _check(rc: int, what: str):
+    if rc != ATTN_OK:
+        raise AttnError(rc, what)
+
+
+def _stream(stream=None) -> int:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+def _dev_tensor(t: torch.Tensor, name: str, dtype):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _dims(q, k, layout):
+    if q.dim() != 4 or k.dim() != 4:
+        raise ValueError("q, k, v must be 4-D")
+    if layout == "bshd":
+        B, Sq, Hq, d = q.shape
+        _, Sk, Hkv, _ = k.shape
+    elif layout == "bhsd":
+        B, Hq, Sq, d = q.shape
+        _, Hkv, Sk, _ = k.shape
+    else:
+        raise ValueError(f"layout must be 'bshd' or 'bhsd', got {layout!r}")
+    return B, Hq, Hkv, Sq, Sk, d
+
+
+def _fwd_call(fn_name, q, k, v, causal, scale, layout, out, lse, stream):
+    lib = load()
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _dev_tensor(t, n, torch.bfloat16)
+    if k.shape != v.shape:
+        raise ValueError("k and v must have the same shape")
+    B, Hq, Hkv, Sq, Sk, d = _dims(q, k, layout)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, Hq, Sq), device=q.device, dtype=torch.float32)
+    elif lse is not False:
+        _dev_tensor(lse, "lse", torch.float32)
+    lse_ptr = None if lse is False else lse.data_ptr()
+    rc = getattr(lib, fn_name)(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse_ptr, B, Hq, Hkv, Sq,
+                               Sk, d, LAYOUTS[layout], int(bool(causal)), float(scale), _stream(stream))
+    _check(rc, fn_name)
+    return out, (None if lse is False else lse)
+
+
+def fwd(q, k, v, *, causal=False, scale=None, layout="bshd", out=None, lse=None, stream=None):
+    """Fused exact attention forward: returns (out bf16 in q's layout, lse fp32 [B, Hq, Sq]).
+
+    Pass ``lse=False`` to skip the log-sum-exp output.
+    """
+    return _fwd_call("attn_fwd", q, k, v, causal, scale, layout, out, lse, stream)
+
+
+def fwd_simple(q, k, v, *, causal=False, scale=None, layout="bshd", out=None, lse=None, stream=None):
+    """The same operation through the plain SIMT kernel (debugging cross-check; slow)."""
+    return _fwd_call("attn_fwd_simple", q, k, v, causal, scale, layout, out, lse, stream)
+
+
+def decode_workspace_bytes(B: int, Hq: int, d: int, max_blocks_per_seq: int) -> int:
+    return int(load().attn_decode_workspace_bytes(B, Hq, d, max_blocks_per_seq))
+
+
+def decode_paged(q, k_pages, v_pages, block_table, seqlens, *, scale=None, out=None, lse=None, workspace=None,
+                 stream=None):
+    """One decode step over a paged KV cache.
+
+    q [B, Hq, d] bf16; k_pages/v_pages [num_pages, 16, Hkv, d] bf16; block_table [B, max_blocks] int32;
+    seqlens [B] int32 (device).  Returns (out [B, Hq, d] bf16, lse [B, Hq] fp32).
+    """
+    lib = load()
+    _dev_tensor(q, "q", torch.bfloat16)
+    _dev_tensor(k_pages, "k_pages", torch.bfloat16)
+    _dev_tensor(v_pages, "v_pages", torch.bfloat16)
+    _dev_tensor(block_table, "block_table", torch.int32)
+    _dev_tensor(seqlens, "seqlens", torch.int32)
+    B, Hq, d = q.shape
+    num_pages, page_size, Hkv, _ = k_pages.shape
+    max_blocks = block_table.shape[1]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, Hq), device=q.device, dtype=torch.float32)
+    need = decode_workspace_bytes(B, Hq, d, max_blocks)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), device=q.device, dtype=torch.uint8)
+    lse_ptr = None if lse is False else lse.data_ptr()
+    rc = lib.attn_decode_paged(q.data_ptr(), k_pages.data_ptr(), v_pages.data_ptr(), block_table.data_ptr(),
+                               seqlens.data_ptr(), out.data_ptr(), lse_ptr, B, Hq, Hkv, d, page_size, num_pages,
+                               max_blocks, float(scale), workspace.data_ptr(), workspace.numel(),
+                               _stream(stream))
+    _check(rc, "attn_decode_paged")
+    return out, (None if lse is False else lse)
+
+
+def lse_merge(o_parts, lse_parts, *, out=None, lse=None, stream=None):
+    """Merge key-range partials: o_parts [rows, nsplit, d] fp32, lse_parts [rows, nsplit] fp32."""
+    lib = load()
+    _dev_tensor(o_parts, "o_parts", torch.float32)
+    _dev_tensor(lse_parts, "lse_parts", torch.float32)
+    rows, nsplit, d = o_parts.shape
+    if out is None:
+        out = torch.empty((rows, d), device=o_parts.device, dtype=torch.bfloat16)
+    if lse is None:
+        lse = torch.empty((rows,), device=o_parts.device, dtype=torch.float32)
+    rc = lib.attn_lse_merge(o_parts.data_ptr(), lse_parts.data_ptr(), out.data_ptr(), lse.data_ptr(), rows, nsplit,
+                            d, _stream(stream))
+    _check(rc, "attn_lse_merge")
+    return out, lse
+
+
+def device_status(stream=None):
+    """Synchronise the stream, read and clear the device status word: (code, site)."""
+    site = _i(0)
+    rc = load().attn_get_device_status(_stream(stream), ctypes.byref(site))
+    return rc, site.value
+
+
+def set_wait_budget_ns(ns: int):
+    _check(load().attn_set_wait_budget_ns(int(ns)), "attn_set_wait_budget_ns")
+
+
+def debug_inject(mode: int):
+    _check(load().attn_debug_inject(int(mode)), "attn_debug_inject")
+
+
+def selftest_umma(a, b, mode: int, stream=None):
+    """128x128x128 tensor-core layout check: mode 0 -> a @ b.T, mode 1 -> a @ b (fp32 [128, 128])."""
+    _dev_tensor(a, "a", torch.bfloat16)
+    _dev_tensor(b, "b", torch.bfloat16)
+    c = torch.empty((128, 128), device=a.device, dtype=torch.float32)
+    _check(load().attn_selftest_umma(a.data_ptr(), b.data_ptr(), c.data_ptr(), int(mode), _stream(stream)),
+           "attn_selftest_umma")
+    return c
+
+
+def status_string(code: int) -> str:
+    return load().attn_status_string(int(code)).decode()
+
+
+def version() -> int:
+    return int(load().attn_version())

@@ -1,0 +1,327 @@
+// api.cu -- the C ABI (include/attn.h): argument validation, TMA tensor-map
+// encoding, the per-device status word, and kernel launches on the caller's
+// stream.  Nothing here allocates device memory.
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include "attn.h"
+#include "prefill_tc.h"
+
+// Device status word: [0] = first error code recorded, [1] = wait/check site.
+__device__ unsigned int g_attn_status[2];
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr uint64_t kDefaultBudgetNs = 2000000000ull;
+
+struct DeviceInfo {
+    bool ready = false;
+    bool supported = false;
+    int sm_count = 0;
+    unsigned *status = nullptr;
+};
+
+std::mutex g_mu;
+DeviceInfo g_dev[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::atomic<uint64_t> g_budget{kDefaultBudgetNs};
+std::atomic<int> g_inject{0};
+
+attn_status_t device_info(DeviceInfo **out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ATTN_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_mu);
+    DeviceInfo &d = g_dev[dev];
+    if (!d.ready) {
+        int major = 0, minor = 0, sms = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return ATTN_ERR_CUDA;
+        // The kernels are built for sm_103a only.
+        d.supported = (major == 10 && minor == 3);
+        d.sm_count = sms;
+        if (d.supported) {
+            void *ptr = nullptr;
+            if (cudaGetSymbolAddress(&ptr, g_attn_status) != cudaSuccess) return ATTN_ERR_CUDA;
+            d.status = static_cast<unsigned *>(ptr);
+            if (cudaMemset(d.status, 0, 2 * sizeof(unsigned)) != cudaSuccess) return ATTN_ERR_CUDA;
+        }
+        if (!g_encode) {
+            void *fn = nullptr;
+            cudaDriverEntryPointQueryResult q;
+            if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+                    cudaSuccess ||
+                q != cudaDriverEntryPointSuccess || fn == nullptr)
+                return ATTN_ERR_CUDA;
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+        }
+        d.ready = true;
+    }
+    if (!d.supported) return ATTN_ERR_UNSUPPORTED;
+    *out = &d;
+    return ATTN_OK;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+uint64_t budget() { return g_budget.load(std::memory_order_relaxed); }
+
+// 4-D bf16 map over a dense BSHD ([B][S][H][d], dims {d,H,S,B}) or BHSD
+// ([B][H][S][d], dims {d,S,H,B}) tensor; box = 64 head-dim elements (128 B,
+// 128-byte swizzle) x `rows` sequence positions of one head.
+bool make_map_4d(CUtensorMap *m, const void *ptr, bool bhsd, int B, int S, int H, int d, int rows) {
+    const cuuint64_t e = 2;
+    cuuint64_t dims[4], strides[3];
+    cuuint32_t box[4];
+    if (bhsd) {
+        dims[0] = d; dims[1] = S; dims[2] = H; dims[3] = B;
+        strides[0] = (cuuint64_t)d * e;
+        strides[1] = (cuuint64_t)S * d * e;
+        strides[2] = (cuuint64_t)H * S * d * e;
+        box[0] = 64; box[1] = rows; box[2] = 1; box[3] = 1;
+    } else {
+        dims[0] = d; dims[1] = H; dims[2] = S; dims[3] = B;
+        strides[0] = (cuuint64_t)d * e;
+        strides[1] = (cuuint64_t)H * d * e;
+        strides[2] = (cuuint64_t)S * H * d * e;
+        box[0] = 64; box[1] = 1; box[2] = rows; box[3] = 1;
+    }
+    const cuuint32_t es[4] = {1, 1, 1, 1};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(ptr), dims, strides, box, es,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// 3-D map over a page pool [P][16][Hkv][d]: dims {d, Hkv, 16P}, box = one
+// page of one KV head (16 rows x 128 elements, 4 KiB, no swizzle).
+bool make_map_pool(CUtensorMap *m, const void *ptr, int num_pages, int Hkv, int d) {
+    const cuuint64_t e = 2;
+    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)Hkv, (cuuint64_t)num_pages * 16};
+    cuuint64_t strides[2] = {(cuuint64_t)d * e, (cuuint64_t)Hkv * d * e};
+    cuuint32_t box[3] = {(cuuint32_t)d, 1, 16};
+    const cuuint32_t es[3] = {1, 1, 1};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box, es,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+attn_status_t check_fwd_args(const void *q, const void *k, const void *v, const void *out, const float *lse,
+                             int B, int Hq, int Hkv, int Sq, int Sk, int d, int layout, float scale) {
+    if (!q || !k || !v || !out) return ATTN_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return ATTN_ERR_INVALID_ARG;
+    if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return ATTN_ERR_INVALID_ARG;
+    if (B < 1 || Hq < 1 || Hkv < 1 || Sq < 1 || Sk < 1) return ATTN_ERR_INVALID_ARG;
+    if (Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
+    if (layout != ATTN_LAYOUT_BSHD && layout != ATTN_LAYOUT_BHSD) return ATTN_ERR_INVALID_ARG;
+    if (!std::isfinite(scale) || scale < 0.f) return ATTN_ERR_INVALID_ARG;
+    if (d != 128) return ATTN_ERR_UNSUPPORTED;
+    // Tensor-map extents are 32-bit; element counts must fit the kernels' 64-bit indexing.
+    if ((int64_t)B * Sq * Hq > (int64_t)1 << 31 || (int64_t)B * Sk * Hkv > (int64_t)1 << 31)
+        return ATTN_ERR_INVALID_ARG;
+    return ATTN_OK;
+}
+
+attn_status_t fill_prefill_params(attn::PrefillParams *p, const DeviceInfo *di, float *lse, int B, int Hq,
+                                  int Hkv, int Sq, int Sk, int layout, int causal, float scale) {
+    p->B = B;
+    p->Hq = Hq;
+    p->Hkv = Hkv;
+    p->Sq = Sq;
+    p->Sk = Sk;
+    p->G = Hq / Hkv;
+    p->causal = causal ? 1 : 0;
+    p->bhsd = layout == ATTN_LAYOUT_BHSD ? 1 : 0;
+    p->scale_log2 = (float)((double)scale * 1.4426950408889634);
+    p->lse = lse;
+    p->n_m = (Sq + 127) / 128;
+    p->pair_heads = (p->G % 2 == 0) ? 1 : 0;
+    p->status = di->status;
+    p->budget_ns = budget();
+    p->inject = 0;
+    return ATTN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+attn_status_t attn_fwd(const void *q, const void *k, const void *v, void *out, float *lse, int B, int Hq, int Hkv,
+                       int Sq, int Sk, int d, int layout, int causal, float scale, void *stream) {
+    attn_status_t st = check_fwd_args(q, k, v, out, lse, B, Hq, Hkv, Sq, Sk, d, layout, scale);
+    if (st != ATTN_OK) return st;
+    DeviceInfo *di = nullptr;
+    if ((st = device_info(&di)) != ATTN_OK) return st;
+    attn::PrefillParams p;
+    fill_prefill_params(&p, di, lse, B, Hq, Hkv, Sq, Sk, layout, causal, scale);
+    p.inject = g_inject.exchange(0);
+    const bool bhsd = p.bhsd != 0;
+    CUtensorMap mq, mk, mv, mo;
+    if (!make_map_4d(&mq, q, bhsd, B, Sq, Hq, d, 128) || !make_map_4d(&mk, k, bhsd, B, Sk, Hkv, d, 128) ||
+        !make_map_4d(&mv, v, bhsd, B, Sk, Hkv, d, 128) || !make_map_4d(&mo, out, bhsd, B, Sq, Hq, d, 128))
+        return ATTN_ERR_CUDA;
+    const int units = attn::prefill_num_units(p);
+    if (attn::launch_prefill(mq, mk, mv, mo, p, units, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return ATTN_ERR_CUDA;
+    return ATTN_OK;
+}
+
+attn_status_t attn_fwd_simple(const void *q, const void *k, const void *v, void *out, float *lse, int B, int Hq,
+                              int Hkv, int Sq, int Sk, int d, int layout, int causal, float scale, void *stream) {
+    attn_status_t st = check_fwd_args(q, k, v, out, lse, B, Hq, Hkv, Sq, Sk, d, layout, scale);
+    if (st != ATTN_OK) return st;
+    DeviceInfo *di = nullptr;
+    if ((st = device_info(&di)) != ATTN_OK) return st;
+    if (B > 65535 || Hq > 65535) return ATTN_ERR_INVALID_ARG;
+    attn::PrefillParams p;
+    fill_prefill_params(&p, di, lse, B, Hq, Hkv, Sq, Sk, layout, causal, scale);
+    if (attn::launch_prefill_simple(q, k, v, out, lse, p, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return ATTN_ERR_CUDA;
+    return ATTN_OK;
+}
+
+size_t attn_decode_workspace_bytes(int B, int Hq, int d, int max_blocks_per_seq) {
+    if (B < 1 || Hq < 1 || d != 128 || max_blocks_per_seq < 1) return 0;
+    const int pps = attn::decode_pages_per_split();
+    const size_t nsplit = (size_t)((max_blocks_per_seq + pps - 1) / pps);
+    const size_t rows = (size_t)B * Hq;
+    // o_part [rows][nsplit][d] fp32, then lse_part [rows][nsplit] fp32, each 256-B aligned.
+    size_t o_bytes = rows * nsplit * d * 4;
+    o_bytes = (o_bytes + 255) & ~(size_t)255;
+    size_t l_bytes = rows * nsplit * 4;
+    l_bytes = (l_bytes + 255) & ~(size_t)255;
+    return o_bytes + l_bytes;
+}
+
+attn_status_t attn_decode_paged(const void *q, const void *k_pages, const void *v_pages,
+                                const int32_t *block_table, const int32_t *seqlens, void *out, float *lse, int B,
+                                int Hq, int Hkv, int d, int page_size, int num_pages, int max_blocks_per_seq,
+                                float scale, void *workspace, size_t workspace_bytes, void *stream) {
+    if (!q || !k_pages || !v_pages || !block_table || !seqlens || !out) return ATTN_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k_pages) || !aligned16(v_pages) || !aligned16(out)) return ATTN_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(block_table) & 3u) || (reinterpret_cast<uintptr_t>(seqlens) & 3u))
+        return ATTN_ERR_INVALID_ARG;
+    if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return ATTN_ERR_INVALID_ARG;
+    if (B < 1 || Hq < 1 || Hkv < 1 || num_pages < 1 || max_blocks_per_seq < 1) return ATTN_ERR_INVALID_ARG;
+    if (Hq % Hkv != 0 || B > 65535) return ATTN_ERR_INVALID_ARG;
+    if (!std::isfinite(scale) || scale < 0.f) return ATTN_ERR_INVALID_ARG;
+    if (d != 128 || page_size != 16) return ATTN_ERR_UNSUPPORTED;
+    if ((int64_t)num_pages * 16 > ((int64_t)1 << 31) - 1) return ATTN_ERR_INVALID_ARG;
+    const size_t need = attn_decode_workspace_bytes(B, Hq, d, max_blocks_per_seq);
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < need)
+        return ATTN_ERR_WORKSPACE;
+    attn_status_t st;
+    DeviceInfo *di = nullptr;
+    if ((st = device_info(&di)) != ATTN_OK) return st;
+    CUtensorMap mk, mv;
+    if (!make_map_pool(&mk, k_pages, num_pages, Hkv, d) || !make_map_pool(&mv, v_pages, num_pages, Hkv, d))
+        return ATTN_ERR_CUDA;
+    attn::DecodeParams p;
+    p.q = q;
+    p.block_table = block_table;
+    p.seqlens = seqlens;
+    p.out = out;
+    p.lse = lse;
+    p.pages_per_split = attn::decode_pages_per_split();
+    p.nsplit = (max_blocks_per_seq + p.pages_per_split - 1) / p.pages_per_split;
+    const size_t rows = (size_t)B * Hq;
+    size_t o_bytes = rows * p.nsplit * d * 4;
+    o_bytes = (o_bytes + 255) & ~(size_t)255;
+    p.o_part = static_cast<float *>(workspace);
+    p.lse_part = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + o_bytes);
+    p.B = B;
+    p.Hq = Hq;
+    p.Hkv = Hkv;
+    p.G = Hq / Hkv;
+    p.num_pages = num_pages;
+    p.max_blocks = max_blocks_per_seq;
+    p.scale_log2 = (float)((double)scale * 1.4426950408889634);
+    p.status = di->status;
+    p.budget_ns = budget();
+    if (attn::launch_decode(mk, mv, p, static_cast<cudaStream_t>(stream)) != cudaSuccess) return ATTN_ERR_CUDA;
+    return ATTN_OK;
+}
+
+attn_status_t attn_lse_merge(const float *o_parts, const float *lse_parts, void *out, float *lse, int rows,
+                             int nsplit, int d, void *stream) {
+    if (!o_parts || !lse_parts || !out) return ATTN_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(o_parts) & 3u) || (reinterpret_cast<uintptr_t>(lse_parts) & 3u) ||
+        !aligned16(out) || (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)))
+        return ATTN_ERR_INVALID_ARG;
+    if (rows < 1 || nsplit < 1) return ATTN_ERR_INVALID_ARG;
+    if (d != 128) return ATTN_ERR_UNSUPPORTED;
+    attn_status_t st;
+    DeviceInfo *di = nullptr;
+    if ((st = device_info(&di)) != ATTN_OK) return st;
+    if (attn::launch_lse_merge(o_parts, lse_parts, out, lse, rows, nsplit, static_cast<cudaStream_t>(stream)) !=
+        cudaSuccess)
+        return ATTN_ERR_CUDA;
+    return ATTN_OK;
+}
+
+attn_status_t attn_get_device_status(void *stream, int *site) {
+    DeviceInfo *di = nullptr;
+    attn_status_t st = device_info(&di);
+    if (st != ATTN_OK) return st;
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return ATTN_ERR_CUDA;
+    unsigned h[2] = {0, 0};
+    if (cudaMemcpy(h, di->status, sizeof h, cudaMemcpyDeviceToHost) != cudaSuccess) return ATTN_ERR_CUDA;
+    if (h[0] != 0 && cudaMemset(di->status, 0, sizeof h) != cudaSuccess) return ATTN_ERR_CUDA;
+    if (site) *site = (int)h[1];
+    return static_cast<attn_status_t>(h[0]);
+}
+
+attn_status_t attn_set_wait_budget_ns(uint64_t ns) {
+    g_budget.store(ns == 0 ? kDefaultBudgetNs : ns, std::memory_order_relaxed);
+    return ATTN_OK;
+}
+
+attn_status_t attn_debug_inject(int mode) {
+    if (mode < 0 || mode > 1) return ATTN_ERR_INVALID_ARG;
+    g_inject.store(mode);
+    return ATTN_OK;
+}
+
+attn_status_t attn_selftest_umma(const void *a, const void *b, float *c, int mode, void *stream) {
+    if (!a || !b || !c || !aligned16(a) || !aligned16(b) || !aligned16(c)) return ATTN_ERR_INVALID_ARG;
+    if (mode != 0 && mode != 1) return ATTN_ERR_INVALID_ARG;
+    attn_status_t st;
+    DeviceInfo *di = nullptr;
+    if ((st = device_info(&di)) != ATTN_OK) return st;
+    CUtensorMap ma, mb;
+    // Treat each [128][128] matrix as a one-head BSHD tensor with 128 rows.
+    if (!make_map_4d(&ma, a, false, 1, 128, 1, 128, 128) || !make_map_4d(&mb, b, false, 1, 128, 1, 128, 128))
+        return ATTN_ERR_CUDA;
+    if (attn::launch_selftest_umma(ma, mb, a, c, mode, di->status, budget(), static_cast<cudaStream_t>(stream)) !=
+        cudaSuccess)
+        return ATTN_ERR_CUDA;
+    return ATTN_OK;
+}
+
+const char *attn_status_string(attn_status_t s) {
+    switch (s) {
+        case ATTN_OK: return "ATTN_OK";
+        case ATTN_ERR_INVALID_ARG: return "ATTN_ERR_INVALID_ARG";
+        case ATTN_ERR_UNSUPPORTED: return "ATTN_ERR_UNSUPPORTED";
+        case ATTN_ERR_CUDA: return "ATTN_ERR_CUDA";
+        case ATTN_ERR_TIMEOUT: return "ATTN_ERR_TIMEOUT";
+        case ATTN_ERR_WORKSPACE: return "ATTN_ERR_WORKSPACE";
+        case ATTN_ERR_DEVICE_BOUNDS: return "ATTN_ERR_DEVICE_BOUNDS";
+    }
+    return "ATTN_ERR_UNKNOWN";
+}
+
+int attn_version(void) { return 100; }
+
+}  // extern "C"

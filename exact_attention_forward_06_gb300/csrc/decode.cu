@@ -1,0 +1,334 @@
+// decode.cu -- paged-KV decode split over the keys, and the log-sum-exp merge.
+//
+// The cache is the paged layout of the ROCm port page ("Vendor-Agnostic 多查询
+// 推理优化": 16-token pages, an int32 block_table per sequence); the split over
+// the keys with a merge of the partial results is the Flash-Decoding style
+// tail split of the MoonMath HIP kernel page.  Decode reads every K/V byte
+// once and does ~4 flops per byte, so it is bound by HBM bandwidth and runs on
+// the CUDA cores; the tensor cores would only add a reshape.
+//
+// Split kernel: one CTA per (split, group of up to 4 query heads sharing a KV
+// head, sequence).  A producer lane gathers the split's pages with one 3-D
+// TMA copy per page and tensor (the 16 rows of one KV head in a page are 2 KiB
+// apart in the pool) into an 8-page shared-memory ring.  Four consumer warps
+// take pages round-robin.  In a warp, lane (tg, ds) = (lane/8, lane%8) owns
+// head-dim slice [16 ds, 16 ds + 16) of tokens tg, tg+4, tg+8, tg+12 of the
+// page: dot products are reduced over the 8 lanes of a token with three
+// shuffles, the page max over the token groups with two more, and each warp
+// keeps its own running max / sum / accumulator (online softmax, with the max
+// moved only past a 2^8 growth).  At the end the four warps are merged in
+// shared memory and the split writes its normalised partial output and
+// log-sum-exp.  The merge kernel then combines the splits in a fixed order.
+#include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+#include "prefill_tc.h"
+
+namespace attn {
+namespace dec {
+
+constexpr int PAGE = 16;
+constexpr int D = 128;
+constexpr int NCW = 4;   // consumer warps
+constexpr int NST = 8;   // pages in flight per CTA
+constexpr int GH_MAX = 4;
+constexpr int NTHREADS = (NCW + 1) * 32;
+constexpr uint32_t PAGE_BYTES = PAGE * D * 2;        // one tensor, one KV head: 4 KiB
+constexpr uint32_t STAGE_BYTES = 2 * PAGE_BYTES;     // K + V
+constexpr uint32_t SMEM_STAGES = NST * STAGE_BYTES;  // 64 KiB
+constexpr uint32_t SMEM_MERGE = NCW * GH_MAX * (D + 2) * 4;
+constexpr uint32_t SMEM_MISC = 256;
+constexpr uint32_t SMEM_ALIGN = 1024;
+constexpr uint32_t SMEM_BYTES = SMEM_ALIGN + SMEM_STAGES + SMEM_MERGE + SMEM_MISC;
+constexpr int PAGES_PER_SPLIT = 32;
+constexpr float RESCALE_LOG2 = 8.0f;
+constexpr float LN2 = 0.6931471805599453f;
+constexpr float LOG2E = 1.4426950408889634f;
+
+__device__ __forceinline__ void bf16x8_to_float(const uint4 &u, float *x) {
+    x[0] = __uint_as_float(u.x << 16);
+    x[1] = __uint_as_float(u.x & 0xffff0000u);
+    x[2] = __uint_as_float(u.y << 16);
+    x[3] = __uint_as_float(u.y & 0xffff0000u);
+    x[4] = __uint_as_float(u.z << 16);
+    x[5] = __uint_as_float(u.z & 0xffff0000u);
+    x[6] = __uint_as_float(u.w << 16);
+    x[7] = __uint_as_float(u.w & 0xffff0000u);
+}
+
+template <int GH>
+__global__ void __launch_bounds__(NTHREADS)
+    split_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
+                 const DecodeParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = ptx::smem_addr(smem_raw);
+    uint8_t *base = smem_raw + ((SMEM_ALIGN - (raw & (SMEM_ALIGN - 1))) & (SMEM_ALIGN - 1));
+    float *merge = reinterpret_cast<float *>(base + SMEM_STAGES);
+    uint64_t *full = reinterpret_cast<uint64_t *>(base + SMEM_STAGES + SMEM_MERGE);
+    uint64_t *empty = full + NST;
+    int *stage_bad = reinterpret_cast<int *>(empty + NST);
+    volatile int *abort_flag = stage_bad + NST;
+
+    const int split = blockIdx.x;
+    const int h0 = blockIdx.y * GH;
+    const int b = blockIdx.z;
+    const int g = h0 / p.G;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    int L = p.seqlens[b];
+    L = max(0, min(L, p.max_blocks * PAGE));
+    const int npages = (L + PAGE - 1) / PAGE;
+    const int page0 = split * p.pages_per_split;
+    const int np = max(0, min(p.pages_per_split, npages - page0));
+    const int64_t row0 = (int64_t)b * p.Hq + h0;  // first (b, h) row of this CTA
+
+    if (np == 0) {  // nothing to attend to in this split
+        for (int i = threadIdx.x; i < GH * D; i += NTHREADS)
+            p.o_part[((row0 + i / D) * p.nsplit + split) * D + (i % D)] = 0.f;
+        if (threadIdx.x < GH) p.lse_part[(row0 + threadIdx.x) * p.nsplit + split] = -INFINITY;
+        return;
+    }
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < NST; ++s) {
+            ptx::mbar_init(full + s, 1);
+            ptx::mbar_init(empty + s, 1);
+            stage_bad[s] = 0;
+        }
+        *abort_flag = 0;
+        ptx::fence_mbar_init();
+    }
+    __syncthreads();
+    const WaitCtx wc{abort_flag, p.status, p.budget_ns};
+
+    if (warp == NCW) {
+        // ---------------- producer
+        if (lane == 0) {
+            ptx::prefetch_tensormap(&map_k);
+            ptx::prefetch_tensormap(&map_v);
+            const uint64_t pol = ptx::policy_evict_first();
+            int issued = 0;
+            for (int i = 0; i < np; ++i) {
+                const int slot = i % NST;
+                const int round = i / NST;
+                if (round > 0 && !wait_bounded(empty + slot, (round - 1) & 1, wc, kSiteDecodeEmpty)) break;
+                const int phys = p.block_table[(int64_t)b * p.max_blocks + page0 + i];
+                uint8_t *dst = base + slot * STAGE_BYTES;
+                if (phys < 0 || phys >= p.num_pages) {
+                    report_status(p.status, kStatusDeviceBounds, kSiteDecodeTable);
+                    stage_bad[slot] = 1;
+                    ptx::mbar_arrive(full + slot);
+                } else {
+                    stage_bad[slot] = 0;
+                    ptx::mbar_arrive_expect_tx(full + slot, STAGE_BYTES);
+                    ptx::tma_load_3d(dst, &map_k, full + slot, 0, g, phys * PAGE);
+                    ptx::tma_load_3d(dst + PAGE_BYTES, &map_v, full + slot, 0, g, phys * PAGE);
+                    (void)pol;
+                }
+                ++issued;
+            }
+            for (int i = max(0, issued - NST); i < issued; ++i) drain_wait(full + i % NST, (i / NST) & 1, wc);
+        }
+        __syncwarp();
+    } else {
+        // ---------------- consumers
+        const int tg = lane >> 3;  // token group
+        const int ds = lane & 7;   // 16-element head-dim slice
+        float qf[GH][16];
+#pragma unroll
+        for (int h = 0; h < GH; ++h) {
+            const uint4 *qp = reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(p.q) +
+                                                              (row0 + h) * D + ds * 16);
+            bf16x8_to_float(qp[0], qf[h]);
+            bf16x8_to_float(qp[1], qf[h] + 8);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) qf[h][e] *= p.scale_log2;
+        }
+        float m[GH], lsum[GH], acc[GH][16];
+#pragma unroll
+        for (int h = 0; h < GH; ++h) {
+            m[h] = -INFINITY;
+            lsum[h] = 0.f;
+#pragma unroll
+            for (int e = 0; e < 16; ++e) acc[h][e] = 0.f;
+        }
+        for (int i = warp; i < np; i += NCW) {
+            const int slot = i % NST;
+            if (!wait_bounded(full + slot, (i / NST) & 1, wc, kSiteDecodeFull)) break;
+            const uint8_t *ks = base + slot * STAGE_BYTES;
+            const uint8_t *vs = ks + PAGE_BYTES;
+            const bool bad = stage_bad[slot] != 0;
+            const int tok0 = (page0 + i) * PAGE;
+            float sc[4][GH];
+#pragma unroll
+            for (int ps = 0; ps < 4; ++ps) {
+                const int t = ps * 4 + tg;
+                const uint4 *kp = reinterpret_cast<const uint4 *>(ks + t * (D * 2) + ds * 32);
+                float kf[16];
+                bf16x8_to_float(kp[0], kf);
+                bf16x8_to_float(kp[1], kf + 8);
+#pragma unroll
+                for (int h = 0; h < GH; ++h) {
+                    float dot = 0.f;
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) dot = fmaf(qf[h][e], kf[e], dot);
+                    dot += __shfl_xor_sync(0xffffffffu, dot, 1);
+                    dot += __shfl_xor_sync(0xffffffffu, dot, 2);
+                    dot += __shfl_xor_sync(0xffffffffu, dot, 4);
+                    sc[ps][h] = (!bad && tok0 + t < L) ? dot : -INFINITY;
+                }
+            }
+            float pr[4][GH];
+#pragma unroll
+            for (int h = 0; h < GH; ++h) {
+                float pm = fmaxf(fmaxf(sc[0][h], sc[1][h]), fmaxf(sc[2][h], sc[3][h]));
+                pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 8));
+                pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 16));
+                if (pm > m[h] + RESCALE_LOG2) {  // warp-uniform
+                    const float alpha = ptx::ex2(m[h] - pm);
+                    lsum[h] *= alpha;
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) acc[h][e] *= alpha;
+                    m[h] = pm;
+                }
+                const float msub = (m[h] == -INFINITY) ? 0.f : m[h];
+#pragma unroll
+                for (int ps = 0; ps < 4; ++ps) {
+                    pr[ps][h] = (sc[ps][h] == -INFINITY) ? 0.f : ptx::ex2(sc[ps][h] - msub);
+                    lsum[h] += pr[ps][h];
+                }
+            }
+#pragma unroll
+            for (int ps = 0; ps < 4; ++ps) {
+                const int t = ps * 4 + tg;
+                const uint4 *vp = reinterpret_cast<const uint4 *>(vs + t * (D * 2) + ds * 32);
+                float vf[16];
+                bf16x8_to_float(vp[0], vf);
+                bf16x8_to_float(vp[1], vf + 8);
+#pragma unroll
+                for (int h = 0; h < GH; ++h)
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) acc[h][e] = fmaf(pr[ps][h], vf[e], acc[h][e]);
+            }
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(empty + slot);
+        }
+        // Sum the four token groups (lanes 8 and 16 apart share a slice).
+#pragma unroll
+        for (int h = 0; h < GH; ++h) {
+            lsum[h] += __shfl_xor_sync(0xffffffffu, lsum[h], 8);
+            lsum[h] += __shfl_xor_sync(0xffffffffu, lsum[h], 16);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+                acc[h][e] += __shfl_xor_sync(0xffffffffu, acc[h][e], 8);
+                acc[h][e] += __shfl_xor_sync(0xffffffffu, acc[h][e], 16);
+            }
+        }
+        float *mw = merge + (warp * GH_MAX) * (D + 2);
+#pragma unroll
+        for (int h = 0; h < GH; ++h) {
+            float *row = mw + h * (D + 2);
+            if (tg == 0) {
+#pragma unroll
+                for (int e = 0; e < 16; ++e) row[ds * 16 + e] = acc[h][e];
+            }
+            if (lane == 0) {
+                row[D] = m[h];
+                row[D + 1] = lsum[h];
+            }
+        }
+    }
+    __syncthreads();
+    if (*abort_flag) return;
+    // Merge the four warps: thread = head-dim element, loop over heads.
+    if (threadIdx.x < D) {
+        const int e = threadIdx.x;
+#pragma unroll
+        for (int h = 0; h < GH; ++h) {
+            float M = -INFINITY;
+#pragma unroll
+            for (int w = 0; w < NCW; ++w) M = fmaxf(M, merge[(w * GH_MAX + h) * (D + 2) + D]);
+            float Ls = 0.f, o = 0.f;
+            if (M != -INFINITY) {
+#pragma unroll
+                for (int w = 0; w < NCW; ++w) {
+                    const float *row = merge + (w * GH_MAX + h) * (D + 2);
+                    const float f = ptx::ex2(row[D] - M);  // -inf -> 0
+                    Ls += row[D + 1] * f;
+                    o += row[e] * f;
+                }
+            }
+            const int64_t r = row0 + h;
+            p.o_part[(r * p.nsplit + split) * D + e] = Ls > 0.f ? o / Ls : 0.f;
+            if (e == 0) p.lse_part[r * p.nsplit + split] = Ls > 0.f ? (M + ptx::lg2(Ls)) * LN2 : -INFINITY;
+        }
+    }
+}
+
+// One CTA per row, one thread per head-dim element; splits merged in order.
+__global__ void __launch_bounds__(D) merge_kernel(const float *__restrict__ o_parts,
+                                                  const float *__restrict__ lse_parts,
+                                                  __nv_bfloat16 *__restrict__ out, float *__restrict__ lse,
+                                                  int nsplit) {
+    const int64_t r = blockIdx.x;
+    const int e = threadIdx.x;
+    const float *ls = lse_parts + r * nsplit;
+    float M = -INFINITY;
+    for (int s = 0; s < nsplit; ++s) M = fmaxf(M, ls[s]);
+    float total = 0.f, o = 0.f;
+    if (M != -INFINITY) {
+        for (int s = 0; s < nsplit; ++s) {
+            const float w = ptx::ex2((ls[s] - M) * LOG2E);
+            total += w;
+            o = fmaf(w, o_parts[(r * nsplit + s) * D + e], o);
+        }
+    }
+    out[r * D + e] = __float2bfloat16_rn(total > 0.f ? o / total : 0.f);
+    if (e == 0 && lse != nullptr) lse[r] = total > 0.f ? M + ptx::lg2(total) * LN2 : -INFINITY;
+}
+
+}  // namespace dec
+
+int decode_pages_per_split() { return dec::PAGES_PER_SPLIT; }
+
+cudaError_t launch_decode(const CUtensorMap &mk, const CUtensorMap &mv, const DecodeParams &p,
+                          cudaStream_t stream) {
+    // Heads per CTA: the largest of 4, 2, 1 dividing the group size.
+    const int GH = (p.G % 4 == 0) ? 4 : (p.G % 2 == 0) ? 2 : 1;
+    dim3 grid(p.nsplit, p.Hq / GH, p.B);
+    const int smem = (int)dec::SMEM_BYTES;
+    static thread_local int configured_device = -1;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (configured_device != dev) {
+        e = cudaFuncSetAttribute(dec::split_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(dec::split_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(dec::split_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        configured_device = dev;
+    }
+    if (GH == 4)
+        dec::split_kernel<4><<<grid, dec::NTHREADS, smem, stream>>>(mk, mv, p);
+    else if (GH == 2)
+        dec::split_kernel<2><<<grid, dec::NTHREADS, smem, stream>>>(mk, mv, p);
+    else
+        dec::split_kernel<1><<<grid, dec::NTHREADS, smem, stream>>>(mk, mv, p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    return launch_lse_merge(p.o_part, p.lse_part, p.out, p.lse, p.B * p.Hq, p.nsplit, stream);
+}
+
+cudaError_t launch_lse_merge(const float *o_parts, const float *lse_parts, void *out, float *lse, int rows,
+                             int nsplit, cudaStream_t stream) {
+    dec::merge_kernel<<<rows, dec::D, 0, stream>>>(o_parts, lse_parts, static_cast<__nv_bfloat16 *>(out), lse,
+                                                   nsplit);
+    return cudaGetLastError();
+}
+
+}  // namespace attn

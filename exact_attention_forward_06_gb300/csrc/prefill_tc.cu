@@ -1,0 +1,510 @@
+// prefill_tc.cu -- fused exact attention forward on sm_103a tensor cores.
+//
+// O = softmax(Q K^T * scale [+ causal mask]) V and the per-row log-sum-exp,
+// with the IO-aware tiling of "FlashAttention-4 中的 IO 感知块分块策略": Q is cut
+// into 128-row blocks, K/V stream through shared memory in 128-key tiles, and
+// each row keeps a running max m and running sum l (m' = max(m, m_new),
+// l' = l exp(m - m') + l_new) while the output accumulator is rescaled, so the
+// Sq x Sk score matrix never reaches HBM.  Tiles entirely above the causal
+// diagonal are never loaded or computed (the upper-triangle skip of the
+// reverse-engineering page, 观点一).
+//
+// One CTA owns two 128-row Q tiles ("units" of 256 rows: two heads of one KV
+// group at the same positions when the group size is even, else two adjacent
+// position blocks of one head), so every K/V tile that is loaded serves 256
+// query rows.  Warp roles (320 threads):
+//   warp 0      TMA producer: Q tiles once, then K_j / V_j into a 5-slot ring
+//               of 32 KiB slots (full/empty mbarrier pairs);
+//   warp 1      TMEM allocator and single-thread tcgen05 MMA issuer;
+//   warps 2-5   softmax warpgroup for Q tile 0 (one thread per row);
+//   warps 6-9   softmax warpgroup for Q tile 1.
+// Tensor memory (512 columns): S_t at column 256t, O_t at 256t + 128; the
+// bf16 probabilities P_t overwrite the first 64 columns of S_t and feed the
+// P V product straight from tensor memory.  The MMA thread interleaves the
+// two tiles' chains S_t(j) -> softmax_t(j) -> PV_t(j) -> S_t(j+1) and issues
+// whichever chain is ready, so one tile's softmax runs while the tensor core
+// works on the other tile (the two-group alternation of the MoonMath page,
+// realised as two Q tiles instead of two wave groups).
+//
+// Softmax: scores are scaled into the log2 domain (scale * log2 e folded into
+// one FFMA) and exponentiated with ex2.approx.  A row's running max is only
+// moved (and O rescaled) when the new tile's max exceeds it by more than
+// 2^8; otherwise the stale max is kept, which is exact because m and l stay
+// consistent and P <= 256 is representable.  The rescale, when needed, is done
+// by the softmax warp itself on its own 32 rows of O in tensor memory, after
+// the previous P V product has completed.
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+#include "prefill_tc.h"
+
+namespace attn {
+namespace g1 {
+
+constexpr int BM = 128;          // rows per Q tile
+constexpr int BN = 128;          // keys per K/V tile
+constexpr int D = 128;           // head dim
+constexpr int NSLOT = 5;         // K/V ring slots
+constexpr uint32_t TILE_BYTES = BM * D * 2;  // 32 KiB (128 rows x 256 B)
+constexpr uint32_t HALF_BYTES = TILE_BYTES / 2;  // one 64-column half (128 B rows, 128-B swizzle)
+constexpr int NUM_THREADS = 320;
+constexpr uint32_t SMEM_Q0 = 0;
+constexpr uint32_t SMEM_Q1 = TILE_BYTES;
+constexpr uint32_t SMEM_SLOTS = 2 * TILE_BYTES;
+constexpr uint32_t SMEM_TILES = SMEM_SLOTS + NSLOT * TILE_BYTES;
+constexpr int NBARS = 1 + 2 * NSLOT + 2 + 2 + 2 + 1;
+constexpr uint32_t SMEM_MISC = 256;
+constexpr uint32_t SMEM_ALIGN = 1024;
+constexpr float RESCALE_LOG2 = 8.0f;  // move the running max only past a 2^8 growth
+constexpr float LN2 = 0.6931471805599453f;
+
+static_assert(NBARS * 8 + 16 <= SMEM_MISC, "barrier area too small");
+
+constexpr uint32_t IDESC_S = ptx::idesc_bf16_f32(128, 128, 0, 0);   // Q K^T: both K-major
+constexpr uint32_t IDESC_PV = ptx::idesc_bf16_f32(128, 128, 0, 1);  // P V: V is N(d)-major
+
+struct SmemLayout {
+    uint8_t *base;
+    uint64_t *bars;
+    __device__ uint64_t *q_full() const { return bars; }
+    __device__ uint64_t *kv_full(int s) const { return bars + 1 + s; }
+    __device__ uint64_t *kv_empty(int s) const { return bars + 1 + NSLOT + s; }
+    __device__ uint64_t *s_full(int t) const { return bars + 1 + 2 * NSLOT + t; }
+    __device__ uint64_t *p_full(int t) const { return bars + 3 + 2 * NSLOT + t; }
+    __device__ uint64_t *o_full(int t) const { return bars + 5 + 2 * NSLOT + t; }
+    __device__ uint64_t *fin() const { return bars + 7 + 2 * NSLOT; }
+    __device__ uint32_t *tmem_slot() const { return reinterpret_cast<uint32_t *>(bars + NBARS); }
+    __device__ volatile int *abort_flag() const { return reinterpret_cast<volatile int *>(bars + NBARS) + 1; }
+    __device__ uint8_t *q_tile(int t) const { return base + (t ? SMEM_Q1 : SMEM_Q0); }
+    __device__ uint8_t *slot(int s) const { return base + SMEM_SLOTS + s * TILE_BYTES; }
+};
+
+// Which two (head, first row) tiles a unit covers, and its K/V tile count.
+struct Unit {
+    int b, g;
+    int h[2];
+    int s0[2];
+    int n_kv;
+};
+
+__device__ __forceinline__ Unit decode_unit(const PrefillParams &p, int u) {
+    Unit w;
+    int m_step;
+    if (p.pair_heads) {
+        const int per = p.B * p.Hkv * (p.G / 2);
+        m_step = u / per;
+        int r = u % per;
+        w.b = r / (p.Hkv * (p.G / 2));
+        r %= p.Hkv * (p.G / 2);
+        w.g = r / (p.G / 2);
+        const int pr = r % (p.G / 2);
+        const int mb = p.causal ? (p.n_m - 1 - m_step) : m_step;  // causal: longest units first
+        w.h[0] = w.g * p.G + 2 * pr;
+        w.h[1] = w.h[0] + 1;
+        w.s0[0] = w.s0[1] = mb * BM;
+    } else {
+        const int per = p.B * p.Hq;
+        m_step = u / per;
+        const int r = u % per;
+        w.b = r / p.Hq;
+        const int h = r % p.Hq;
+        w.g = h / p.G;
+        const int n_mp = (p.n_m + 1) / 2;
+        const int mp = p.causal ? (n_mp - 1 - m_step) : m_step;
+        w.h[0] = w.h[1] = h;
+        w.s0[0] = mp * 2 * BM;
+        w.s0[1] = mp * 2 * BM + BM;
+    }
+    const int n_full = (p.Sk + BN - 1) / BN;
+    if (p.causal) {
+        int last_row = w.s0[0] + BM - 1;
+        if (w.s0[1] < p.Sq) last_row = max(last_row, w.s0[1] + BM - 1);
+        last_row = min(last_row, p.Sq - 1);
+        const int lim = last_row + p.Sk - p.Sq;  // last visible key of the lowest row
+        w.n_kv = lim < 0 ? 0 : min(n_full, lim / BN + 1);
+    } else {
+        w.n_kv = n_full;
+    }
+    return w;
+}
+
+// ------------------------------------------------------------------ producer
+
+__device__ __forceinline__ void load_tile(const CUtensorMap *map, uint8_t *dst, uint64_t *bar, bool bhsd, int h,
+                                          int s, int b, uint64_t pol) {
+    const Coord4 lo = coord4(bhsd, 0, h, s, b);
+    const Coord4 hi = coord4(bhsd, 64, h, s, b);
+    ptx::tma_load_4d(dst, map, bar, lo.c0, lo.c1, lo.c2, lo.c3, pol);
+    ptx::tma_load_4d(dst + HALF_BYTES, map, bar, hi.c0, hi.c1, hi.c2, hi.c3, pol);
+}
+
+__device__ void producer(const PrefillParams &p, const Unit &w, const SmemLayout &sm, const WaitCtx &wc,
+                         const CUtensorMap *mq, const CUtensorMap *mk, const CUtensorMap *mv) {
+    if (p.inject == 1) return;  // fault injection: issue nothing
+    const uint64_t pol_q = ptx::policy_evict_first();
+    const uint64_t pol_kv = ptx::policy_evict_last();
+    ptx::mbar_arrive_expect_tx(sm.q_full(), 2 * TILE_BYTES);
+    load_tile(mq, sm.q_tile(0), sm.q_full(), p.bhsd, w.h[0], w.s0[0], w.b, pol_q);
+    load_tile(mq, sm.q_tile(1), sm.q_full(), p.bhsd, w.h[1], w.s0[1], w.b, pol_q);
+    const int total = 2 * w.n_kv;
+    int issued = 0;
+    for (int n = 0; n < total; ++n) {
+        const int slot = n % NSLOT;
+        const int round = n / NSLOT;
+        if (round > 0 && !wait_bounded(sm.kv_empty(slot), (round - 1) & 1, wc, kSiteProducerEmpty)) break;
+        ptx::mbar_arrive_expect_tx(sm.kv_full(slot), TILE_BYTES);
+        load_tile((n & 1) ? mv : mk, sm.slot(slot), sm.kv_full(slot), p.bhsd, w.g, (n >> 1) * BN, w.b, pol_kv);
+        ++issued;
+    }
+    // On the way out make sure no copy is still writing into shared memory.
+    drain_wait(sm.q_full(), 0, wc);
+    for (int n = max(0, issued - NSLOT); n < issued; ++n) drain_wait(sm.kv_full(n % NSLOT), (n / NSLOT) & 1, wc);
+}
+
+// ------------------------------------------------------------------ MMA issuer
+
+__device__ __forceinline__ void issue_s(uint32_t tmem_s, uint32_t q_addr, uint32_t k_addr) {
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t off = (kk >> 2) * HALF_BYTES + (kk & 3) * 32;
+        ptx::umma_ss(tmem_s, ptx::desc_kmajor_sw128(q_addr + off), ptx::desc_kmajor_sw128(k_addr + off), IDESC_S,
+                     kk > 0);
+    }
+}
+
+__device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t tmem_p, uint32_t v_addr, bool accumulate) {
+#pragma unroll
+    for (int kk = 0; kk < BN / 16; ++kk) {
+        // 16 keys per step: 8 packed bf16x2 columns of P, 16 rows (2 x 1024-B atoms) of V.
+        ptx::umma_ts(tmem_o, tmem_p + kk * 8, ptx::desc_mnmajor_sw128(v_addr + kk * 2048, HALF_BYTES), IDESC_PV,
+                     (accumulate || kk > 0) ? 1u : 0u);
+    }
+}
+
+__device__ void mma_issuer(const Unit &w, const SmemLayout &sm, const WaitCtx &wc, uint32_t tmem_base) {
+    if (!wait_bounded(sm.q_full(), 0, wc, kSiteMmaQ)) return;
+    ptx::tc_fence_after();
+    const uint32_t q_addr[2] = {ptx::smem_addr(sm.q_tile(0)), ptx::smem_addr(sm.q_tile(1))};
+    const int total = 2 * w.n_kv;
+    int step[2] = {0, 0};
+    int krel = 0, vrel = 0;
+    uint32_t idle = 0;
+    uint64_t t_idle = 0;
+    while (step[0] < total || step[1] < total) {
+        bool progressed = false;
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+            const int st = step[t];
+            if (st >= total) continue;
+            const int j = st >> 1;
+            const int n = (st & 1) ? 2 * j + 1 : 2 * j;
+            const int slot = n % NSLOT;
+            const uint32_t par = (n / NSLOT) & 1;
+            const uint32_t tmem_s = tmem_base + t * 256;
+            if ((st & 1) == 0) {
+                // S_t(j) = Q_t K_j^T: needs K_j and the completion of PV_t(j-1),
+                // whose P operand lives in the columns S_t(j) overwrites.
+                if (!ptx::mbar_test(sm.kv_full(slot), par)) continue;
+                if (j > 0 && !ptx::mbar_test(sm.o_full(t), (j - 1) & 1)) continue;
+                ptx::tc_fence_after();
+                issue_s(tmem_s, q_addr[t], ptx::smem_addr(sm.slot(slot)));
+                ptx::umma_commit(sm.s_full(t));
+            } else {
+                // O_t += P_t(j) V_j: needs the softmax's P_t(j) and V_j.
+                if (!ptx::mbar_test(sm.p_full(t), j & 1)) continue;
+                if (!ptx::mbar_test(sm.kv_full(slot), par)) continue;
+                ptx::tc_fence_after();
+                issue_pv(tmem_s + 128, tmem_s, ptx::smem_addr(sm.slot(slot)), j > 0);
+                ptx::umma_commit(sm.o_full(t));
+            }
+            step[t] = st + 1;
+            progressed = true;
+            // Release a ring slot once both chains have issued every product reading it.
+            const int mn = min(step[0], step[1]);
+            while (krel < w.n_kv && mn > 2 * krel) {
+                ptx::umma_commit(sm.kv_empty((2 * krel) % NSLOT));
+                ++krel;
+            }
+            while (vrel < w.n_kv && mn > 2 * vrel + 1) {
+                ptx::umma_commit(sm.kv_empty((2 * vrel + 1) % NSLOT));
+                ++vrel;
+            }
+        }
+        if (progressed) {
+            idle = 0;
+            continue;
+        }
+        if (idle == 0) t_idle = ptx::globaltimer();
+        ++idle;
+        if ((idle & 63u) == 0) {
+            if (*wc.abort_flag) return;
+            if (ptx::globaltimer() - t_idle > wc.budget_ns) {
+                *wc.abort_flag = 1;
+                report_status(wc.status, kStatusTimeout, kSiteMmaPoll);
+                return;
+            }
+        }
+    }
+}
+
+// ------------------------------------------------------------------ softmax / epilogue
+
+template <bool MASKED>
+__device__ __forceinline__ float softmax_tile(float (&s)[128], uint32_t (&pk)[64], float scale_log2, float m_sub,
+                                              int kbase, int lim_row) {
+    float rowsum = 0.f;
+#pragma unroll
+    for (int c = 0; c < 128; c += 2) {
+        float p0 = ptx::ex2(fmaf(s[c], scale_log2, -m_sub));
+        float p1 = ptx::ex2(fmaf(s[c + 1], scale_log2, -m_sub));
+        if (MASKED) {
+            p0 = (kbase + c <= lim_row) ? p0 : 0.f;
+            p1 = (kbase + c + 1 <= lim_row) ? p1 : 0.f;
+        }
+        rowsum += p0;
+        rowsum += p1;
+        pk[c >> 1] = ptx::pack_bf16x2(p0, p1);
+    }
+    return rowsum;
+}
+
+__device__ void softmax_wg(const PrefillParams &p, const Unit &w, const SmemLayout &sm, const WaitCtx &wc,
+                           uint32_t tmem_base, int t, int quarter, int lane, const CUtensorMap *mo) {
+    const int r = quarter * 32 + lane;  // row within the tile == TMEM lane
+    const uint32_t tS = tmem_base + ((uint32_t)(quarter * 32) << 16) + t * 256;
+    const uint32_t tO = tS + 128;
+    const int s0 = w.s0[t];
+    const int lim_row = p.causal ? min(s0 + r + p.Sk - p.Sq, p.Sk - 1) : p.Sk - 1;
+    const int lim_tile = p.causal ? min(s0 + p.Sk - p.Sq, p.Sk - 1) : p.Sk - 1;
+    const float sl2 = p.scale_log2;
+    float m_run = -INFINITY, l_run = 0.f;
+    bool ok = true;
+
+    for (int j = 0; j < w.n_kv; ++j) {
+        if (!wait_bounded(sm.s_full(t), j & 1, wc, kSiteSoftmaxS)) {
+            ok = false;
+            break;
+        }
+        ptx::tc_fence_after();
+        float s[128];
+        {
+            uint32_t a[32], b[32], c[32], d[32];
+            ptx::tmem_ld32(tS + 0, a);
+            ptx::tmem_ld32(tS + 32, b);
+            ptx::tmem_ld32(tS + 64, c);
+            ptx::tmem_ld32(tS + 96, d);
+            ptx::tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                s[i] = __uint_as_float(a[i]);
+                s[32 + i] = __uint_as_float(b[i]);
+                s[64 + i] = __uint_as_float(c[i]);
+                s[96 + i] = __uint_as_float(d[i]);
+            }
+        }
+        const int kbase = j * BN;
+        const bool masked = kbase + BN - 1 > lim_tile;
+        float mx = -INFINITY;
+        if (masked) {
+#pragma unroll
+            for (int c = 0; c < 128; ++c) mx = (kbase + c <= lim_row) ? fmaxf(mx, s[c]) : mx;
+        } else {
+#pragma unroll
+            for (int c = 0; c < 128; ++c) mx = fmaxf(mx, s[c]);
+        }
+        const float m_tile = (mx == -INFINITY) ? -INFINITY : mx * sl2;
+        bool need = false;
+        float m_new = m_tile;
+        if (j > 0) {
+            need = m_tile > m_run + RESCALE_LOG2;
+            m_new = need ? m_tile : m_run;
+        }
+        const float alpha = need ? ptx::ex2(m_run - m_new) : 1.f;
+        const float m_sub = (m_new == -INFINITY) ? 0.f : m_new;
+        uint32_t pk[64];
+        const float rowsum = masked ? softmax_tile<true>(s, pk, sl2, m_sub, kbase, lim_row)
+                                    : softmax_tile<false>(s, pk, sl2, m_sub, kbase, lim_row);
+        {
+            uint32_t lo[32], hi[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                lo[i] = pk[i];
+                hi[i] = pk[32 + i];
+            }
+            ptx::tmem_st32(tS + 0, lo);
+            ptx::tmem_st32(tS + 32, hi);
+        }
+        ptx::tmem_wait_st();
+        if (j > 0 && __any_sync(0xffffffffu, need)) {
+            // O still holds the sum over tiles < j scaled by the old max: wait
+            // for PV_t(j-1) and rescale this warp's 32 rows in place.
+            if (!wait_bounded(sm.o_full(t), (j - 1) & 1, wc, kSiteSoftmaxO)) {
+                ok = false;
+                break;
+            }
+            ptx::tc_fence_after();
+#pragma unroll 1
+            for (int ch = 0; ch < 4; ++ch) {
+                uint32_t o[32];
+                ptx::tmem_ld32(tO + ch * 32, o);
+                ptx::tmem_wait_ld();
+#pragma unroll
+                for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                ptx::tmem_st32(tO + ch * 32, o);
+            }
+            ptx::tmem_wait_st();
+        }
+        l_run = l_run * alpha + rowsum;
+        m_run = m_new;
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(sm.p_full(t));
+    }
+
+    // Epilogue: O / l -> bf16 into the (now free) Q tile buffer, then TMA store.
+    // Every warp of the group reaches the named barrier exactly once, whether
+    // or not it gave up on a wait, so the barrier itself can never hang; a warp
+    // that gave up has raised the abort flag before arriving, and the leader
+    // checks it after the barrier.
+    if (ok && w.n_kv > 0) ok = wait_bounded(sm.o_full(t), (w.n_kv - 1) & 1, wc, kSiteEpilogueO);
+    uint8_t *stage = sm.q_tile(t);
+    if (ok) {
+        ptx::tc_fence_after();
+        const float inv = l_run > 0.f ? 1.0f / l_run : 0.f;
+#pragma unroll 1
+        for (int ch = 0; ch < 4; ++ch) {
+            uint32_t o[32];
+            ptx::tmem_ld32(tO + ch * 32, o);
+            ptx::tmem_wait_ld();
+            uint32_t wv[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const float x0 = l_run > 0.f ? __uint_as_float(o[2 * i]) * inv : 0.f;
+                const float x1 = l_run > 0.f ? __uint_as_float(o[2 * i + 1]) * inv : 0.f;
+                wv[i] = ptx::pack_bf16x2(x0, x1);
+            }
+            // 32 columns = 64 bytes = four 16-byte chunks of the 128-B swizzled row.
+            uint8_t *rowp = stage + (ch >> 1) * HALF_BYTES + r * 128;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int cc = (ch & 1) * 4 + k;
+                *reinterpret_cast<uint4 *>(rowp + ((cc ^ (r & 7)) << 4)) =
+                    make_uint4(wv[4 * k], wv[4 * k + 1], wv[4 * k + 2], wv[4 * k + 3]);
+            }
+        }
+        const int srow = s0 + r;
+        if (p.lse != nullptr && srow < p.Sq) {
+            const float lse = l_run > 0.f ? (m_run + ptx::lg2(l_run)) * LN2 : -INFINITY;
+            p.lse[((int64_t)w.b * p.Hq + w.h[t]) * p.Sq + srow] = lse;
+        }
+    }
+    ptx::fence_proxy_async_smem();
+    ptx::named_bar_sync(1 + t, 128);
+    if (quarter == 0 && lane == 0 && s0 < p.Sq && !*wc.abort_flag) {
+        const Coord4 lo = coord4(p.bhsd, 0, w.h[t], s0, w.b);
+        const Coord4 hi = coord4(p.bhsd, 64, w.h[t], s0, w.b);
+        ptx::tma_store_4d(mo, stage, lo.c0, lo.c1, lo.c2, lo.c3);
+        ptx::tma_store_4d(mo, stage + HALF_BYTES, hi.c0, hi.c1, hi.c2, hi.c3);
+        ptx::bulk_commit_group();
+        ptx::bulk_wait_group_read0();
+    }
+}
+
+// ------------------------------------------------------------------ kernel
+
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    prefill_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
+                   const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_o,
+                   const PrefillParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = ptx::smem_addr(smem_raw);
+    SmemLayout sm;
+    sm.base = smem_raw + ((SMEM_ALIGN - (raw & (SMEM_ALIGN - 1))) & (SMEM_ALIGN - 1));
+    sm.bars = reinterpret_cast<uint64_t *>(sm.base + SMEM_TILES);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const Unit w = decode_unit(p, blockIdx.x);
+
+    if (threadIdx.x == 0) {
+        ptx::mbar_init(sm.q_full(), 1);
+        for (int s = 0; s < NSLOT; ++s) {
+            ptx::mbar_init(sm.kv_full(s), 1);
+            ptx::mbar_init(sm.kv_empty(s), 1);
+        }
+        for (int t = 0; t < 2; ++t) {
+            ptx::mbar_init(sm.s_full(t), 1);
+            ptx::mbar_init(sm.p_full(t), 128);
+            ptx::mbar_init(sm.o_full(t), 1);
+        }
+        ptx::mbar_init(sm.fin(), 1);
+        *sm.abort_flag() = 0;
+        ptx::fence_mbar_init();
+        ptx::prefetch_tensormap(&map_q);
+        ptx::prefetch_tensormap(&map_k);
+        ptx::prefetch_tensormap(&map_v);
+        ptx::prefetch_tensormap(&map_o);
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc(sm.tmem_slot(), 512);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem_base = *sm.tmem_slot();
+    const WaitCtx wc{sm.abort_flag(), p.status, p.budget_ns};
+
+    if (warp == 0) {
+        if (lane == 0) producer(p, w, sm, wc, &map_q, &map_k, &map_v);
+        __syncwarp();
+    } else if (warp == 1) {
+        if (lane == 0) {
+            mma_issuer(w, sm, wc, tmem_base);
+            // Whatever happened, wait until every product issued has completed
+            // before tensor memory is released.
+            ptx::umma_commit(sm.fin());
+            drain_wait(sm.fin(), 0, wc);
+        }
+        __syncwarp();
+    } else {
+        const int t = (warp - 2) >> 2;
+        softmax_wg(p, w, sm, wc, tmem_base, t, warp & 3, lane, &map_o);
+        __syncwarp();
+    }
+
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem_base, 512);
+    }
+}
+
+}  // namespace g1
+
+int prefill_smem_bytes() { return (int)(g1::SMEM_TILES + g1::SMEM_MISC + g1::SMEM_ALIGN); }
+
+cudaError_t launch_prefill(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
+                           const CUtensorMap &mo, const PrefillParams &p, int num_units, cudaStream_t stream) {
+    const int smem = prefill_smem_bytes();
+    static thread_local int configured_device = -1;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (configured_device != dev) {
+        e = cudaFuncSetAttribute(g1::prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        configured_device = dev;
+    }
+    g1::prefill_kernel<<<num_units, g1::NUM_THREADS, smem, stream>>>(mq, mk, mv, mo, p);
+    return cudaGetLastError();
+}
+
+int prefill_num_units(const PrefillParams &p) {
+    if (p.pair_heads) return p.B * p.Hkv * (p.G / 2) * p.n_m;
+    return p.B * p.Hq * ((p.n_m + 1) / 2);
+}
+
+}  // namespace attn

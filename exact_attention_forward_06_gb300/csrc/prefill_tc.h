@@ -1,0 +1,58 @@
+// prefill_tc.h -- host-side interface of the tensor-core prefill kernel.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace attn {
+
+struct PrefillParams {
+    int B, Hq, Hkv, Sq, Sk;
+    int G;             // Hq / Hkv
+    int causal;        // bottom-right causal mask
+    int bhsd;          // 1: tensors are [B][H][S][d]; 0: [B][S][H][d]
+    float scale_log2;  // softmax scale * log2(e)
+    float *lse;        // [B][Hq][Sq] or nullptr
+    int n_m;           // ceil(Sq / 128)
+    int pair_heads;    // 1: a unit is two heads of one KV group at the same rows
+    unsigned *status;  // device status word [code, site]
+    uint64_t budget_ns;
+    int inject;        // 1: producer issues nothing (fault-injection test)
+};
+
+int prefill_smem_bytes();
+int prefill_num_units(const PrefillParams &p);
+cudaError_t launch_prefill(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
+                           const CUtensorMap &mo, const PrefillParams &p, int num_units, cudaStream_t stream);
+
+// Plain SIMT kernel, one warp per query row (debugging cross-check).
+cudaError_t launch_prefill_simple(const void *q, const void *k, const void *v, void *out, float *lse,
+                                  const PrefillParams &p, cudaStream_t stream);
+
+// Paged decode: split kernel + log-sum-exp merge.
+struct DecodeParams {
+    const void *q;            // [B][Hq][d] bf16
+    const int32_t *block_table;
+    const int32_t *seqlens;
+    void *out;                // [B][Hq][d] bf16
+    float *lse;               // [B][Hq] or nullptr
+    float *o_part;            // [B*Hq][nsplit][d] fp32
+    float *lse_part;          // [B*Hq][nsplit] fp32
+    int B, Hq, Hkv, G, num_pages, max_blocks, nsplit, pages_per_split;
+    float scale_log2;
+    unsigned *status;
+    uint64_t budget_ns;
+};
+
+int decode_pages_per_split();
+cudaError_t launch_decode(const CUtensorMap &mk, const CUtensorMap &mv, const DecodeParams &p,
+                          cudaStream_t stream);
+cudaError_t launch_lse_merge(const float *o_parts, const float *lse_parts, void *out, float *lse, int rows,
+                             int nsplit, cudaStream_t stream);
+
+// Tensor-core layout self-test.
+cudaError_t launch_selftest_umma(const CUtensorMap &ma, const CUtensorMap &mb, const void *a, float *c, int mode,
+                                 unsigned *status, uint64_t budget_ns, cudaStream_t stream);
+
+}  // namespace attn

@@ -1,0 +1,194 @@
+/*
+ * attn.h -- C ABI of the GB300 (sm_103a) exact-attention library.
+ *
+ * Operation (prefill): for every batch b, query head h and query row i,
+ *
+ *     O[b,i,h,:] = softmax_j( scale * q[b,i,h,:] . k[b,j,g,:] ) v[b,j,g,:]
+ *     lse[b,h,i] = ln sum_j exp( scale * q[b,i,h,:] . k[b,j,g,:] )
+ *
+ * with g = h / (Hq / Hkv), j over the keys the row may see.  This is the fused
+ * softmax(Q K^T / sqrt(d)) V of the MoonMath HIP attention page (opening
+ * section and its feature list: bf16, BSHD or BHSD with no transpose,
+ * head dim 128, any sequence lengths including cross-attention), computed
+ * with the IO-aware tiling and online softmax of "FlashAttention-4 中的 IO
+ * 感知块分块策略" (running max m, running sum l, m' = max(m, m_new),
+ * l' = l exp(m - m') + l_new; only m and l are kept as row statistics), with
+ * the causal upper-triangle skip and the grouped-query sharing of the
+ * reverse-engineering page (观点一 tiling strategy and multi-query settings)
+ * and the paged KV cache of the ROCm port page ("Vendor-Agnostic 多查询推理
+ * 优化": 16-token pages, int32 block_table).
+ *
+ * Readings taken where the pages are silent:
+ *   - causal alignment is bottom-right: key j is visible to row i iff
+ *     j <= i + Sk - Sq;
+ *   - a row that sees no key gets O = 0 and lse = -inf;
+ *   - lse is the natural log of the sum of exp of the *scaled* scores;
+ *   - O is rounded to bf16 round-to-nearest-even.
+ *
+ * Conventions for every entry point:
+ *   - Pointers named q, k, v, out, lse, k_pages, v_pages, block_table, seqlens,
+ *     workspace, o_parts, lse_parts are DEVICE pointers owned by the caller;
+ *     the library never frees or keeps them past the call.  The library
+ *     allocates no device memory on any call.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Work is
+ *     enqueued asynchronously; only attn_get_device_status synchronises.
+ *   - bf16 tensors are dense and contiguous; every device pointer must be
+ *     16-byte aligned.
+ *   - Arguments are validated before anything is launched; a rejected call
+ *     returns ATTN_ERR_INVALID_ARG or ATTN_ERR_UNSUPPORTED and enqueues nothing.
+ *   - A kernel that gives up on a bounded wait (see attn_set_wait_budget_ns)
+ *     records ATTN_ERR_TIMEOUT in the device status word and exits cleanly;
+ *     read it with attn_get_device_status.
+ *   - No entry point throws or aborts; all report through attn_status_t.
+ */
+#ifndef ATTN_H
+#define ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    ATTN_OK = 0,
+    ATTN_ERR_INVALID_ARG = 1,   /* NULL/misaligned pointer, bad shape, bad enum, non-finite scale */
+    ATTN_ERR_UNSUPPORTED = 2,   /* d != 128, page_size != 16, or not an sm_103 / sm_100 family GPU */
+    ATTN_ERR_CUDA = 3,          /* a CUDA runtime/driver call failed (launch error etc.) */
+    ATTN_ERR_TIMEOUT = 4,       /* a kernel's bounded wait expired (device status only) */
+    ATTN_ERR_WORKSPACE = 5,     /* workspace NULL, misaligned or smaller than required */
+    ATTN_ERR_DEVICE_BOUNDS = 6  /* a kernel met an out-of-range block_table entry (device status only) */
+} attn_status_t;
+
+typedef enum {
+    ATTN_LAYOUT_BSHD = 0,       /* [B][S][H][d] */
+    ATTN_LAYOUT_BHSD = 1        /* [B][H][S][d] */
+} attn_layout_t;
+
+/*
+ * attn_fwd -- fused exact attention forward (prefill), tcgen05 + TMA kernel.
+ *
+ * q:   bf16, layout `layout`, shape [B,Sq,Hq,d] (BSHD) or [B,Hq,Sq,d] (BHSD).
+ * k,v: bf16, same layout, shape [B,Sk,Hkv,d] or [B,Hkv,Sk,d].
+ * out: bf16, same layout and shape as q (written).
+ * lse: fp32 [B][Hq][Sq] (written), or NULL to skip it.
+ * d must be 128.  Hq must be a multiple of Hkv (MQA: Hkv = 1).  Sq and Sk are
+ * any lengths >= 1 and may differ.  causal != 0 applies the bottom-right
+ * causal mask.  scale is the softmax scale (usually 1/sqrt(d)); any finite
+ * value >= 0 is accepted.
+ * Results are deterministic: the same call on the same device returns
+ * bitwise-identical out and lse.
+ */
+attn_status_t attn_fwd(const void *q, const void *k, const void *v, void *out, float *lse,
+                       int B, int Hq, int Hkv, int Sq, int Sk, int d,
+                       int layout, int causal, float scale, void *stream);
+
+/*
+ * attn_fwd_simple -- the same operation and contract as attn_fwd, computed by
+ * a plain SIMT CUDA kernel (one warp per query row, no tensor cores).  It is
+ * a debugging cross-check for attn_fwd, not a fallback: nothing routes to it
+ * automatically.  Slow; meant for small shapes.
+ */
+attn_status_t attn_fwd_simple(const void *q, const void *k, const void *v, void *out, float *lse,
+                              int B, int Hq, int Hkv, int Sq, int Sk, int d,
+                              int layout, int causal, float scale, void *stream);
+
+/*
+ * attn_decode_workspace_bytes -- bytes of device workspace attn_decode_paged
+ * needs for this shape.  A pure function of the arguments (the key-split plan
+ * depends only on the shape and the device's SM count, never on device data).
+ * Returns 0 for invalid arguments.
+ */
+size_t attn_decode_workspace_bytes(int B, int Hq, int d, int max_blocks_per_seq);
+
+/*
+ * attn_decode_paged -- one decode step over a paged KV cache, split over the
+ * keys (Flash-Decoding style, as in the MoonMath page's tail split) and
+ * merged by log-sum-exp.
+ *
+ * q:           bf16 [B][Hq][d], one query per sequence and head.
+ * k_pages,
+ * v_pages:     bf16 [num_pages][page_size][Hkv][d], the page pool.
+ * block_table: int32 [B][max_blocks_per_seq]; entry p of row b is the
+ *              physical page of keys 16p .. 16p+15 of sequence b.  Entries at
+ *              or past ceil(seqlens[b]/16) are never read (may hold -1).
+ * seqlens:     int32 [B] on the device, each in [0, 16 * max_blocks_per_seq].
+ * out:         bf16 [B][Hq][d] (written); a sequence of length 0 gets zeros.
+ * lse:         fp32 [B][Hq] (written, -inf for length 0), or NULL.
+ * page_size must be 16; d must be 128; Hq % Hkv == 0.
+ * workspace:   device buffer of at least attn_decode_workspace_bytes(...)
+ *              bytes, 256-byte aligned, owned by the caller; its contents on
+ *              entry do not matter and are overwritten.
+ * A block_table entry outside [0, num_pages) that is needed is not read: the
+ * keys of that page count as absent and ATTN_ERR_DEVICE_BOUNDS is recorded
+ * in the device status word.
+ */
+attn_status_t attn_decode_paged(const void *q, const void *k_pages, const void *v_pages,
+                                const int32_t *block_table, const int32_t *seqlens,
+                                void *out, float *lse,
+                                int B, int Hq, int Hkv, int d, int page_size,
+                                int num_pages, int max_blocks_per_seq, float scale,
+                                void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * attn_lse_merge -- merge key-range partial results by log-sum-exp (the merge
+ * step of the Flash-Decoding style split).  For each row r:
+ *     M = max_s lse_parts[r][s];  lse = M + ln sum_s exp(lse_parts[r][s] - M)
+ *     out[r][:] = sum_s exp(lse_parts[r][s] - lse) * o_parts[r][s][:]
+ * in a fixed split order (deterministic).  Rows whose partials are all -inf
+ * get out = 0 and lse = -inf.
+ * o_parts: fp32 [rows][nsplit][d], each partial normalised within its range.
+ * lse_parts: fp32 [rows][nsplit].  out: bf16 [rows][d].  lse: fp32 [rows] or NULL.
+ * d must be 128; nsplit >= 1.
+ */
+attn_status_t attn_lse_merge(const float *o_parts, const float *lse_parts, void *out, float *lse,
+                             int rows, int nsplit, int d, void *stream);
+
+/*
+ * attn_get_device_status -- synchronise `stream`, then read and clear the
+ * current device's status word.  Returns ATTN_OK, ATTN_ERR_TIMEOUT or
+ * ATTN_ERR_DEVICE_BOUNDS as recorded by kernels since the last call (or
+ * ATTN_ERR_CUDA if the synchronisation itself failed).  *site (may be NULL)
+ * receives the id of the wait or check that recorded it.
+ */
+attn_status_t attn_get_device_status(void *stream, int *site);
+
+/*
+ * attn_set_wait_budget_ns -- time budget of every bounded wait inside the
+ * kernels (mbarrier waits), in nanoseconds of the GPU's global timer.
+ * Default 2e9 (2 s); 0 restores the default.  Applies to later launches.
+ */
+attn_status_t attn_set_wait_budget_ns(uint64_t ns);
+
+/*
+ * attn_debug_inject -- host-side fault injection for the failure-detection
+ * tests.  mode 0: off (default).  mode 1: the next attn_fwd launches its
+ * kernel with the load-issuing warp told to issue nothing, so the other warps'
+ * bounded waits expire, they record ATTN_ERR_TIMEOUT and the kernel exits
+ * cleanly (no fault, no hang, nothing left in flight).  The flag clears
+ * itself after one launch.
+ */
+attn_status_t attn_debug_inject(int mode);
+
+/*
+ * attn_selftest_umma -- checks the tensor-core operand layouts this library
+ * uses, on one 128x128x128 tile: c[i][j] = sum_k a[i][k] * b[j][k] (mode 0:
+ * both operands from shared memory, K-major) or c[i][j] = sum_k a[i][k] *
+ * b[k][j] (mode 1: a from tensor memory, b from shared memory N-major, the
+ * form the P*V product uses).  a, b: bf16 [128][128] row-major device
+ * buffers; c: fp32 [128][128] (written).
+ */
+attn_status_t attn_selftest_umma(const void *a, const void *b, float *c, int mode, void *stream);
+
+/* attn_status_string -- static, human-readable name of a status code. */
+const char *attn_status_string(attn_status_t status);
+
+/* attn_version -- library version, major * 10000 + minor * 100 + patch. */
+int attn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_H */

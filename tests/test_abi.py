@@ -1,0 +1,112 @@
+"""C-ABI checks that need no GPU: the library loads, exports every symbol the
+header declares, and rejects bad arguments before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import exact_attention_forward_06_gb300 as A
+from exact_attention_forward_06_gb300 import _binding
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADERS = [os.path.join(ROOT, "include", f) for f in sorted(os.listdir(os.path.join(ROOT, "include")))
+           if f.endswith(".h")]
+
+
+def declared_functions():
+    names = set()
+    for h in HEADERS:
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names.update(re.findall(r"\b(attn_[a-z0-9_]+)\s*\(", text))
+    return sorted(names)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(_binding.LIBRARY_PATH):
+        import __graft_entry__
+        __graft_entry__.build()
+    return A.load()
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for must in ("attn_fwd", "attn_decode_paged", "attn_decode_workspace_bytes", "attn_lse_merge",
+                 "attn_get_device_status", "attn_status_string"):
+        assert must in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    raw = ctypes.CDLL(_binding.LIBRARY_PATH)
+    missing = [n for n in declared_functions() if not hasattr(raw, n)]
+    assert not missing, f"declared but not exported: {missing}"
+
+
+def test_status_strings(lib):
+    for code, name in _binding.STATUS_NAMES.items():
+        assert A.status_string(code) == name
+    assert A.version() >= 100
+
+
+def _fwd(lib, **kw):
+    args = dict(q=16, k=16, v=16, out=16, lse=None, B=1, Hq=2, Hkv=2, Sq=8, Sk=8, d=128, layout=0, causal=0,
+                scale=0.1)
+    args.update(kw)
+    return lib.attn_fwd(args["q"], args["k"], args["v"], args["out"], args["lse"], args["B"], args["Hq"],
+                        args["Hkv"], args["Sq"], args["Sk"], args["d"], args["layout"], args["causal"],
+                        args["scale"], None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=None), 1), (dict(out=None), 1), (dict(q=24), 1), (dict(B=0), 1), (dict(Sq=0), 1), (dict(Sk=-1), 1),
+    (dict(Hq=3, Hkv=2), 1), (dict(layout=2), 1), (dict(scale=float("nan")), 1), (dict(scale=float("inf")), 1),
+    (dict(scale=-1.0), 1), (dict(d=64), 2), (dict(lse=18), 1),
+])
+def test_fwd_rejects_bad_arguments_before_any_launch(lib, kw, code):
+    assert _fwd(lib, **kw) == code
+    # the simple kernel shares the validation
+    args = dict(q=16, k=16, v=16, out=16, lse=None, B=1, Hq=2, Hkv=2, Sq=8, Sk=8, d=128, layout=0, causal=0,
+                scale=0.1)
+    args.update(kw)
+    assert lib.attn_fwd_simple(*[args[n] for n in ("q", "k", "v", "out", "lse", "B", "Hq", "Hkv", "Sq", "Sk",
+                                                   "d", "layout", "causal", "scale")], None) == code
+
+
+def test_decode_workspace_is_a_pure_function_of_shape(lib):
+    a = A.decode_workspace_bytes(32, 32, 128, 512)
+    assert a == A.decode_workspace_bytes(32, 32, 128, 512) and a > 0
+    assert A.decode_workspace_bytes(32, 32, 128, 513) > a
+    assert A.decode_workspace_bytes(32, 32, 64, 512) == 0
+    assert A.decode_workspace_bytes(0, 32, 128, 512) == 0
+
+
+def _decode(lib, **kw):
+    a = dict(q=16, kp=16, vp=16, bt=16, sl=16, out=16, lse=None, B=2, Hq=4, Hkv=2, d=128, page=16, npages=10,
+             maxb=4, scale=0.1, ws=256, wsb=1 << 20)
+    a.update(kw)
+    return lib.attn_decode_paged(a["q"], a["kp"], a["vp"], a["bt"], a["sl"], a["out"], a["lse"], a["B"], a["Hq"],
+                                 a["Hkv"], a["d"], a["page"], a["npages"], a["maxb"], a["scale"], a["ws"],
+                                 a["wsb"], None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=None), 1), (dict(bt=None), 1), (dict(bt=18), 1), (dict(Hq=5), 1), (dict(npages=0), 1),
+    (dict(maxb=0), 1), (dict(scale=float("nan")), 1), (dict(page=32), 2), (dict(d=256), 2),
+    (dict(ws=None), 5), (dict(ws=272), 5), (dict(wsb=16), 5),
+])
+def test_decode_rejects_bad_arguments_before_any_launch(lib, kw, code):
+    assert _decode(lib, **kw) == code
+
+
+def test_merge_rejects_bad_arguments(lib):
+    assert lib.attn_lse_merge(None, 16, 16, None, 4, 2, 128, None) == 1
+    assert lib.attn_lse_merge(16, 16, 16, None, 0, 2, 128, None) == 1
+    assert lib.attn_lse_merge(16, 16, 16, None, 4, 2, 64, None) == 2
+
+
+def test_debug_controls(lib):
+    assert lib.attn_debug_inject(7) == 1
+    assert lib.attn_debug_inject(0) == 0
+    assert lib.attn_set_wait_budget_ns(0) == 0
