@@ -143,6 +143,10 @@ __device__ __forceinline__ void load_tile(const CUtensorMap *map, uint8_t *dst, 
 __device__ void producer(const PrefillParams &p, const Unit &w, const SmemLayout &sm, const WaitCtx &wc,
                          const CUtensorMap *mq, const CUtensorMap *mk, const CUtensorMap *mv) {
     if (p.inject == 1) return;  // fault injection: issue nothing
+    // A unit whose rows see no key loads nothing: its output tiles are zeros,
+    // written into the Q tile buffers, which therefore must not receive a
+    // late-landing Q copy.
+    if (w.n_kv == 0) return;
     const uint64_t pol_q = ptx::policy_evict_first();
     const uint64_t pol_kv = ptx::policy_evict_last();
     ptx::mbar_arrive_expect_tx(sm.q_full(), 2 * TILE_BYTES);
@@ -184,6 +188,7 @@ __device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t tmem_p, uint3
 }
 
 __device__ void mma_issuer(const Unit &w, const SmemLayout &sm, const WaitCtx &wc, uint32_t tmem_base) {
+    if (w.n_kv == 0) return;  // nothing to multiply (and no Q is loaded)
     if (!wait_bounded(sm.q_full(), 0, wc, kSiteMmaQ)) return;
     ptx::tc_fence_after();
     const uint32_t q_addr[2] = {ptx::smem_addr(sm.q_tile(0)), ptx::smem_addr(sm.q_tile(1))};
