@@ -1,0 +1,62 @@
+"""Host-side multi-rank logic of bench.py on CPU: two gloo ranks.
+
+Each GPU would run its own replica of the step (weak scaling, no collective on
+the data path); the only cross-rank traffic is the barrier around the timed
+region and the max over ranks of the measured times.  This checks that logic
+with world_size 2 over gloo, rendezvous on 127.0.0.1.
+"""
+import os
+import socket
+
+import pytest
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, results):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world))
+    import bench
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        bench.barrier()
+        got = bench.reduce_max_over_ranks(10.0 + rank)
+        results[rank] = got
+        bench.barrier()
+    finally:
+        dist.destroy_process_group()
+
+
+def test_max_over_two_gloo_ranks():
+    world = 2
+    port = _free_port()
+    with mp.Manager() as m:
+        results = m.dict()
+        mp.spawn(_worker, args=(world, port, results), nprocs=world, join=True)
+        assert dict(results) == {0: 11.0, 1: 11.0}
+
+
+def test_single_process_is_identity():
+    import bench
+    assert not dist.is_initialized()
+    assert bench.reduce_max_over_ranks(3.5) == 3.5
+
+
+def test_prefill_units_match_kernel_plan():
+    import bench
+    from exact_attention_forward_06_gb300 import inputs
+    assert bench.prefill_units(inputs.GQA_CAUSAL) == 4 * 8 * 2 * 32       # paired heads, 32 row blocks
+    assert bench.prefill_units(inputs.RAGGED_SELF) == 2 * 12 * 128        # G = 1: pairs of row blocks
+    assert bench.prefill_units(inputs.MQA_CAUSAL) == 1 * 1 * 16 * 128
+
+
+@pytest.mark.parametrize("warmup", [0, 2])
+def test_bench_rejects_short_warmup(warmup):
+    import bench
+    with pytest.raises(SystemExit):
+        bench.main(["--warmup", str(warmup)])
