@@ -4,10 +4,12 @@ The computation lives in the CUDA library ``libattn.so`` (C ABI, include/attn.h)
 this package is its thin Python binding.  Importing the package does not load
 the library; the first call does, and raises if it has not been built.
 """
-from ._binding import (AttnError, LIBRARY_PATH, debug_inject, decode_paged, decode_workspace_bytes,
+from ._binding import (AttnError, LIBRARY_PATH, debug_inject, decode_paged, decode_paged_noalloc,
+                       decode_workspace_bytes,
                        device_status, fwd, fwd_simple, load, lse_merge, selftest_umma, set_wait_budget_ns,
                        status_string, version)
 
-__all__ = ["AttnError", "LIBRARY_PATH", "debug_inject", "decode_paged", "decode_workspace_bytes", "device_status",
+__all__ = ["AttnError", "LIBRARY_PATH", "debug_inject", "decode_paged", "decode_paged_noalloc",
+           "decode_workspace_bytes", "device_status",
            "fwd", "fwd_simple", "load", "lse_merge", "selftest_umma", "set_wait_budget_ns", "status_string",
            "version"]

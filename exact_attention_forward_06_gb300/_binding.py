@@ -55,6 +55,9 @@ def load():
             lib.attn_decode_workspace_bytes.restype = _sz
             lib.attn_decode_paged.argtypes = [_p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _f, _p,
                                               _sz, _p]
+            lib.attn_decode_paged_noalloc.argtypes = [_p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i,
+                                                      _f, _p]
+            lib.attn_decode_paged_noalloc.restype = _i
             lib.attn_lse_merge.argtypes = [_p, _p, _p, _p, _i, _i, _i, _p]
             lib.attn_get_device_status.argtypes = [_p, ctypes.POINTER(_i)]
             lib.attn_set_wait_budget_ns.argtypes = [_u64]
@@ -174,6 +177,39 @@ def decode_paged(q, k_pages, v_pages, block_table, seqlens, *, scale=None, out=N
                                max_blocks, float(scale), workspace.data_ptr(), workspace.numel(),
                                _stream(stream))
     _check(rc, "attn_decode_paged")
+    return out, (None if lse is False else lse)
+
+
+def decode_paged_noalloc(q, k_pages, v_pages, block_table, seqlens, *, scale=None, out=None, lse=None,
+                         stream=None):
+    """decode_paged for callers that cannot allocate device memory.
+
+    Same arguments and results as ``decode_paged`` minus the workspace: the
+    split partials live in a fixed 16 MiB device array owned by the library
+    (shared by every call, so calls must not overlap on the GPU).  ``out`` and
+    ``lse`` must be passed by a caller that cannot allocate; when they are
+    omitted this wrapper allocates them with torch for convenience.
+    """
+    lib = load()
+    _dev_tensor(q, "q", torch.bfloat16)
+    _dev_tensor(k_pages, "k_pages", torch.bfloat16)
+    _dev_tensor(v_pages, "v_pages", torch.bfloat16)
+    _dev_tensor(block_table, "block_table", torch.int32)
+    _dev_tensor(seqlens, "seqlens", torch.int32)
+    B, Hq, d = q.shape
+    num_pages, page_size, Hkv, _ = k_pages.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, Hq), device=q.device, dtype=torch.float32)
+    lse_ptr = None if lse is False else lse.data_ptr()
+    rc = lib.attn_decode_paged_noalloc(q.data_ptr(), k_pages.data_ptr(), v_pages.data_ptr(),
+                                       block_table.data_ptr(), seqlens.data_ptr(), out.data_ptr(), lse_ptr, B, Hq,
+                                       Hkv, d, page_size, num_pages, block_table.shape[1], float(scale),
+                                       _stream(stream))
+    _check(rc, "attn_decode_paged_noalloc")
     return out, (None if lse is False else lse)
 
 

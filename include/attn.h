@@ -132,6 +132,42 @@ attn_status_t attn_decode_paged(const void *q, const void *k_pages, const void *
                                 void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * ATTN_DECODE_NOALLOC_SCRATCH_BYTES -- capacity of the device array that
+ * attn_decode_paged_noalloc keeps its split partials in: 16 MiB, held on every
+ * GPU that loads the library until the process exits.
+ */
+#define ATTN_DECODE_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
+
+/*
+ * attn_decode_paged_noalloc -- attn_decode_paged for callers that cannot
+ * allocate device memory.  (The pages have no counterpart of this entry point;
+ * it exists for such callers, not for the method.)
+ *
+ * Some callers cannot hand the decode step a workspace: an operator interface
+ * of a host framework that passes a kernel only its inputs and outputs and has
+ * no allocator or workspace hook, or an engine that reserved all of HBM for its
+ * own pools and forbids further cudaMalloc calls (which would also synchronise
+ * the device inside a latency-critical loop).  This entry point takes the same
+ * arguments as attn_decode_paged minus the workspace and keeps the split
+ * partials in a library-owned device array of ATTN_DECODE_NOALLOC_SCRATCH_BYTES
+ * instead.  It calls no cudaMalloc, cudaFree or other allocating routine.
+ *
+ * The caller still passes every input and output buffer.  A shape whose
+ * attn_decode_workspace_bytes(B, Hq, d, max_blocks_per_seq) exceeds the array
+ * is rejected with ATTN_ERR_WORKSPACE before anything is launched.  The first
+ * call on a device looks up the array's device address (cudaGetSymbolAddress)
+ * on that device; make that first call before any stream capture.  All calls
+ * share the one array, which keeps the last call's contents (nothing in it
+ * needs to start at zero): calls that overlap on the GPU, e.g. on two streams
+ * with no ordering between them, race on it and must not be issued.
+ */
+attn_status_t attn_decode_paged_noalloc(const void *q, const void *k_pages, const void *v_pages,
+                                        const int32_t *block_table, const int32_t *seqlens,
+                                        void *out, float *lse,
+                                        int B, int Hq, int Hkv, int d, int page_size,
+                                        int num_pages, int max_blocks_per_seq, float scale, void *stream);
+
+/*
  * attn_lse_merge -- merge key-range partial results by log-sum-exp (the merge
  * step of the Flash-Decoding style split).  For each row r:
  *     M = max_s lse_parts[r][s];  lse = M + ln sum_s exp(lse_parts[r][s] - M)
