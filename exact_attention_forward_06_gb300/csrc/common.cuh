@@ -45,7 +45,10 @@ struct WaitCtx {
 // Wait for the phase of `bar` with the given parity.  Gives up (returns false)
 // when another thread of the CTA has raised the abort flag, or when the budget
 // runs out, in which case it raises the flag and records a timeout.
-static __device__ __noinline__ bool wait_bounded(uint64_t *bar, uint32_t parity, const WaitCtx &w, unsigned site) {
+// Both waits are inlined: a kernel whose warpgroups run under different
+// setmaxnreg register budgets must not share an out-of-line device function
+// between them.
+static __device__ __forceinline__ bool wait_bounded(uint64_t *bar, uint32_t parity, const WaitCtx &w, unsigned site) {
     if (ptx::mbar_try(bar, parity)) return true;
     const uint64_t t0 = ptx::globaltimer();
     for (uint32_t it = 1;; ++it) {
@@ -63,7 +66,7 @@ static __device__ __noinline__ bool wait_bounded(uint64_t *bar, uint32_t parity,
 // an MMA in flight), ignoring the abort flag: used on the way out so that no
 // asynchronous write into shared or tensor memory outlives the CTA.  Still
 // bounded by the budget.
-static __device__ __noinline__ bool drain_wait(uint64_t *bar, uint32_t parity, const WaitCtx &w) {
+static __device__ __forceinline__ bool drain_wait(uint64_t *bar, uint32_t parity, const WaitCtx &w) {
     const uint64_t t0 = ptx::globaltimer();
     for (uint32_t it = 0;; ++it) {
         if (ptx::mbar_try(bar, parity)) return true;

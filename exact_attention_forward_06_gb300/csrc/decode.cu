@@ -7,16 +7,21 @@
 // once and does ~4 flops per byte, so it is bound by HBM bandwidth and runs on
 // the CUDA cores; the tensor cores would only add a reshape.
 //
-// Split kernel: one CTA per (split, group of up to 4 query heads sharing a KV
-// head, sequence).  A producer lane gathers the split's pages with one 3-D
-// TMA copy per page and tensor (the 16 rows of one KV head in a page are 2 KiB
-// apart in the pool) into an 8-page shared-memory ring.  Four consumer warps
-// take pages round-robin.  In a warp, lane (tg, ds) = (lane/8, lane%8) owns
-// head-dim slice [16 ds, 16 ds + 16) of tokens tg, tg+4, tg+8, tg+12 of the
-// page: dot products are reduced over the 8 lanes of a token with three
-// shuffles, the page max over the token groups with two more, and each warp
-// keeps its own running max / sum / accumulator (online softmax, with the max
-// moved only past a 2^8 growth).  At the end the four warps are merged in
+// Split kernel: one CTA per (group of up to 2 query heads sharing a KV head,
+// split, sequence); the head groups of one split are adjacent in the grid so
+// that their reads of the same pages meet in L2.  The CTAs are small (one
+// producer warp and four consumer warps, about 128 registers a thread) so
+// three of them share an SM.  The producer lane gathers the split's pages with
+// one 3-D TMA copy per page and tensor (the 16 rows of one KV head in a page
+// are 2 KiB apart in the pool) into an 8-page shared-memory ring.  The four
+// consumer warps take pages round-robin.  In a warp, lane (tg, ds) =
+// (lane/8, lane%8) owns head-dim elements [8 ds, 8 ds + 8) and
+// [64 + 8 ds, 64 + 8 ds + 8) of tokens tg, tg+4, tg+8, tg+12 of the page (two
+// 16-byte chunks, so the eight lanes of a token read one 256-byte row without
+// bank conflicts).  Dot products are reduced over the 8 lanes of a token with
+// three shuffles, the page max over the token groups with two more, and each
+// warp keeps its own running max / sum / accumulator (online softmax, with the
+// max moved only past a 2^8 growth).  At the end the four warps are merged in
 // shared memory and the split writes its normalised partial output and
 // log-sum-exp.  The merge kernel then combines the splits in a fixed order.
 #include <cstdint>
@@ -33,7 +38,7 @@ constexpr int PAGE = 16;
 constexpr int D = 128;
 constexpr int NCW = 4;   // consumer warps
 constexpr int NST = 8;   // pages in flight per CTA
-constexpr int GH_MAX = 4;
+constexpr int GH_MAX = 2;
 constexpr int NTHREADS = (NCW + 1) * 32;
 constexpr uint32_t PAGE_BYTES = PAGE * D * 2;        // one tensor, one KV head: 4 KiB
 constexpr uint32_t STAGE_BYTES = 2 * PAGE_BYTES;     // K + V
@@ -59,7 +64,7 @@ __device__ __forceinline__ void bf16x8_to_float(const uint4 &u, float *x) {
 }
 
 template <int GH>
-__global__ void __launch_bounds__(NTHREADS)
+__global__ void __launch_bounds__(NTHREADS, 3)
     split_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
                  const DecodeParams p) {
     extern __shared__ uint8_t smem_raw[];
@@ -71,8 +76,8 @@ __global__ void __launch_bounds__(NTHREADS)
     int *stage_bad = reinterpret_cast<int *>(empty + NST);
     volatile int *abort_flag = stage_bad + NST;
 
-    const int split = blockIdx.x;
-    const int h0 = blockIdx.y * GH;
+    const int split = blockIdx.y;
+    const int h0 = blockIdx.x * GH;
     const int b = blockIdx.z;
     const int g = h0 / p.G;
     const int warp = threadIdx.x >> 5;
@@ -109,7 +114,6 @@ __global__ void __launch_bounds__(NTHREADS)
         if (lane == 0) {
             ptx::prefetch_tensormap(&map_k);
             ptx::prefetch_tensormap(&map_v);
-            const uint64_t pol = ptx::policy_evict_first();
             int issued = 0;
             for (int i = 0; i < np; ++i) {
                 const int slot = i % NST;
@@ -126,7 +130,6 @@ __global__ void __launch_bounds__(NTHREADS)
                     ptx::mbar_arrive_expect_tx(full + slot, STAGE_BYTES);
                     ptx::tma_load_3d(dst, &map_k, full + slot, 0, g, phys * PAGE);
                     ptx::tma_load_3d(dst + PAGE_BYTES, &map_v, full + slot, 0, g, phys * PAGE);
-                    (void)pol;
                 }
                 ++issued;
             }
@@ -136,14 +139,14 @@ __global__ void __launch_bounds__(NTHREADS)
     } else {
         // ---------------- consumers
         const int tg = lane >> 3;  // token group
-        const int ds = lane & 7;   // 16-element head-dim slice
+        const int ds = lane & 7;   // head-dim chunks ds and 8 + ds
         float qf[GH][16];
 #pragma unroll
         for (int h = 0; h < GH; ++h) {
             const uint4 *qp = reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(p.q) +
-                                                              (row0 + h) * D + ds * 16);
-            bf16x8_to_float(qp[0], qf[h]);
-            bf16x8_to_float(qp[1], qf[h] + 8);
+                                                              (row0 + h) * D);
+            bf16x8_to_float(qp[ds], qf[h]);
+            bf16x8_to_float(qp[8 + ds], qf[h] + 8);
 #pragma unroll
             for (int e = 0; e < 16; ++e) qf[h][e] *= p.scale_log2;
         }
@@ -166,10 +169,10 @@ __global__ void __launch_bounds__(NTHREADS)
 #pragma unroll
             for (int ps = 0; ps < 4; ++ps) {
                 const int t = ps * 4 + tg;
-                const uint4 *kp = reinterpret_cast<const uint4 *>(ks + t * (D * 2) + ds * 32);
+                const uint4 *kp = reinterpret_cast<const uint4 *>(ks + t * (D * 2));
                 float kf[16];
-                bf16x8_to_float(kp[0], kf);
-                bf16x8_to_float(kp[1], kf + 8);
+                bf16x8_to_float(kp[ds], kf);
+                bf16x8_to_float(kp[8 + ds], kf + 8);
 #pragma unroll
                 for (int h = 0; h < GH; ++h) {
                     float dot = 0.f;
@@ -204,10 +207,10 @@ __global__ void __launch_bounds__(NTHREADS)
 #pragma unroll
             for (int ps = 0; ps < 4; ++ps) {
                 const int t = ps * 4 + tg;
-                const uint4 *vp = reinterpret_cast<const uint4 *>(vs + t * (D * 2) + ds * 32);
+                const uint4 *vp = reinterpret_cast<const uint4 *>(vs + t * (D * 2));
                 float vf[16];
-                bf16x8_to_float(vp[0], vf);
-                bf16x8_to_float(vp[1], vf + 8);
+                bf16x8_to_float(vp[ds], vf);
+                bf16x8_to_float(vp[8 + ds], vf + 8);
 #pragma unroll
                 for (int h = 0; h < GH; ++h)
 #pragma unroll
@@ -233,7 +236,10 @@ __global__ void __launch_bounds__(NTHREADS)
             float *row = mw + h * (D + 2);
             if (tg == 0) {
 #pragma unroll
-                for (int e = 0; e < 16; ++e) row[ds * 16 + e] = acc[h][e];
+                for (int e = 0; e < 8; ++e) {
+                    row[ds * 8 + e] = acc[h][e];
+                    row[64 + ds * 8 + e] = acc[h][8 + e];
+                }
             }
             if (lane == 0) {
                 row[D] = m[h];
@@ -296,26 +302,29 @@ int decode_pages_per_split() { return dec::PAGES_PER_SPLIT; }
 
 cudaError_t launch_decode(const CUtensorMap &mk, const CUtensorMap &mv, const DecodeParams &p,
                           cudaStream_t stream) {
-    // Heads per CTA: the largest of 4, 2, 1 dividing the group size.
-    const int GH = (p.G % 4 == 0) ? 4 : (p.G % 2 == 0) ? 2 : 1;
-    dim3 grid(p.nsplit, p.Hq / GH, p.B);
+    // Heads per CTA: 2 when the group size is even, else 1.
+    const int GH = (p.G % 2 == 0) ? 2 : 1;
+    dim3 grid(p.Hq / GH, p.nsplit, p.B);
     const int smem = (int)dec::SMEM_BYTES;
     static thread_local int configured_device = -1;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (configured_device != dev) {
-        e = cudaFuncSetAttribute(dec::split_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(dec::split_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        e = cudaFuncSetAttribute(dec::split_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(dec::split_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        // Three CTAs of ~74 KiB per SM need the largest shared-memory carveout.
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(dec::split_kernel<2>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                     cudaSharedmemCarveoutMaxShared);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(dec::split_kernel<1>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                     cudaSharedmemCarveoutMaxShared);
         if (e != cudaSuccess) return e;
         configured_device = dev;
     }
-    if (GH == 4)
-        dec::split_kernel<4><<<grid, dec::NTHREADS, smem, stream>>>(mk, mv, p);
-    else if (GH == 2)
+    if (GH == 2)
         dec::split_kernel<2><<<grid, dec::NTHREADS, smem, stream>>>(mk, mv, p);
     else
         dec::split_kernel<1><<<grid, dec::NTHREADS, smem, stream>>>(mk, mv, p);

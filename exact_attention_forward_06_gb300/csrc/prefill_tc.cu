@@ -12,19 +12,23 @@
 // One CTA owns two 128-row Q tiles ("units" of 256 rows: two heads of one KV
 // group at the same positions when the group size is even, else two adjacent
 // position blocks of one head), so every K/V tile that is loaded serves 256
-// query rows.  Warp roles (320 threads):
+// query rows.  Warp roles (384 threads, three warpgroups):
 //   warp 0      TMA producer: Q tiles once, then K_j / V_j into a 5-slot ring
 //               of 32 KiB slots (full/empty mbarrier pairs);
 //   warp 1      TMEM allocator and single-thread tcgen05 MMA issuer;
-//   warps 2-5   softmax warpgroup for Q tile 0 (one thread per row);
-//   warps 6-9   softmax warpgroup for Q tile 1.
-// Tensor memory (512 columns): S_t at column 256t, O_t at 256t + 128; the
-// bf16 probabilities P_t overwrite the first 64 columns of S_t and feed the
-// P V product straight from tensor memory.  The MMA thread interleaves the
-// two tiles' chains S_t(j) -> softmax_t(j) -> PV_t(j) -> S_t(j+1) and issues
-// whichever chain is ready, so one tile's softmax runs while the tensor core
-// works on the other tile (the two-group alternation of the MoonMath page,
-// realised as two Q tiles instead of two wave groups).
+//   warps 2-3   idle (they complete warpgroup 0, which gives up registers);
+//   warps 4-7   softmax warpgroup for Q tile 0 (one thread per row);
+//   warps 8-11  softmax warpgroup for Q tile 1.
+// setmaxnreg moves registers from warpgroup 0 (96 each) to the softmax
+// warpgroups (200 each), which hold a whole 128-column score row.
+// Tensor memory (512 columns): one fp32 score buffer S that the two tiles use
+// in turn, a bf16 probability buffer P_t per tile (64 columns of packed
+// pairs, read by the P V product straight from tensor memory) and an fp32
+// output accumulator O_t per tile.  The MMA thread issues, for every K/V tile
+// j, PV_0(j), S_0(j+1), PV_1(j), S_1(j+1): while one tile's softmax runs, the
+// tensor core works on the other tile's products, and a softmax releases S as
+// soon as it has loaded its scores (the two-group alternation of the MoonMath
+// page, realised as two Q tiles instead of two wave groups).
 //
 // Softmax: scores are scaled into the log2 domain (scale * log2 e folded into
 // one FFMA) and exponentiated with ex2.approx.  A row's running max is only
@@ -49,12 +53,17 @@ constexpr int D = 128;           // head dim
 constexpr int NSLOT = 5;         // K/V ring slots
 constexpr uint32_t TILE_BYTES = BM * D * 2;  // 32 KiB (128 rows x 256 B)
 constexpr uint32_t HALF_BYTES = TILE_BYTES / 2;  // one 64-column half (128 B rows, 128-B swizzle)
-constexpr int NUM_THREADS = 320;
+constexpr int NUM_THREADS = 384;  // three warpgroups
+constexpr uint32_t REGS_CONTROL = 96;   // warpgroup 0: producer, MMA issuer
+constexpr uint32_t REGS_SOFTMAX = 200;  // warpgroups 1-2: softmax
+// setmaxnreg hands registers between warpgroups within the launch budget
+// (384 threads x 168): 128 x 96 + 256 x 200 <= 384 x 168.
+static_assert(128 * REGS_CONTROL + 256 * REGS_SOFTMAX <= NUM_THREADS * 168, "register split exceeds the launch budget");
 constexpr uint32_t SMEM_Q0 = 0;
 constexpr uint32_t SMEM_Q1 = TILE_BYTES;
 constexpr uint32_t SMEM_SLOTS = 2 * TILE_BYTES;
 constexpr uint32_t SMEM_TILES = SMEM_SLOTS + NSLOT * TILE_BYTES;
-constexpr int NBARS = 1 + 2 * NSLOT + 2 + 2 + 2 + 1;
+constexpr int NBARS = 1 + 2 * NSLOT + 2 + 1 + 2 + 2 + 1;
 constexpr uint32_t SMEM_MISC = 256;
 constexpr uint32_t SMEM_ALIGN = 1024;
 constexpr float RESCALE_LOG2 = 8.0f;  // move the running max only past a 2^8 growth
@@ -65,6 +74,15 @@ static_assert(NBARS * 8 + 16 <= SMEM_MISC, "barrier area too small");
 constexpr uint32_t IDESC_S = ptx::idesc_bf16_f32(128, 128, 0, 0);   // Q K^T: both K-major
 constexpr uint32_t IDESC_PV = ptx::idesc_bf16_f32(128, 128, 0, 1);  // P V: V is N(d)-major
 
+// Tensor-memory columns: one S buffer shared by the two tiles in turn, a bf16
+// P buffer per tile (64 columns of packed pairs) and an fp32 O accumulator per
+// tile.  P never aliases an S that a later product writes.
+constexpr uint32_t TM_S = 0;
+constexpr uint32_t TM_P0 = 128;
+constexpr uint32_t TM_O0 = 256;
+__device__ __forceinline__ uint32_t tm_p(int t) { return TM_P0 + 64 * t; }
+__device__ __forceinline__ uint32_t tm_o(int t) { return TM_O0 + 128 * t; }
+
 struct SmemLayout {
     uint8_t *base;
     uint64_t *bars;
@@ -72,9 +90,10 @@ struct SmemLayout {
     __device__ uint64_t *kv_full(int s) const { return bars + 1 + s; }
     __device__ uint64_t *kv_empty(int s) const { return bars + 1 + NSLOT + s; }
     __device__ uint64_t *s_full(int t) const { return bars + 1 + 2 * NSLOT + t; }
-    __device__ uint64_t *p_full(int t) const { return bars + 3 + 2 * NSLOT + t; }
-    __device__ uint64_t *o_full(int t) const { return bars + 5 + 2 * NSLOT + t; }
-    __device__ uint64_t *fin() const { return bars + 7 + 2 * NSLOT; }
+    __device__ uint64_t *s_free() const { return bars + 3 + 2 * NSLOT; }
+    __device__ uint64_t *p_full(int t) const { return bars + 4 + 2 * NSLOT + t; }
+    __device__ uint64_t *o_full(int t) const { return bars + 6 + 2 * NSLOT + t; }
+    __device__ uint64_t *fin() const { return bars + 8 + 2 * NSLOT; }
     __device__ uint32_t *tmem_slot() const { return reinterpret_cast<uint32_t *>(bars + NBARS); }
     __device__ volatile int *abort_flag() const { return reinterpret_cast<volatile int *>(bars + NBARS) + 1; }
     __device__ uint8_t *q_tile(int t) const { return base + (t ? SMEM_Q1 : SMEM_Q0); }
@@ -169,117 +188,128 @@ __device__ void producer(const PrefillParams &p, const Unit &w, const SmemLayout
 
 // ------------------------------------------------------------------ MMA issuer
 
-__device__ __forceinline__ void issue_s(uint32_t tmem_s, uint32_t q_addr, uint32_t k_addr) {
+// The issue path is kept to a few integer operations per MMA: each operand
+// descriptor is built once per tile and every k-step adds a compile-time
+// offset (the start-address field is the low 14 bits, and no step carries out
+// of it), so the single issuing thread keeps up with the tensor core.
+__device__ __forceinline__ void issue_s(uint32_t tmem_s, uint64_t q_desc, uint64_t k_desc) {
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) {
-        const uint32_t off = (kk >> 2) * HALF_BYTES + (kk & 3) * 32;
-        ptx::umma_ss(tmem_s, ptx::desc_kmajor_sw128(q_addr + off), ptx::desc_kmajor_sw128(k_addr + off), IDESC_S,
-                     kk > 0);
+        const uint64_t off = (uint64_t)(((kk >> 2) * HALF_BYTES + (kk & 3) * 32) >> 4);
+        ptx::umma_ss(tmem_s, q_desc + off, k_desc + off, IDESC_S, kk > 0);
     }
 }
 
-__device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t tmem_p, uint32_t v_addr, bool accumulate) {
+__device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t tmem_p, uint64_t v_desc, uint32_t accumulate) {
 #pragma unroll
     for (int kk = 0; kk < BN / 16; ++kk) {
         // 16 keys per step: 8 packed bf16x2 columns of P, 16 rows (2 x 1024-B atoms) of V.
-        ptx::umma_ts(tmem_o, tmem_p + kk * 8, ptx::desc_mnmajor_sw128(v_addr + kk * 2048, HALF_BYTES), IDESC_PV,
-                     (accumulate || kk > 0) ? 1u : 0u);
+        ptx::umma_ts(tmem_o, tmem_p + kk * 8, v_desc + (uint64_t)((kk * 2048) >> 4), IDESC_PV,
+                     kk > 0 ? 1u : accumulate);
     }
 }
 
+// Static issue order S0(0), S1(0), then for every K/V tile j:
+//   PV0(j), S0(j+1), PV1(j), S1(j+1)
+// so the two softmax warpgroups alternate: while one works on its scores the
+// tensor core runs the other tile's P V and next Q K^T.  Every product waits
+// (bounded) on exactly the barriers it needs:
+//   S(n)  -- the n-th score tile, n = 2j + t -- needs K_j and the shared S
+//            buffer released by the softmax that consumed S(n-1) (s_free);
+//   PV_t(j) needs P_t(j) (p_full[t]) and V_j.
+// Ring slots are released by a commit once both products reading them are issued.
 __device__ void mma_issuer(const Unit &w, const SmemLayout &sm, const WaitCtx &wc, uint32_t tmem_base) {
     if (w.n_kv == 0) return;  // nothing to multiply (and no Q is loaded)
     if (!wait_bounded(sm.q_full(), 0, wc, kSiteMmaQ)) return;
     ptx::tc_fence_after();
-    const uint32_t q_addr[2] = {ptx::smem_addr(sm.q_tile(0)), ptx::smem_addr(sm.q_tile(1))};
-    const int total = 2 * w.n_kv;
-    int step[2] = {0, 0};
-    int krel = 0, vrel = 0;
-    uint32_t idle = 0;
-    uint64_t t_idle = 0;
-    while (step[0] < total || step[1] < total) {
-        bool progressed = false;
-#pragma unroll
-        for (int t = 0; t < 2; ++t) {
-            const int st = step[t];
-            if (st >= total) continue;
-            const int j = st >> 1;
-            const int n = (st & 1) ? 2 * j + 1 : 2 * j;
-            const int slot = n % NSLOT;
-            const uint32_t par = (n / NSLOT) & 1;
-            const uint32_t tmem_s = tmem_base + t * 256;
-            if ((st & 1) == 0) {
-                // S_t(j) = Q_t K_j^T: needs K_j and the completion of PV_t(j-1),
-                // whose P operand lives in the columns S_t(j) overwrites.
-                if (!ptx::mbar_test(sm.kv_full(slot), par)) continue;
-                if (j > 0 && !ptx::mbar_test(sm.o_full(t), (j - 1) & 1)) continue;
-                ptx::tc_fence_after();
-                issue_s(tmem_s, q_addr[t], ptx::smem_addr(sm.slot(slot)));
-                ptx::umma_commit(sm.s_full(t));
-            } else {
-                // O_t += P_t(j) V_j: needs the softmax's P_t(j) and V_j.
-                if (!ptx::mbar_test(sm.p_full(t), j & 1)) continue;
-                if (!ptx::mbar_test(sm.kv_full(slot), par)) continue;
-                ptx::tc_fence_after();
-                issue_pv(tmem_s + 128, tmem_s, ptx::smem_addr(sm.slot(slot)), j > 0);
-                ptx::umma_commit(sm.o_full(t));
-            }
-            step[t] = st + 1;
-            progressed = true;
-            // Release a ring slot once both chains have issued every product reading it.
-            const int mn = min(step[0], step[1]);
-            while (krel < w.n_kv && mn > 2 * krel) {
-                ptx::umma_commit(sm.kv_empty((2 * krel) % NSLOT));
-                ++krel;
-            }
-            while (vrel < w.n_kv && mn > 2 * vrel + 1) {
-                ptx::umma_commit(sm.kv_empty((2 * vrel + 1) % NSLOT));
-                ++vrel;
-            }
-        }
-        if (progressed) {
-            idle = 0;
-            continue;
-        }
-        if (idle == 0) t_idle = ptx::globaltimer();
-        ++idle;
-        if ((idle & 63u) == 0) {
-            if (*wc.abort_flag) return;
-            if (ptx::globaltimer() - t_idle > wc.budget_ns) {
-                *wc.abort_flag = 1;
-                report_status(wc.status, kStatusTimeout, kSiteMmaPoll);
-                return;
-            }
-        }
+    const uint64_t q_desc[2] = {ptx::desc_kmajor_sw128(ptx::smem_addr(sm.q_tile(0))),
+                                ptx::desc_kmajor_sw128(ptx::smem_addr(sm.q_tile(1)))};
+    const uint32_t slot0 = ptx::smem_addr(sm.slot(0));
+    auto slot_of = [](int n) { return n % NSLOT; };
+    auto par_of = [](int n) { return (uint32_t)((n / NSLOT) & 1); };
+
+    // One score tile: S_t(j) into the shared buffer.
+    auto do_s = [&](int t, int j) -> bool {
+        const int n = 2 * j + t;  // score tile number
+        const int item = 2 * j;   // ring item holding K_j
+        if (n > 0 && !wait_bounded(sm.s_free(), (uint32_t)((n - 1) & 1), wc, kSiteMmaPoll)) return false;
+        if (!wait_bounded(sm.kv_full(slot_of(item)), par_of(item), wc, kSiteMmaPoll)) return false;
+        ptx::tc_fence_after();
+        issue_s(tmem_base + TM_S, q_desc[t], ptx::desc_kmajor_sw128(slot0 + slot_of(item) * TILE_BYTES));
+        ptx::umma_commit(sm.s_full(t));
+        if (t == 1) ptx::umma_commit(sm.kv_empty(slot_of(item)));  // K_j done
+        return true;
+    };
+    // One P V product: O_t += P_t(j) V_j.
+    auto do_pv = [&](int t, int j) -> bool {
+        const int item = 2 * j + 1;  // ring item holding V_j
+        if (!wait_bounded(sm.p_full(t), (uint32_t)(j & 1), wc, kSiteMmaPoll)) return false;
+        if (!wait_bounded(sm.kv_full(slot_of(item)), par_of(item), wc, kSiteMmaPoll)) return false;
+        ptx::tc_fence_after();
+        issue_pv(tmem_base + tm_o(t), tmem_base + tm_p(t),
+                 ptx::desc_mnmajor_sw128(slot0 + slot_of(item) * TILE_BYTES, HALF_BYTES), j > 0 ? 1u : 0u);
+        ptx::umma_commit(sm.o_full(t));
+        if (t == 1) ptx::umma_commit(sm.kv_empty(slot_of(item)));  // V_j done
+        return true;
+    };
+
+    if (!do_s(0, 0) || !do_s(1, 0)) return;
+    for (int j = 0; j < w.n_kv; ++j) {
+        const bool more = j + 1 < w.n_kv;
+        if (!do_pv(0, j)) return;
+        if (more && !do_s(0, j + 1)) return;
+        if (!do_pv(1, j)) return;
+        if (more && !do_s(1, j + 1)) return;
     }
 }
 
 // ------------------------------------------------------------------ softmax / epilogue
 
-template <bool MASKED>
-__device__ __forceinline__ float softmax_tile(float (&s)[128], uint32_t (&pk)[64], float scale_log2, float m_sub,
-                                              int kbase, int lim_row) {
-    float rowsum = 0.f;
+// Row max of 128 scores: four independent chains of three-input max.
+__device__ __forceinline__ float row_max(const float2 (&s)[64]) {
+    float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
 #pragma unroll
-    for (int c = 0; c < 128; c += 2) {
-        float p0 = ptx::ex2(fmaf(s[c], scale_log2, -m_sub));
-        float p1 = ptx::ex2(fmaf(s[c + 1], scale_log2, -m_sub));
-        if (MASKED) {
-            p0 = (kbase + c <= lim_row) ? p0 : 0.f;
-            p1 = (kbase + c + 1 <= lim_row) ? p1 : 0.f;
-        }
-        rowsum += p0;
-        rowsum += p1;
-        pk[c >> 1] = ptx::pack_bf16x2(p0, p1);
+    for (int i = 0; i < 64; i += 4) {
+        m0 = ptx::max3(m0, s[i].x, s[i].y);
+        m1 = ptx::max3(m1, s[i + 1].x, s[i + 1].y);
+        m2 = ptx::max3(m2, s[i + 2].x, s[i + 2].y);
+        m3 = ptx::max3(m3, s[i + 3].x, s[i + 3].y);
     }
-    return rowsum;
+    return ptx::max3(m0, m1, fmaxf(m2, m3));
+}
+
+// P = exp2(s * scale_log2 - m_sub) for 128 scores, packed to bf16 pairs;
+// returns the fp32 row sum.  Pairs go through the packed fp32 FMA/ADD, the
+// sum through four independent accumulators.  MASKED: columns past the row's
+// last visible key become exactly 0.
+template <bool MASKED>
+__device__ __forceinline__ float softmax_tile(const float2 (&s)[64], uint32_t (&pk)[64], float scale_log2,
+                                              float m_sub, int kbase, int lim_row) {
+    const float2 c2 = make_float2(scale_log2, scale_log2);
+    const float2 n2 = make_float2(-m_sub, -m_sub);
+    float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+#pragma unroll
+    for (int i = 0; i < 64; ++i) {
+        const float2 t = __ffma2_rn(s[i], c2, n2);
+        float2 pp = make_float2(ptx::ex2(t.x), ptx::ex2(t.y));
+        if (MASKED) {
+            pp.x = (kbase + 2 * i <= lim_row) ? pp.x : 0.f;
+            pp.y = (kbase + 2 * i + 1 <= lim_row) ? pp.y : 0.f;
+        }
+        acc[i & 3] = __fadd2_rn(acc[i & 3], pp);
+        pk[i] = ptx::pack_bf16x2(pp.x, pp.y);
+    }
+    const float2 a = __fadd2_rn(__fadd2_rn(acc[0], acc[1]), __fadd2_rn(acc[2], acc[3]));
+    return a.x + a.y;
 }
 
 __device__ void softmax_wg(const PrefillParams &p, const Unit &w, const SmemLayout &sm, const WaitCtx &wc,
                            uint32_t tmem_base, int t, int quarter, int lane, const CUtensorMap *mo) {
     const int r = quarter * 32 + lane;  // row within the tile == TMEM lane
-    const uint32_t tS = tmem_base + ((uint32_t)(quarter * 32) << 16) + t * 256;
-    const uint32_t tO = tS + 128;
+    const uint32_t lanes = tmem_base + ((uint32_t)(quarter * 32) << 16);
+    const uint32_t tS = lanes + TM_S;     // shared score buffer
+    const uint32_t tP = lanes + tm_p(t);  // this tile's bf16 P
+    const uint32_t tO = lanes + tm_o(t);  // this tile's O accumulator
     const int s0 = w.s0[t];
     const int lim_row = p.causal ? min(s0 + r + p.Sk - p.Sq, p.Sk - 1) : p.Sk - 1;
     const int lim_tile = p.causal ? min(s0 + p.Sk - p.Sq, p.Sk - 1) : p.Sk - 1;
@@ -293,7 +323,7 @@ __device__ void softmax_wg(const PrefillParams &p, const Unit &w, const SmemLayo
             break;
         }
         ptx::tc_fence_after();
-        float s[128];
+        float2 s[64];
         {
             uint32_t a[32], b[32], c[32], d[32];
             ptx::tmem_ld32(tS + 0, a);
@@ -301,23 +331,32 @@ __device__ void softmax_wg(const PrefillParams &p, const Unit &w, const SmemLayo
             ptx::tmem_ld32(tS + 64, c);
             ptx::tmem_ld32(tS + 96, d);
             ptx::tmem_wait_ld();
+            // The scores are in registers: release the shared S buffer so the
+            // other tile's next Q K^T can start while this tile's softmax runs.
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(sm.s_free());
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                s[i] = __uint_as_float(a[i]);
-                s[32 + i] = __uint_as_float(b[i]);
-                s[64 + i] = __uint_as_float(c[i]);
-                s[96 + i] = __uint_as_float(d[i]);
+            for (int i = 0; i < 16; ++i) {
+                s[i] = make_float2(__uint_as_float(a[2 * i]), __uint_as_float(a[2 * i + 1]));
+                s[16 + i] = make_float2(__uint_as_float(b[2 * i]), __uint_as_float(b[2 * i + 1]));
+                s[32 + i] = make_float2(__uint_as_float(c[2 * i]), __uint_as_float(c[2 * i + 1]));
+                s[48 + i] = make_float2(__uint_as_float(d[2 * i]), __uint_as_float(d[2 * i + 1]));
             }
         }
         const int kbase = j * BN;
         const bool masked = kbase + BN - 1 > lim_tile;
-        float mx = -INFINITY;
+        float mx;
         if (masked) {
+            // Scores of keys the row may not see take no part in the max.
+            float2 sm2[64];
 #pragma unroll
-            for (int c = 0; c < 128; ++c) mx = (kbase + c <= lim_row) ? fmaxf(mx, s[c]) : mx;
+            for (int i = 0; i < 64; ++i) {
+                sm2[i].x = (kbase + 2 * i <= lim_row) ? s[i].x : -INFINITY;
+                sm2[i].y = (kbase + 2 * i + 1 <= lim_row) ? s[i].y : -INFINITY;
+            }
+            mx = row_max(sm2);
         } else {
-#pragma unroll
-            for (int c = 0; c < 128; ++c) mx = fmaxf(mx, s[c]);
+            mx = row_max(s);
         }
         const float m_tile = (mx == -INFINITY) ? -INFINITY : mx * sl2;
         bool need = false;
@@ -331,6 +370,15 @@ __device__ void softmax_wg(const PrefillParams &p, const Unit &w, const SmemLayo
         uint32_t pk[64];
         const float rowsum = masked ? softmax_tile<true>(s, pk, sl2, m_sub, kbase, lim_row)
                                     : softmax_tile<false>(s, pk, sl2, m_sub, kbase, lim_row);
+        // P_t(j-1) and O_t are read / written by PV_t(j-1): wait for it before
+        // overwriting P_t or rescaling O_t (normally it finished long ago).
+        if (j > 0) {
+            if (!wait_bounded(sm.o_full(t), (j - 1) & 1, wc, kSiteSoftmaxO)) {
+                ok = false;
+                break;
+            }
+            ptx::tc_fence_after();
+        }
         {
             uint32_t lo[32], hi[32];
 #pragma unroll
@@ -338,29 +386,28 @@ __device__ void softmax_wg(const PrefillParams &p, const Unit &w, const SmemLayo
                 lo[i] = pk[i];
                 hi[i] = pk[32 + i];
             }
-            ptx::tmem_st32(tS + 0, lo);
-            ptx::tmem_st32(tS + 32, hi);
+            ptx::tmem_st32(tP + 0, lo);
+            ptx::tmem_st32(tP + 32, hi);
         }
-        ptx::tmem_wait_st();
         if (j > 0 && __any_sync(0xffffffffu, need)) {
-            // O still holds the sum over tiles < j scaled by the old max: wait
-            // for PV_t(j-1) and rescale this warp's 32 rows in place.
-            if (!wait_bounded(sm.o_full(t), (j - 1) & 1, wc, kSiteSoftmaxO)) {
-                ok = false;
-                break;
-            }
-            ptx::tc_fence_after();
+            // O still holds the sum over tiles < j scaled by the old max:
+            // rescale this warp's 32 rows in place.
+            const float2 a2 = make_float2(alpha, alpha);
 #pragma unroll 1
             for (int ch = 0; ch < 4; ++ch) {
                 uint32_t o[32];
                 ptx::tmem_ld32(tO + ch * 32, o);
                 ptx::tmem_wait_ld();
 #pragma unroll
-                for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                for (int i = 0; i < 16; ++i) {
+                    const float2 v = __fmul2_rn(make_float2(__uint_as_float(o[2 * i]), __uint_as_float(o[2 * i + 1])), a2);
+                    o[2 * i] = __float_as_uint(v.x);
+                    o[2 * i + 1] = __float_as_uint(v.y);
+                }
                 ptx::tmem_st32(tO + ch * 32, o);
             }
-            ptx::tmem_wait_st();
         }
+        ptx::tmem_wait_st();
         l_run = l_run * alpha + rowsum;
         m_run = m_new;
         ptx::tc_fence_before();
@@ -385,9 +432,10 @@ __device__ void softmax_wg(const PrefillParams &p, const Unit &w, const SmemLayo
             uint32_t wv[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
-                const float x0 = l_run > 0.f ? __uint_as_float(o[2 * i]) * inv : 0.f;
-                const float x1 = l_run > 0.f ? __uint_as_float(o[2 * i + 1]) * inv : 0.f;
-                wv[i] = ptx::pack_bf16x2(x0, x1);
+                float2 x = __fmul2_rn(make_float2(__uint_as_float(o[2 * i]), __uint_as_float(o[2 * i + 1])),
+                                      make_float2(inv, inv));
+                if (!(l_run > 0.f)) x = make_float2(0.f, 0.f);
+                wv[i] = ptx::pack_bf16x2(x.x, x.y);
             }
             // 32 columns = 64 bytes = four 16-byte chunks of the 128-B swizzled row.
             uint8_t *rowp = stage + (ch >> 1) * HALF_BYTES + r * 128;
@@ -443,6 +491,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             ptx::mbar_init(sm.p_full(t), 128);
             ptx::mbar_init(sm.o_full(t), 1);
         }
+        ptx::mbar_init(sm.s_free(), 128);
         ptx::mbar_init(sm.fin(), 1);
         *sm.abort_flag() = 0;
         ptx::fence_mbar_init();
@@ -461,20 +510,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t tmem_base = *sm.tmem_slot();
     const WaitCtx wc{sm.abort_flag(), p.status, p.budget_ns};
 
-    if (warp == 0) {
-        if (lane == 0) producer(p, w, sm, wc, &map_q, &map_k, &map_v);
-        __syncwarp();
-    } else if (warp == 1) {
-        if (lane == 0) {
-            mma_issuer(w, sm, wc, tmem_base);
-            // Whatever happened, wait until every product issued has completed
-            // before tensor memory is released.
-            ptx::umma_commit(sm.fin());
-            drain_wait(sm.fin(), 0, wc);
+    if (warp < 4) {
+        ptx::setmaxnreg_dec<REGS_CONTROL>();
+        if (warp == 0) {
+            if (lane == 0) producer(p, w, sm, wc, &map_q, &map_k, &map_v);
+        } else if (warp == 1) {
+            if (lane == 0) {
+                mma_issuer(w, sm, wc, tmem_base);
+                // Whatever happened, wait until every product issued has
+                // completed before tensor memory is released.
+                ptx::umma_commit(sm.fin());
+                drain_wait(sm.fin(), 0, wc);
+            }
         }
         __syncwarp();
     } else {
-        const int t = (warp - 2) >> 2;
+        ptx::setmaxnreg_inc<REGS_SOFTMAX>();
+        const int t = (warp - 4) >> 2;
         softmax_wg(p, w, sm, wc, tmem_base, t, warp & 3, lane, &map_o);
         __syncwarp();
     }
