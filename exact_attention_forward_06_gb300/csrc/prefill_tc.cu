@@ -25,7 +25,7 @@
 // in turn, a bf16 probability buffer P_t per tile (64 columns of packed
 // pairs, read by the P V product straight from tensor memory) and an fp32
 // output accumulator O_t per tile.  The MMA thread issues, for every K/V tile
-// j, PV_0(j), S_0(j+1), PV_1(j), S_1(j+1): while one tile's softmax runs, the
+// j, S_0(j+1), PV_0(j), S_1(j+1), PV_1(j): while one tile's softmax runs, the
 // tensor core works on the other tile's products, and a softmax releases S as
 // soon as it has loaded its scores (the two-group alternation of the MoonMath
 // page, realised as two Q tiles instead of two wave groups).
@@ -210,7 +210,7 @@ __device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t tmem_p, uint6
 }
 
 // Static issue order S0(0), S1(0), then for every K/V tile j:
-//   PV0(j), S0(j+1), PV1(j), S1(j+1)
+//   S0(j+1), PV0(j), S1(j+1), PV1(j)
 // so the two softmax warpgroups alternate: while one works on its scores the
 // tensor core runs the other tile's P V and next Q K^T.  Every product waits
 // (bounded) on exactly the barriers it needs:
@@ -253,13 +253,17 @@ __device__ void mma_issuer(const Unit &w, const SmemLayout &sm, const WaitCtx &w
         return true;
     };
 
+    // S production is the tight loop: each score tile needs the previous one
+    // loaded out of the shared buffer, so S0(j+1) goes out as soon as tile 1's
+    // softmax has read S1(j), before PV0(j) (which waits for tile 0's whole
+    // softmax).  The P V products fill the gaps.
     if (!do_s(0, 0) || !do_s(1, 0)) return;
     for (int j = 0; j < w.n_kv; ++j) {
         const bool more = j + 1 < w.n_kv;
-        if (!do_pv(0, j)) return;
         if (more && !do_s(0, j + 1)) return;
-        if (!do_pv(1, j)) return;
+        if (!do_pv(0, j)) return;
         if (more && !do_s(1, j + 1)) return;
+        if (!do_pv(1, j)) return;
     }
 }
 
@@ -303,6 +307,14 @@ __device__ __forceinline__ float softmax_tile(const float2 (&s)[64], uint32_t (&
     return a.x + a.y;
 }
 
+// Hand a barrier one arrival for the whole warp once every lane's tensor-memory
+// accesses are complete.
+__device__ __forceinline__ void warp_arrive(uint64_t *bar, int lane) {
+    ptx::tc_fence_before();
+    __syncwarp();
+    if (lane == 0) ptx::mbar_arrive(bar);
+}
+
 __device__ void softmax_wg(const PrefillParams &p, const Unit &w, const SmemLayout &sm, const WaitCtx &wc,
                            uint32_t tmem_base, int t, int quarter, int lane, const CUtensorMap *mo) {
     const int r = quarter * 32 + lane;  // row within the tile == TMEM lane
@@ -333,8 +345,7 @@ __device__ void softmax_wg(const PrefillParams &p, const Unit &w, const SmemLayo
             ptx::tmem_wait_ld();
             // The scores are in registers: release the shared S buffer so the
             // other tile's next Q K^T can start while this tile's softmax runs.
-            ptx::tc_fence_before();
-            ptx::mbar_arrive(sm.s_free());
+            warp_arrive(sm.s_free(), lane);
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
                 s[i] = make_float2(__uint_as_float(a[2 * i]), __uint_as_float(a[2 * i + 1]));
@@ -410,8 +421,7 @@ __device__ void softmax_wg(const PrefillParams &p, const Unit &w, const SmemLayo
         ptx::tmem_wait_st();
         l_run = l_run * alpha + rowsum;
         m_run = m_new;
-        ptx::tc_fence_before();
-        ptx::mbar_arrive(sm.p_full(t));
+        warp_arrive(sm.p_full(t), lane);
     }
 
     // Epilogue: O / l -> bf16 into the (now free) Q tile buffer, then TMA store.
@@ -486,12 +496,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             ptx::mbar_init(sm.kv_full(s), 1);
             ptx::mbar_init(sm.kv_empty(s), 1);
         }
+        // Softmax-side barriers take one arrival per warp (lane 0, after the
+        // warp's tcgen05 fence and __syncwarp).
         for (int t = 0; t < 2; ++t) {
             ptx::mbar_init(sm.s_full(t), 1);
-            ptx::mbar_init(sm.p_full(t), 128);
+            ptx::mbar_init(sm.p_full(t), 4);
             ptx::mbar_init(sm.o_full(t), 1);
         }
-        ptx::mbar_init(sm.s_free(), 128);
+        ptx::mbar_init(sm.s_free(), 4);
         ptx::mbar_init(sm.fin(), 1);
         *sm.abort_flag() = 0;
         ptx::fence_mbar_init();
