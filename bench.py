@@ -176,6 +176,10 @@ def run_ours(args, rank, world, local_rank):
     dout = torch.empty_like(dq)
     dlse = torch.empty((wd.B, wd.Hq), device=dev, dtype=torch.float32)
     ws = torch.empty(A.decode_workspace_bytes(wd.B, wd.Hq, wd.d, wd.max_blocks), device=dev, dtype=torch.uint8)
+    # Workspace for the prefill's tail split, when the shape gets one on this device.
+    fws_bytes = A.fwd_workspace_bytes(wp.B, wp.Hq, wp.Hkv, wp.Sq, wp.Sk, wp.d, wp.causal)
+    fws = torch.empty(fws_bytes, device=dev, dtype=torch.uint8) if fws_bytes else None
+    A.set_workspace(fws)
     stream = torch.cuda.current_stream(dev)
 
     def prefill():
@@ -252,6 +256,7 @@ def run_ours(args, rank, world, local_rank):
                    "page_size": wd.page_size, "l2": "inputs larger than L2 (no flush)",
                    "parallelism": f"replicas x{world}"},
         "prefill_ms_per_launch": round(prefill_ms, 4),
+        "prefill_tail_split_workspace_bytes": fws_bytes,
         "roofline": {"bound": "tensor", "achieved": round(per_launch_tflops, 2),
                      "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                      "frac": round(per_launch_tflops / peaks["bf16_tflops"], 4),
@@ -265,7 +270,7 @@ def run_ours(args, rank, world, local_rank):
                                 "kernel": "attn::dec::split_kernel + merge_kernel",
                                 "algorithmic": f"{kv_bytes} B K+V per launch (4096 B per token)"}},
         "e2e": e2e,
-        "gpu_launches": 3 * K,
+        "gpu_launches": (4 if fws_bytes else 3) * K,
         "clocks": clk,
     }
     if not args.no_cpu_baseline and world == 1:

@@ -51,6 +51,10 @@ def load():
             fwd_args = [_p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _i, _f, _p]
             lib.attn_fwd.argtypes = fwd_args
             lib.attn_fwd_simple.argtypes = fwd_args
+            lib.attn_fwd_workspace_bytes.argtypes = [_i, _i, _i, _i, _i, _i, _i]
+            lib.attn_fwd_workspace_bytes.restype = _sz
+            lib.attn_set_workspace.argtypes = [_p, _sz]
+            lib.attn_set_workspace.restype = _i
             lib.attn_decode_workspace_bytes.argtypes = [_i, _i, _i, _i]
             lib.attn_decode_workspace_bytes.restype = _sz
             lib.attn_decode_paged.argtypes = [_p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _f, _p,
@@ -140,6 +144,23 @@ def fwd(q, k, v, *, causal=False, scale=None, layout="bshd", out=None, lse=None,
 def fwd_simple(q, k, v, *, causal=False, scale=None, layout="bshd", out=None, lse=None, stream=None):
     """The same operation through the plain SIMT kernel (debugging cross-check; slow)."""
     return _fwd_call("attn_fwd_simple", q, k, v, causal, scale, layout, out, lse, stream)
+
+
+def fwd_workspace_bytes(B: int, Hq: int, Hkv: int, Sq: int, Sk: int, d: int = 128, causal: bool = False) -> int:
+    """Workspace bytes that let attn_fwd split its last wave of work for this shape (current device)."""
+    return int(load().attn_fwd_workspace_bytes(B, Hq, Hkv, Sq, Sk, d, int(bool(causal))))
+
+
+def set_workspace(buf=None):
+    """Register a CUDA uint8 tensor (or None to clear) as the current device's attn_fwd workspace.
+
+    The caller keeps ownership and must keep the tensor alive while it is registered.
+    """
+    if buf is None:
+        _check(load().attn_set_workspace(None, 0), "attn_set_workspace")
+        return
+    _dev_tensor(buf, "workspace", torch.uint8)
+    _check(load().attn_set_workspace(buf.data_ptr(), buf.numel()), "attn_set_workspace")
 
 
 def decode_workspace_bytes(B: int, Hq: int, d: int, max_blocks_per_seq: int) -> int:

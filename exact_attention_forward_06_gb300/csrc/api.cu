@@ -28,6 +28,8 @@ struct DeviceInfo {
     bool supported = false;
     int sm_count = 0;
     unsigned *status = nullptr;
+    void *workspace = nullptr;  // caller-owned, for attn_fwd's tail split
+    size_t workspace_bytes = 0;
 };
 
 std::mutex g_mu;
@@ -150,6 +152,11 @@ attn_status_t fill_prefill_params(attn::PrefillParams *p, const DeviceInfo *di, 
     p->status = di->status;
     p->budget_ns = budget();
     p->inject = 0;
+    p->n_full_units = attn::prefill_num_units(*p);
+    p->split_units = 0;
+    p->split_parts = 1;
+    p->ws_o = nullptr;
+    p->ws_lse = nullptr;
     return ATTN_OK;
 }
 
@@ -172,8 +179,49 @@ attn_status_t attn_fwd(const void *q, const void *k, const void *v, void *out, f
         !make_map_4d(&mv, v, bhsd, B, Sk, Hkv, d, 128) || !make_map_4d(&mo, out, bhsd, B, Sq, Hq, d, 128))
         return ATTN_ERR_CUDA;
     const int units = attn::prefill_num_units(p);
-    if (attn::launch_prefill(mq, mk, mv, mo, p, units, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    int ctas = units;
+    {
+        // Tail split, when the shape calls for one and the caller has set a
+        // large enough workspace on this device; otherwise whole units only.
+        int su = 0, parts = 1;
+        const size_t need = attn::prefill_split_plan(p, di->sm_count, &su, &parts);
+        std::lock_guard<std::mutex> lock(g_mu);
+        if (su > 0 && di->workspace != nullptr && di->workspace_bytes >= need) {
+            const size_t rows = (size_t)su * 256;
+            size_t o_bytes = rows * parts * 128 * 4;
+            o_bytes = (o_bytes + 255) & ~(size_t)255;
+            p.n_full_units = units - su;
+            p.split_units = su;
+            p.split_parts = parts;
+            p.ws_o = static_cast<float *>(di->workspace);
+            p.ws_lse = reinterpret_cast<float *>(static_cast<uint8_t *>(di->workspace) + o_bytes);
+            ctas = p.n_full_units + su * parts;
+        }
+    }
+    if (attn::launch_prefill(mq, mk, mv, mo, p, ctas, static_cast<cudaStream_t>(stream)) != cudaSuccess)
         return ATTN_ERR_CUDA;
+    if (attn::launch_prefill_merge(out, p, static_cast<cudaStream_t>(stream)) != cudaSuccess) return ATTN_ERR_CUDA;
+    return ATTN_OK;
+}
+
+size_t attn_fwd_workspace_bytes(int B, int Hq, int Hkv, int Sq, int Sk, int d, int causal) {
+    if (B < 1 || Hq < 1 || Hkv < 1 || Sq < 1 || Sk < 1 || d != 128 || Hq % Hkv != 0) return 0;
+    DeviceInfo *di = nullptr;
+    if (device_info(&di) != ATTN_OK) return 0;
+    attn::PrefillParams p;
+    fill_prefill_params(&p, di, nullptr, B, Hq, Hkv, Sq, Sk, ATTN_LAYOUT_BSHD, causal, 1.0f);
+    int su = 0, parts = 1;
+    return attn::prefill_split_plan(p, di->sm_count, &su, &parts);
+}
+
+attn_status_t attn_set_workspace(void *ptr, size_t bytes) {
+    if (ptr != nullptr && (reinterpret_cast<uintptr_t>(ptr) & 255u)) return ATTN_ERR_INVALID_ARG;
+    DeviceInfo *di = nullptr;
+    attn_status_t st = device_info(&di);
+    if (st != ATTN_OK) return st;
+    std::lock_guard<std::mutex> lock(g_mu);
+    di->workspace = ptr;
+    di->workspace_bytes = ptr != nullptr ? bytes : 0;
     return ATTN_OK;
 }
 

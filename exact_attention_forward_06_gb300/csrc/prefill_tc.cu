@@ -39,6 +39,7 @@
 // the previous P V product has completed.
 #include <cstdint>
 #include <cuda.h>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include "common.cuh"
@@ -105,10 +106,14 @@ struct Unit {
     int b, g;
     int h[2];
     int s0[2];
-    int n_kv;
+    int n_kv;    // K/V tiles this CTA processes
+    int j_lo;    // first K/V tile (absolute)
+    int part;    // key-range part of a split unit, -1 for a whole unit
+    int ws_row;  // first workspace row of a split unit (256 rows per unit)
 };
 
-__device__ __forceinline__ Unit decode_unit(const PrefillParams &p, int u) {
+// Heads, rows and K/V tile count of work unit u (two 128-row Q tiles).
+__host__ __device__ __forceinline__ Unit unit_coords(const PrefillParams &p, int u) {
     Unit w;
     int m_step;
     if (p.pair_heads) {
@@ -139,13 +144,33 @@ __device__ __forceinline__ Unit decode_unit(const PrefillParams &p, int u) {
     const int n_full = (p.Sk + BN - 1) / BN;
     if (p.causal) {
         int last_row = w.s0[0] + BM - 1;
-        if (w.s0[1] < p.Sq) last_row = max(last_row, w.s0[1] + BM - 1);
-        last_row = min(last_row, p.Sq - 1);
+        if (w.s0[1] < p.Sq) last_row = last_row > w.s0[1] + BM - 1 ? last_row : w.s0[1] + BM - 1;
+        last_row = last_row < p.Sq - 1 ? last_row : p.Sq - 1;
         const int lim = last_row + p.Sk - p.Sq;  // last visible key of the lowest row
-        w.n_kv = lim < 0 ? 0 : min(n_full, lim / BN + 1);
+        w.n_kv = lim < 0 ? 0 : (n_full < lim / BN + 1 ? n_full : lim / BN + 1);
     } else {
         w.n_kv = n_full;
     }
+    w.j_lo = 0;
+    w.part = -1;
+    w.ws_row = 0;
+    return w;
+}
+
+// The unit (and key range) CTA number cta works on.  CTAs past the whole
+// units are the parts of the tail units, part-major within a unit.
+__device__ __forceinline__ Unit decode_unit(const PrefillParams &p, int cta) {
+    if (cta < p.n_full_units) return unit_coords(p, cta);
+    const int v = cta - p.n_full_units;
+    const int su = v / p.split_parts;
+    const int part = v % p.split_parts;
+    Unit w = unit_coords(p, p.n_full_units + su);
+    const int lo = part * w.n_kv / p.split_parts;
+    const int hi = (part + 1) * w.n_kv / p.split_parts;
+    w.j_lo = lo;
+    w.n_kv = hi - lo;
+    w.part = part;
+    w.ws_row = su * 2 * BM;
     return w;
 }
 
@@ -178,7 +203,8 @@ __device__ void producer(const PrefillParams &p, const Unit &w, const SmemLayout
         const int round = n / NSLOT;
         if (round > 0 && !wait_bounded(sm.kv_empty(slot), (round - 1) & 1, wc, kSiteProducerEmpty)) break;
         ptx::mbar_arrive_expect_tx(sm.kv_full(slot), TILE_BYTES);
-        load_tile((n & 1) ? mv : mk, sm.slot(slot), sm.kv_full(slot), p.bhsd, w.g, (n >> 1) * BN, w.b, pol_kv);
+        load_tile((n & 1) ? mv : mk, sm.slot(slot), sm.kv_full(slot), p.bhsd, w.g, (w.j_lo + (n >> 1)) * BN, w.b,
+                  pol_kv);
         ++issued;
     }
     // On the way out make sure no copy is still writing into shared memory.
@@ -354,7 +380,7 @@ __device__ void softmax_wg(const PrefillParams &p, const Unit &w, const SmemLayo
                 s[48 + i] = make_float2(__uint_as_float(d[2 * i]), __uint_as_float(d[2 * i + 1]));
             }
         }
-        const int kbase = j * BN;
+        const int kbase = (w.j_lo + j) * BN;  // absolute first key of this tile
         const bool masked = kbase + BN - 1 > lim_tile;
         float mx;
         if (masked) {
@@ -431,7 +457,28 @@ __device__ void softmax_wg(const PrefillParams &p, const Unit &w, const SmemLayo
     // checks it after the barrier.
     if (ok && w.n_kv > 0) ok = wait_bounded(sm.o_full(t), (w.n_kv - 1) & 1, wc, kSiteEpilogueO);
     uint8_t *stage = sm.q_tile(t);
-    if (ok) {
+    if (ok && w.part >= 0) {
+        // A key-range part of a split unit: its O (normalised within the range)
+        // and log-sum-exp go to the workspace in fp32 for the merge kernel.
+        ptx::tc_fence_after();
+        const float inv = l_run > 0.f ? 1.0f / l_run : 0.f;
+        const int64_t row = w.ws_row + t * BM + r;
+        float4 *dst = reinterpret_cast<float4 *>(p.ws_o + (row * p.split_parts + w.part) * D);
+#pragma unroll 1
+        for (int ch = 0; ch < 4; ++ch) {
+            uint32_t o[32];
+            ptx::tmem_ld32(tO + ch * 32, o);
+            ptx::tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                float4 x = make_float4(__uint_as_float(o[4 * i]) * inv, __uint_as_float(o[4 * i + 1]) * inv,
+                                       __uint_as_float(o[4 * i + 2]) * inv, __uint_as_float(o[4 * i + 3]) * inv);
+                if (!(l_run > 0.f)) x = make_float4(0.f, 0.f, 0.f, 0.f);
+                dst[ch * 8 + i] = x;
+            }
+        }
+        p.ws_lse[row * p.split_parts + w.part] = l_run > 0.f ? (m_run + ptx::lg2(l_run)) * LN2 : -INFINITY;
+    } else if (ok) {
         ptx::tc_fence_after();
         const float inv = l_run > 0.f ? 1.0f / l_run : 0.f;
 #pragma unroll 1
@@ -464,7 +511,7 @@ __device__ void softmax_wg(const PrefillParams &p, const Unit &w, const SmemLayo
     }
     ptx::fence_proxy_async_smem();
     ptx::named_bar_sync(1 + t, 128);
-    if (quarter == 0 && lane == 0 && s0 < p.Sq && !*wc.abort_flag) {
+    if (quarter == 0 && lane == 0 && s0 < p.Sq && w.part < 0 && !*wc.abort_flag) {
         const Coord4 lo = coord4(p.bhsd, 0, w.h[t], s0, w.b);
         const Coord4 hi = coord4(p.bhsd, 64, w.h[t], s0, w.b);
         ptx::tma_store_4d(mo, stage, lo.c0, lo.c1, lo.c2, lo.c3);
@@ -556,7 +603,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 int prefill_smem_bytes() { return (int)(g1::SMEM_TILES + g1::SMEM_MISC + g1::SMEM_ALIGN); }
 
 cudaError_t launch_prefill(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
-                           const CUtensorMap &mo, const PrefillParams &p, int num_units, cudaStream_t stream) {
+                           const CUtensorMap &mo, const PrefillParams &p, int num_ctas, cudaStream_t stream) {
     const int smem = prefill_smem_bytes();
     static thread_local int configured_device = -1;
     int dev = 0;
@@ -567,13 +614,81 @@ cudaError_t launch_prefill(const CUtensorMap &mq, const CUtensorMap &mk, const C
         if (e != cudaSuccess) return e;
         configured_device = dev;
     }
-    g1::prefill_kernel<<<num_units, g1::NUM_THREADS, smem, stream>>>(mq, mk, mv, mo, p);
+    g1::prefill_kernel<<<num_ctas, g1::NUM_THREADS, smem, stream>>>(mq, mk, mv, mo, p);
     return cudaGetLastError();
 }
 
 int prefill_num_units(const PrefillParams &p) {
     if (p.pair_heads) return p.B * p.Hkv * (p.G / 2) * p.n_m;
     return p.B * p.Hq * ((p.n_m + 1) / 2);
+}
+
+// Tail split (the Flash-Decoding style split of the MoonMath page, applied to
+// the prefill's last wave).  CTAs are dispatched in index order and one fits
+// per SM, so the last units % num_sms units run as a partial final wave.
+// When every unit has the same length (non-causal) and that wave would leave
+// SMs idle, each of those units is cut into parts key ranges (at least 4 K/V
+// tiles each) so that the last wave fills the SMs.  Causal launches run
+// longest units first and end on short units, so they are left whole.
+size_t prefill_split_plan(const PrefillParams &p, int num_sms, int *split_units, int *split_parts) {
+    *split_units = 0;
+    *split_parts = 1;
+    const int units = prefill_num_units(p);
+    const int n_kv = (p.Sk + g1::BN - 1) / g1::BN;
+    if (p.causal || num_sms < 2 || n_kv < 8) return 0;
+    const int tail = units % num_sms;
+    if (tail == 0) return 0;
+    int parts = num_sms / tail;
+    if (parts > n_kv / 4) parts = n_kv / 4;
+    if (parts < 2) return 0;
+    *split_units = tail;
+    *split_parts = parts;
+    const size_t rows = (size_t)tail * 2 * g1::BM;
+    size_t o_bytes = rows * parts * g1::D * 4;
+    o_bytes = (o_bytes + 255) & ~(size_t)255;
+    size_t l_bytes = rows * parts * 4;
+    l_bytes = (l_bytes + 255) & ~(size_t)255;
+    return o_bytes + l_bytes;
+}
+
+namespace g1 {
+
+// One CTA per row of the split units, one thread per head-dim element: merge
+// the key-range partials in part order (deterministic) and write the row of O
+// in q's layout, rounded to bf16, and its log-sum-exp.
+__global__ void __launch_bounds__(D) merge_kernel(__nv_bfloat16 *__restrict__ out, const PrefillParams p) {
+    const int row = blockIdx.x;  // within the split units
+    const int su = row / (2 * BM);
+    const int t = (row / BM) & 1;
+    const int r = row % BM;
+    const Unit w = unit_coords(p, p.n_full_units + su);
+    const int s = w.s0[t] + r;
+    if (s >= p.Sq) return;
+    const int h = w.h[t];
+    const int e = threadIdx.x;
+    const float *ls = p.ws_lse + (int64_t)row * p.split_parts;
+    float M = -INFINITY;
+    for (int k = 0; k < p.split_parts; ++k) M = fmaxf(M, ls[k]);
+    float total = 0.f, o = 0.f;
+    if (M != -INFINITY) {
+        for (int k = 0; k < p.split_parts; ++k) {
+            const float wk = ptx::ex2((ls[k] - M) * 1.4426950408889634f);
+            total += wk;
+            o = fmaf(wk, p.ws_o[((int64_t)row * p.split_parts + k) * D + e], o);
+        }
+    }
+    const int64_t off = p.bhsd ? (((int64_t)w.b * p.Hq + h) * p.Sq + s) * D : (((int64_t)w.b * p.Sq + s) * p.Hq + h) * D;
+    out[off + e] = __float2bfloat16_rn(total > 0.f ? o / total : 0.f);
+    if (e == 0 && p.lse != nullptr)
+        p.lse[((int64_t)w.b * p.Hq + h) * p.Sq + s] = total > 0.f ? M + ptx::lg2(total) * LN2 : -INFINITY;
+}
+
+}  // namespace g1
+
+cudaError_t launch_prefill_merge(void *out, const PrefillParams &p, cudaStream_t stream) {
+    if (p.split_units == 0) return cudaSuccess;
+    g1::merge_kernel<<<p.split_units * 2 * g1::BM, g1::D, 0, stream>>>(static_cast<__nv_bfloat16 *>(out), p);
+    return cudaGetLastError();
 }
 
 }  // namespace attn

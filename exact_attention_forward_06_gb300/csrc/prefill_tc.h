@@ -19,12 +19,26 @@ struct PrefillParams {
     unsigned *status;  // device status word [code, site]
     uint64_t budget_ns;
     int inject;        // 1: producer issues nothing (fault-injection test)
+    // Tail split: units [0, n_full_units) run whole; each of the following
+    // split_units units is cut into split_parts key ranges, one CTA each, whose
+    // fp32 partials go to ws_o [split_units*256][split_parts][128] and
+    // ws_lse [split_units*256][split_parts] and are merged afterwards.
+    int n_full_units;
+    int split_units;
+    int split_parts;
+    float *ws_o;
+    float *ws_lse;
 };
 
 int prefill_smem_bytes();
 int prefill_num_units(const PrefillParams &p);
 cudaError_t launch_prefill(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
-                           const CUtensorMap &mo, const PrefillParams &p, int num_units, cudaStream_t stream);
+                           const CUtensorMap &mo, const PrefillParams &p, int num_ctas, cudaStream_t stream);
+// Merge of the tail-split partials into out (q's layout) and lse.
+cudaError_t launch_prefill_merge(void *out, const PrefillParams &p, cudaStream_t stream);
+// Tail-split plan for a shape on a device with num_sms SMs: split_units and
+// split_parts (0 / 1 when no split is worth it) and the workspace it needs.
+size_t prefill_split_plan(const PrefillParams &p, int num_sms, int *split_units, int *split_parts);
 
 // Plain SIMT kernel, one warp per query row (debugging cross-check).
 cudaError_t launch_prefill_simple(const void *q, const void *k, const void *v, void *out, float *lse,

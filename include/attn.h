@@ -28,8 +28,9 @@
  * Conventions for every entry point:
  *   - Pointers named q, k, v, out, lse, k_pages, v_pages, block_table, seqlens,
  *     workspace, o_parts, lse_parts are DEVICE pointers owned by the caller;
- *     the library never frees or keeps them past the call.  The library
- *     allocates no device memory on any call.
+ *     the library never frees them and keeps none past the call, except the
+ *     workspace registered with attn_set_workspace.  The library allocates no
+ *     device memory on any call.
  *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Work is
  *     enqueued asynchronously; only attn_get_device_status synchronises.
  *   - bf16 tensors are dense and contiguous; every device pointer must be
@@ -85,6 +86,28 @@ attn_status_t attn_fwd(const void *q, const void *k, const void *v, void *out, f
                        int layout, int causal, float scale, void *stream);
 
 /*
+ * attn_fwd_workspace_bytes -- device workspace that lets attn_fwd split the
+ * key ranges of its last wave of work units (the Flash-Decoding style tail
+ * split of the MoonMath page: the partial results are merged by log-sum-exp)
+ * for this shape on the CURRENT device (the plan depends on its SM count).
+ * Returns 0 when the shape gets no split (causal shapes, shapes whose units
+ * fill the last wave, short key ranges) or the arguments are invalid.
+ */
+size_t attn_fwd_workspace_bytes(int B, int Hq, int Hkv, int Sq, int Sk, int d, int causal);
+
+/*
+ * attn_set_workspace -- register a caller-owned device buffer as the current
+ * device's workspace for attn_fwd's tail split (NULL clears it).  ptr must be
+ * 256-byte aligned; the library keeps the pointer until it is replaced or
+ * cleared and never frees it.  attn_fwd splits only when a registered buffer
+ * is at least attn_fwd_workspace_bytes(...) large; otherwise it runs every
+ * unit whole, with the same result to within rounding.  The buffer is used by
+ * every attn_fwd on the device: calls that overlap on the GPU must not share
+ * one (give each stream its own, or order the streams).
+ */
+attn_status_t attn_set_workspace(void *ptr, size_t bytes);
+
+/*
  * attn_fwd_simple -- the same operation and contract as attn_fwd, computed by
  * a plain SIMT CUDA kernel (one warp per query row, no tensor cores).  It is
  * a debugging cross-check for attn_fwd, not a fallback: nothing routes to it
@@ -97,7 +120,7 @@ attn_status_t attn_fwd_simple(const void *q, const void *k, const void *v, void 
 /*
  * attn_decode_workspace_bytes -- bytes of device workspace attn_decode_paged
  * needs for this shape.  A pure function of the arguments (the key-split plan
- * depends only on the shape and the device's SM count, never on device data).
+ * depends only on the shape, never on device data).
  * Returns 0 for invalid arguments.
  */
 size_t attn_decode_workspace_bytes(int B, int Hq, int d, int max_blocks_per_seq);

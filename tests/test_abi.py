@@ -110,3 +110,10 @@ def test_debug_controls(lib):
     assert lib.attn_debug_inject(7) == 1
     assert lib.attn_debug_inject(0) == 0
     assert lib.attn_set_wait_budget_ns(0) == 0
+
+
+def test_fwd_workspace_query_and_registration_validate(lib):
+    assert lib.attn_fwd_workspace_bytes(0, 1, 1, 8, 8, 128, 0) == 0
+    assert lib.attn_fwd_workspace_bytes(1, 3, 2, 8, 8, 128, 0) == 0
+    assert lib.attn_fwd_workspace_bytes(1, 2, 2, 8, 8, 64, 0) == 0
+    assert lib.attn_set_workspace(264, 1024) == 1     # not 256-byte aligned
