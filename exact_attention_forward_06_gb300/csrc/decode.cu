@@ -52,6 +52,14 @@ constexpr float RESCALE_LOG2 = 8.0f;
 constexpr float LN2 = 0.6931471805599453f;
 constexpr float LOG2E = 1.4426950408889634f;
 
+// Eight bf16 values (one 16-byte chunk) as four fp32 pairs, in element order.
+__device__ __forceinline__ void bf16x8_to_float2(const uint4 &u, float2 *x) {
+    x[0] = make_float2(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u));
+    x[1] = make_float2(__uint_as_float(u.y << 16), __uint_as_float(u.y & 0xffff0000u));
+    x[2] = make_float2(__uint_as_float(u.z << 16), __uint_as_float(u.z & 0xffff0000u));
+    x[3] = make_float2(__uint_as_float(u.w << 16), __uint_as_float(u.w & 0xffff0000u));
+}
+
 __device__ __forceinline__ void bf16x8_to_float(const uint4 &u, float *x) {
     x[0] = __uint_as_float(u.x << 16);
     x[1] = __uint_as_float(u.x & 0xffff0000u);
@@ -140,23 +148,27 @@ __global__ void __launch_bounds__(NTHREADS, 3)
         // ---------------- consumers
         const int tg = lane >> 3;  // token group
         const int ds = lane & 7;   // head-dim chunks ds and 8 + ds
-        float qf[GH][16];
+        // Dot products and the P V accumulation run on fp32 pairs (packed
+        // FFMA2): element pairs (2i, 2i+1) of the lane's 16 head-dim elements.
+        float2 qf[GH][8];
 #pragma unroll
         for (int h = 0; h < GH; ++h) {
             const uint4 *qp = reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(p.q) +
                                                               (row0 + h) * D);
-            bf16x8_to_float(qp[ds], qf[h]);
-            bf16x8_to_float(qp[8 + ds], qf[h] + 8);
+            bf16x8_to_float2(qp[ds], qf[h]);
+            bf16x8_to_float2(qp[8 + ds], qf[h] + 4);
+            const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
 #pragma unroll
-            for (int e = 0; e < 16; ++e) qf[h][e] *= p.scale_log2;
+            for (int e = 0; e < 8; ++e) qf[h][e] = __fmul2_rn(qf[h][e], sc2);
         }
-        float m[GH], lsum[GH], acc[GH][16];
+        float m[GH], lsum[GH];
+        float2 acc[GH][8];
 #pragma unroll
         for (int h = 0; h < GH; ++h) {
             m[h] = -INFINITY;
             lsum[h] = 0.f;
 #pragma unroll
-            for (int e = 0; e < 16; ++e) acc[h][e] = 0.f;
+            for (int e = 0; e < 8; ++e) acc[h][e] = make_float2(0.f, 0.f);
         }
         for (int i = warp; i < np; i += NCW) {
             const int slot = i % NST;
@@ -170,14 +182,15 @@ __global__ void __launch_bounds__(NTHREADS, 3)
             for (int ps = 0; ps < 4; ++ps) {
                 const int t = ps * 4 + tg;
                 const uint4 *kp = reinterpret_cast<const uint4 *>(ks + t * (D * 2));
-                float kf[16];
-                bf16x8_to_float(kp[ds], kf);
-                bf16x8_to_float(kp[8 + ds], kf + 8);
+                float2 kf[8];
+                bf16x8_to_float2(kp[ds], kf);
+                bf16x8_to_float2(kp[8 + ds], kf + 4);
 #pragma unroll
                 for (int h = 0; h < GH; ++h) {
-                    float dot = 0.f;
+                    float2 d2 = __fmul2_rn(qf[h][0], kf[0]);
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) dot = fmaf(qf[h][e], kf[e], dot);
+                    for (int e = 1; e < 8; ++e) d2 = __ffma2_rn(qf[h][e], kf[e], d2);
+                    float dot = d2.x + d2.y;
                     dot += __shfl_xor_sync(0xffffffffu, dot, 1);
                     dot += __shfl_xor_sync(0xffffffffu, dot, 2);
                     dot += __shfl_xor_sync(0xffffffffu, dot, 4);
@@ -194,7 +207,7 @@ __global__ void __launch_bounds__(NTHREADS, 3)
                     const float alpha = ptx::ex2(m[h] - pm);
                     lsum[h] *= alpha;
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) acc[h][e] *= alpha;
+                    for (int e = 0; e < 8; ++e) acc[h][e] = __fmul2_rn(acc[h][e], make_float2(alpha, alpha));
                     m[h] = pm;
                 }
                 const float msub = (m[h] == -INFINITY) ? 0.f : m[h];
@@ -208,13 +221,15 @@ __global__ void __launch_bounds__(NTHREADS, 3)
             for (int ps = 0; ps < 4; ++ps) {
                 const int t = ps * 4 + tg;
                 const uint4 *vp = reinterpret_cast<const uint4 *>(vs + t * (D * 2));
-                float vf[16];
-                bf16x8_to_float(vp[ds], vf);
-                bf16x8_to_float(vp[8 + ds], vf + 8);
+                float2 vf[8];
+                bf16x8_to_float2(vp[ds], vf);
+                bf16x8_to_float2(vp[8 + ds], vf + 4);
 #pragma unroll
-                for (int h = 0; h < GH; ++h)
+                for (int h = 0; h < GH; ++h) {
+                    const float2 p2 = make_float2(pr[ps][h], pr[ps][h]);
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) acc[h][e] = fmaf(pr[ps][h], vf[e], acc[h][e]);
+                    for (int e = 0; e < 8; ++e) acc[h][e] = __ffma2_rn(p2, vf[e], acc[h][e]);
+                }
             }
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(empty + slot);
@@ -225,9 +240,11 @@ __global__ void __launch_bounds__(NTHREADS, 3)
             lsum[h] += __shfl_xor_sync(0xffffffffu, lsum[h], 8);
             lsum[h] += __shfl_xor_sync(0xffffffffu, lsum[h], 16);
 #pragma unroll
-            for (int e = 0; e < 16; ++e) {
-                acc[h][e] += __shfl_xor_sync(0xffffffffu, acc[h][e], 8);
-                acc[h][e] += __shfl_xor_sync(0xffffffffu, acc[h][e], 16);
+            for (int e = 0; e < 8; ++e) {
+                acc[h][e].x += __shfl_xor_sync(0xffffffffu, acc[h][e].x, 8);
+                acc[h][e].y += __shfl_xor_sync(0xffffffffu, acc[h][e].y, 8);
+                acc[h][e].x += __shfl_xor_sync(0xffffffffu, acc[h][e].x, 16);
+                acc[h][e].y += __shfl_xor_sync(0xffffffffu, acc[h][e].y, 16);
             }
         }
         float *mw = merge + (warp * GH_MAX) * (D + 2);
@@ -236,9 +253,11 @@ __global__ void __launch_bounds__(NTHREADS, 3)
             float *row = mw + h * (D + 2);
             if (tg == 0) {
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    row[ds * 8 + e] = acc[h][e];
-                    row[64 + ds * 8 + e] = acc[h][8 + e];
+                for (int e = 0; e < 4; ++e) {
+                    row[ds * 8 + 2 * e] = acc[h][e].x;
+                    row[ds * 8 + 2 * e + 1] = acc[h][e].y;
+                    row[64 + ds * 8 + 2 * e] = acc[h][4 + e].x;
+                    row[64 + ds * 8 + 2 * e + 1] = acc[h][4 + e].y;
                 }
             }
             if (lane == 0) {
