@@ -44,10 +44,12 @@ constexpr uint32_t PAGE_BYTES = PAGE * D * 2;        // one tensor, one KV head:
 constexpr uint32_t STAGE_BYTES = 2 * PAGE_BYTES;     // K + V
 constexpr uint32_t SMEM_STAGES = NST * STAGE_BYTES;  // 64 KiB
 constexpr uint32_t SMEM_MERGE = NCW * GH_MAX * (D + 2) * 4;
-constexpr uint32_t SMEM_MISC = 256;
+constexpr uint32_t SMEM_MISC = 512;
 constexpr uint32_t SMEM_ALIGN = 1024;
 constexpr uint32_t SMEM_BYTES = SMEM_ALIGN + SMEM_STAGES + SMEM_MERGE + SMEM_MISC;
 constexpr int PAGES_PER_SPLIT = 32;
+// barriers, per-stage flags, the abort flag and the split's page ids
+static_assert(2 * NST * 8 + (NST + 4 + PAGES_PER_SPLIT) * 4 <= SMEM_MISC, "misc shared area too small");
 constexpr float RESCALE_LOG2 = 8.0f;
 constexpr float LN2 = 0.6931471805599453f;
 constexpr float LOG2E = 1.4426950408889634f;
@@ -83,6 +85,7 @@ __global__ void __launch_bounds__(NTHREADS, 3)
     uint64_t *empty = full + NST;
     int *stage_bad = reinterpret_cast<int *>(empty + NST);
     volatile int *abort_flag = stage_bad + NST;
+    int *split_pages = stage_bad + NST + 4;  // physical page ids of this split (PAGES_PER_SPLIT)
 
     const int split = blockIdx.y;
     const int h0 = blockIdx.x * GH;
@@ -119,6 +122,10 @@ __global__ void __launch_bounds__(NTHREADS, 3)
 
     if (warp == NCW) {
         // ---------------- producer
+        // The whole warp reads the split's block-table entries in one go, so
+        // the copy-issuing lane never waits on a global load per page.
+        for (int k = lane; k < np; k += 32) split_pages[k] = p.block_table[(int64_t)b * p.max_blocks + page0 + k];
+        __syncwarp();
         if (lane == 0) {
             ptx::prefetch_tensormap(&map_k);
             ptx::prefetch_tensormap(&map_v);
@@ -127,7 +134,7 @@ __global__ void __launch_bounds__(NTHREADS, 3)
                 const int slot = i % NST;
                 const int round = i / NST;
                 if (round > 0 && !wait_bounded(empty + slot, (round - 1) & 1, wc, kSiteDecodeEmpty)) break;
-                const int phys = p.block_table[(int64_t)b * p.max_blocks + page0 + i];
+                const int phys = split_pages[i];
                 uint8_t *dst = base + slot * STAGE_BYTES;
                 if (phys < 0 || phys >= p.num_pages) {
                     report_status(p.status, kStatusDeviceBounds, kSiteDecodeTable);
@@ -217,6 +224,10 @@ __global__ void __launch_bounds__(NTHREADS, 3)
                     lsum[h] += pr[ps][h];
                 }
             }
+            // Slots past the sequence end (and pages that could not be read)
+            // hold arbitrary bits: their P is 0, but 0 * NaN is NaN, so on
+            // such a page the V of invalid tokens is replaced by 0 as well.
+            const bool page_full = !bad && tok0 + PAGE <= L;
 #pragma unroll
             for (int ps = 0; ps < 4; ++ps) {
                 const int t = ps * 4 + tg;
@@ -224,6 +235,10 @@ __global__ void __launch_bounds__(NTHREADS, 3)
                 float2 vf[8];
                 bf16x8_to_float2(vp[ds], vf);
                 bf16x8_to_float2(vp[8 + ds], vf + 4);
+                if (!page_full && (bad || tok0 + t >= L)) {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) vf[e] = make_float2(0.f, 0.f);
+                }
 #pragma unroll
                 for (int h = 0; h < GH; ++h) {
                     const float2 p2 = make_float2(pr[ps][h], pr[ps][h]);

@@ -238,6 +238,23 @@ def test_paged_decode_group_sizes(A, Hq, Hkv):
     check_lse(lse, ref_l, f"decode G={Hq // Hkv}")
 
 
+def test_paged_decode_ignores_garbage_past_sequence_end(A):
+    # The unused slots of each sequence's last page may hold anything (here
+    # NaN and Inf); only keys below seqlen take part in the result.
+    w = inputs.DecodeWorkload("garbage", B=4, Hq=8, Hkv=2, max_blocks=64, seed=13)
+    q, kp, vp, table, lens = inputs.make_decode(w, seqlens=[17, 33, 1000, 1])
+    kp2, vp2 = kp.clone(), vp.clone()
+    for b, L in enumerate(lens.tolist()):
+        last = int(table[b, (L - 1) // 16])
+        kp2[last, L % 16 or 16:] = float("nan")
+        vp2[last, L % 16 or 16:] = float("inf")
+    out, lse = A.decode_paged(q.cuda(), kp2.cuda(), vp2.cuda(), table.cuda(), lens.cuda(), scale=w.scale)
+    torch.cuda.synchronize()
+    ref_o, ref_l = oracle.decode_paged(q, kp, vp, table, lens, scale=w.scale)
+    check_out(out, ref_o, "garbage past the end")
+    check_lse(lse, ref_l, "garbage past the end")
+
+
 def test_paged_decode_deterministic(A):
     w = inputs.PAGED_DECODE
     q, kp, vp, table, lens = (t.cuda() for t in inputs.make_decode(w))
