@@ -241,8 +241,9 @@ attn_status_t attn_fwd_simple(const void *q, const void *k, const void *v, void 
 
 size_t attn_decode_workspace_bytes(int B, int Hq, int d, int max_blocks_per_seq) {
     if (B < 1 || Hq < 1 || d != 128 || max_blocks_per_seq < 1) return 0;
-    const int pps = attn::decode_pages_per_split();
-    const size_t nsplit = (size_t)((max_blocks_per_seq + pps - 1) / pps);
+    int ns = 1, pps = 1;
+    attn::decode_split_plan(B, Hq, max_blocks_per_seq, &ns, &pps);
+    const size_t nsplit = (size_t)ns;
     const size_t rows = (size_t)B * Hq;
     // o_part [rows][nsplit][d] fp32, then lse_part [rows][nsplit] fp32, each 256-B aligned.
     size_t o_bytes = rows * nsplit * d * 4;
@@ -281,8 +282,7 @@ attn_status_t attn_decode_paged(const void *q, const void *k_pages, const void *
     p.seqlens = seqlens;
     p.out = out;
     p.lse = lse;
-    p.pages_per_split = attn::decode_pages_per_split();
-    p.nsplit = (max_blocks_per_seq + p.pages_per_split - 1) / p.pages_per_split;
+    attn::decode_split_plan(B, Hq, max_blocks_per_seq, &p.nsplit, &p.pages_per_split);
     const size_t rows = (size_t)B * Hq;
     size_t o_bytes = rows * p.nsplit * d * 4;
     o_bytes = (o_bytes + 255) & ~(size_t)255;

@@ -44,12 +44,13 @@ constexpr uint32_t PAGE_BYTES = PAGE * D * 2;        // one tensor, one KV head:
 constexpr uint32_t STAGE_BYTES = 2 * PAGE_BYTES;     // K + V
 constexpr uint32_t SMEM_STAGES = NST * STAGE_BYTES;  // 64 KiB
 constexpr uint32_t SMEM_MERGE = NCW * GH_MAX * (D + 2) * 4;
-constexpr uint32_t SMEM_MISC = 512;
+constexpr uint32_t SMEM_MISC = 1536;
 constexpr uint32_t SMEM_ALIGN = 1024;
 constexpr uint32_t SMEM_BYTES = SMEM_ALIGN + SMEM_STAGES + SMEM_MERGE + SMEM_MISC;
-constexpr int PAGES_PER_SPLIT = 32;
+constexpr int MAX_PAGES_PER_SPLIT = 256;
+constexpr int TARGET_SPLIT_CTAS = 2048;  // split CTAs the plan aims for (assuming two heads per CTA)
 // barriers, per-stage flags, the abort flag and the split's page ids
-static_assert(2 * NST * 8 + (NST + 4 + PAGES_PER_SPLIT) * 4 <= SMEM_MISC, "misc shared area too small");
+static_assert(2 * NST * 8 + (NST + 4 + MAX_PAGES_PER_SPLIT) * 4 <= SMEM_MISC, "misc shared area too small");
 constexpr float RESCALE_LOG2 = 8.0f;
 constexpr float LN2 = 0.6931471805599453f;
 constexpr float LOG2E = 1.4426950408889634f;
@@ -85,7 +86,7 @@ __global__ void __launch_bounds__(NTHREADS, 3)
     uint64_t *empty = full + NST;
     int *stage_bad = reinterpret_cast<int *>(empty + NST);
     volatile int *abort_flag = stage_bad + NST;
-    int *split_pages = stage_bad + NST + 4;  // physical page ids of this split (PAGES_PER_SPLIT)
+    int *split_pages = stage_bad + NST + 4;  // physical page ids of this split (<= MAX_PAGES_PER_SPLIT)
 
     const int split = blockIdx.y;
     const int h0 = blockIdx.x * GH;
@@ -332,7 +333,20 @@ __global__ void __launch_bounds__(D) merge_kernel(const float *__restrict__ o_pa
 
 }  // namespace dec
 
-int decode_pages_per_split() { return dec::PAGES_PER_SPLIT; }
+// Key-split plan, a pure function of the shape: aim for about
+// TARGET_SPLIT_CTAS split CTAs (B * Hq / 2 head groups times the split count),
+// so that few sequences still fill the GPU and many do not pay for a merge per
+// small split; 16 .. 256 pages per split.
+void decode_split_plan(int B, int Hq, int max_blocks, int *nsplit, int *pages_per_split) {
+    const long groups = (long)B * ((Hq + 1) / 2);
+    long want = (dec::TARGET_SPLIT_CTAS + groups - 1) / groups;
+    if (want < 1) want = 1;
+    long pps = (max_blocks + want - 1) / want;
+    if (pps < 16) pps = 16;
+    if (pps > dec::MAX_PAGES_PER_SPLIT) pps = dec::MAX_PAGES_PER_SPLIT;
+    *pages_per_split = (int)pps;
+    *nsplit = (int)((max_blocks + pps - 1) / pps);
+}
 
 cudaError_t launch_decode(const CUtensorMap &mk, const CUtensorMap &mv, const DecodeParams &p,
                           cudaStream_t stream) {

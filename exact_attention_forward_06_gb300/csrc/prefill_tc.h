@@ -59,7 +59,7 @@ struct DecodeParams {
     uint64_t budget_ns;
 };
 
-int decode_pages_per_split();
+void decode_split_plan(int B, int Hq, int max_blocks, int *nsplit, int *pages_per_split);
 cudaError_t launch_decode(const CUtensorMap &mk, const CUtensorMap &mv, const DecodeParams &p,
                           cudaStream_t stream);
 cudaError_t launch_lse_merge(const float *o_parts, const float *lse_parts, void *out, float *lse, int rows,
