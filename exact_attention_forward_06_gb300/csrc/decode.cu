@@ -7,21 +7,24 @@
 // once and does ~4 flops per byte, so it is bound by HBM bandwidth and runs on
 // the CUDA cores; the tensor cores would only add a reshape.
 //
-// Split kernel: one CTA per (group of up to 2 query heads sharing a KV head,
-// split, sequence); the head groups of one split are adjacent in the grid so
-// that their reads of the same pages meet in L2.  The CTAs are small (one
-// producer warp and four consumer warps, about 128 registers a thread) so
-// three of them share an SM.  The producer lane gathers the split's pages with
-// one 3-D TMA copy per page and tensor (the 16 rows of one KV head in a page
-// are 2 KiB apart in the pool) into an 8-page shared-memory ring.  The four
-// consumer warps take pages round-robin.  In a warp, lane (tg, ds) =
+// Split kernel: one CTA per (group of up to 4 query heads sharing a KV head,
+// split, sequence); when a KV group has more heads, its head groups are
+// adjacent in the grid so that their reads of the same pages meet in L2.  The
+// CTAs are small (one producer warp and four consumer warps, about 128
+// registers a thread) so three of them share an SM.  The producer lane gathers
+// the split's pages with one 3-D TMA copy per page and tensor (the 16 rows of
+// one KV head in a page are 2 KiB apart in the pool) into an 8-page
+// shared-memory ring.  A consumer warp handles at most 2 heads; with 4 heads
+// two warps read each staged page (one per head pair), so the four warps form
+// two page streams that take pages alternately (four streams of one warp with
+// 1 or 2 heads).  In a warp, lane (tg, ds) =
 // (lane/8, lane%8) owns head-dim elements [8 ds, 8 ds + 8) and
 // [64 + 8 ds, 64 + 8 ds + 8) of tokens tg, tg+4, tg+8, tg+12 of the page (two
 // 16-byte chunks, so the eight lanes of a token read one 256-byte row without
 // bank conflicts).  Dot products are reduced over the 8 lanes of a token with
 // three shuffles, the page max over the token groups with two more, and each
 // warp keeps its own running max / sum / accumulator (online softmax, with the
-// max moved only past a 2^8 growth).  At the end the four warps are merged in
+// max moved only past a 2^8 growth).  At the end the page streams are merged in
 // shared memory and the split writes its normalised partial output and
 // log-sum-exp.  The merge kernel then combines the splits in a fixed order.
 #include <cstdint>
@@ -48,7 +51,7 @@ constexpr uint32_t SMEM_MISC = 1536;
 constexpr uint32_t SMEM_ALIGN = 1024;
 constexpr uint32_t SMEM_BYTES = SMEM_ALIGN + SMEM_STAGES + SMEM_MERGE + SMEM_MISC;
 constexpr int MAX_PAGES_PER_SPLIT = 256;
-constexpr int TARGET_SPLIT_CTAS = 2048;  // split CTAs the plan aims for (assuming two heads per CTA)
+constexpr int TARGET_SPLIT_CTAS = 2048;  // split CTAs the plan aims for (assuming four heads per CTA)
 // barriers, per-stage flags, the abort flag and the split's page ids
 static_assert(2 * NST * 8 + (NST + 4 + MAX_PAGES_PER_SPLIT) * 4 <= SMEM_MISC, "misc shared area too small");
 constexpr float RESCALE_LOG2 = 8.0f;
@@ -74,10 +77,17 @@ __device__ __forceinline__ void bf16x8_to_float(const uint4 &u, float *x) {
     x[7] = __uint_as_float(u.w & 0xffff0000u);
 }
 
+// GH query heads per CTA (1, 2 or 4, all of one KV head).  Each consumer warp
+// handles HG <= 2 of them, so the NHG = GH / HG warps of a "page stream" read
+// every staged page together and the page is fetched once for all GH heads.
 template <int GH>
 __global__ void __launch_bounds__(NTHREADS, 3)
     split_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
                  const DecodeParams p) {
+    constexpr int HG = GH >= 2 ? 2 : 1;    // heads per consumer warp
+    constexpr int NHG = GH / HG;           // warps reading each page
+    constexpr int STREAMS = NCW / NHG;     // pages consumed in parallel
+    static_assert(STREAMS * GH <= NCW * GH_MAX, "merge scratch too small");
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = ptx::smem_addr(smem_raw);
     uint8_t *base = smem_raw + ((SMEM_ALIGN - (raw & (SMEM_ALIGN - 1))) & (SMEM_ALIGN - 1));
@@ -112,7 +122,7 @@ __global__ void __launch_bounds__(NTHREADS, 3)
     if (threadIdx.x == 0) {
         for (int s = 0; s < NST; ++s) {
             ptx::mbar_init(full + s, 1);
-            ptx::mbar_init(empty + s, 1);
+            ptx::mbar_init(empty + s, NHG);
             stage_bad[s] = 0;
         }
         *abort_flag = 0;
@@ -156,36 +166,39 @@ __global__ void __launch_bounds__(NTHREADS, 3)
         // ---------------- consumers
         const int tg = lane >> 3;  // token group
         const int ds = lane & 7;   // head-dim chunks ds and 8 + ds
+        const int hg = warp % NHG;       // this warp's heads: hg * HG .. hg * HG + HG - 1
+        const int stream = warp / NHG;   // this warp's pages: stream, stream + STREAMS, ...
+        const int64_t wrow0 = row0 + hg * HG;
         // Dot products and the P V accumulation run on fp32 pairs (packed
         // FFMA2): element pairs (2i, 2i+1) of the lane's 16 head-dim elements.
-        float2 qf[GH][8];
+        float2 qf[HG][8];
 #pragma unroll
-        for (int h = 0; h < GH; ++h) {
+        for (int h = 0; h < HG; ++h) {
             const uint4 *qp = reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(p.q) +
-                                                              (row0 + h) * D);
+                                                              (wrow0 + h) * D);
             bf16x8_to_float2(qp[ds], qf[h]);
             bf16x8_to_float2(qp[8 + ds], qf[h] + 4);
             const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
 #pragma unroll
             for (int e = 0; e < 8; ++e) qf[h][e] = __fmul2_rn(qf[h][e], sc2);
         }
-        float m[GH], lsum[GH];
-        float2 acc[GH][8];
+        float m[HG], lsum[HG];
+        float2 acc[HG][8];
 #pragma unroll
-        for (int h = 0; h < GH; ++h) {
+        for (int h = 0; h < HG; ++h) {
             m[h] = -INFINITY;
             lsum[h] = 0.f;
 #pragma unroll
             for (int e = 0; e < 8; ++e) acc[h][e] = make_float2(0.f, 0.f);
         }
-        for (int i = warp; i < np; i += NCW) {
+        for (int i = stream; i < np; i += STREAMS) {
             const int slot = i % NST;
             if (!wait_bounded(full + slot, (i / NST) & 1, wc, kSiteDecodeFull)) break;
             const uint8_t *ks = base + slot * STAGE_BYTES;
             const uint8_t *vs = ks + PAGE_BYTES;
             const bool bad = stage_bad[slot] != 0;
             const int tok0 = (page0 + i) * PAGE;
-            float sc[4][GH];
+            float sc[4][HG];
 #pragma unroll
             for (int ps = 0; ps < 4; ++ps) {
                 const int t = ps * 4 + tg;
@@ -194,7 +207,7 @@ __global__ void __launch_bounds__(NTHREADS, 3)
                 bf16x8_to_float2(kp[ds], kf);
                 bf16x8_to_float2(kp[8 + ds], kf + 4);
 #pragma unroll
-                for (int h = 0; h < GH; ++h) {
+                for (int h = 0; h < HG; ++h) {
                     float2 d2 = __fmul2_rn(qf[h][0], kf[0]);
 #pragma unroll
                     for (int e = 1; e < 8; ++e) d2 = __ffma2_rn(qf[h][e], kf[e], d2);
@@ -205,9 +218,9 @@ __global__ void __launch_bounds__(NTHREADS, 3)
                     sc[ps][h] = (!bad && tok0 + t < L) ? dot : -INFINITY;
                 }
             }
-            float pr[4][GH];
+            float pr[4][HG];
 #pragma unroll
-            for (int h = 0; h < GH; ++h) {
+            for (int h = 0; h < HG; ++h) {
                 float pm = fmaxf(fmaxf(sc[0][h], sc[1][h]), fmaxf(sc[2][h], sc[3][h]));
                 pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 8));
                 pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 16));
@@ -241,7 +254,7 @@ __global__ void __launch_bounds__(NTHREADS, 3)
                     for (int e = 0; e < 8; ++e) vf[e] = make_float2(0.f, 0.f);
                 }
 #pragma unroll
-                for (int h = 0; h < GH; ++h) {
+                for (int h = 0; h < HG; ++h) {
                     const float2 p2 = make_float2(pr[ps][h], pr[ps][h]);
 #pragma unroll
                     for (int e = 0; e < 8; ++e) acc[h][e] = __ffma2_rn(p2, vf[e], acc[h][e]);
@@ -252,7 +265,7 @@ __global__ void __launch_bounds__(NTHREADS, 3)
         }
         // Sum the four token groups (lanes 8 and 16 apart share a slice).
 #pragma unroll
-        for (int h = 0; h < GH; ++h) {
+        for (int h = 0; h < HG; ++h) {
             lsum[h] += __shfl_xor_sync(0xffffffffu, lsum[h], 8);
             lsum[h] += __shfl_xor_sync(0xffffffffu, lsum[h], 16);
 #pragma unroll
@@ -263,9 +276,10 @@ __global__ void __launch_bounds__(NTHREADS, 3)
                 acc[h][e].y += __shfl_xor_sync(0xffffffffu, acc[h][e].y, 16);
             }
         }
-        float *mw = merge + (warp * GH_MAX) * (D + 2);
+        // merge scratch row of (page stream, head): stream * GH + head
+        float *mw = merge + (stream * GH + hg * HG) * (D + 2);
 #pragma unroll
-        for (int h = 0; h < GH; ++h) {
+        for (int h = 0; h < HG; ++h) {
             float *row = mw + h * (D + 2);
             if (tg == 0) {
 #pragma unroll
@@ -284,19 +298,19 @@ __global__ void __launch_bounds__(NTHREADS, 3)
     }
     __syncthreads();
     if (*abort_flag) return;
-    // Merge the four warps: thread = head-dim element, loop over heads.
+    // Merge the page streams: thread = head-dim element, loop over heads.
     if (threadIdx.x < D) {
         const int e = threadIdx.x;
 #pragma unroll
         for (int h = 0; h < GH; ++h) {
             float M = -INFINITY;
 #pragma unroll
-            for (int w = 0; w < NCW; ++w) M = fmaxf(M, merge[(w * GH_MAX + h) * (D + 2) + D]);
+            for (int w = 0; w < STREAMS; ++w) M = fmaxf(M, merge[(w * GH + h) * (D + 2) + D]);
             float Ls = 0.f, o = 0.f;
             if (M != -INFINITY) {
 #pragma unroll
-                for (int w = 0; w < NCW; ++w) {
-                    const float *row = merge + (w * GH_MAX + h) * (D + 2);
+                for (int w = 0; w < STREAMS; ++w) {
+                    const float *row = merge + (w * GH + h) * (D + 2);
                     const float f = ptx::ex2(row[D] - M);  // -inf -> 0
                     Ls += row[D + 1] * f;
                     o += row[e] * f;
@@ -334,11 +348,11 @@ __global__ void __launch_bounds__(D) merge_kernel(const float *__restrict__ o_pa
 }  // namespace dec
 
 // Key-split plan, a pure function of the shape: aim for about
-// TARGET_SPLIT_CTAS split CTAs (B * Hq / 2 head groups times the split count),
+// TARGET_SPLIT_CTAS split CTAs (B * Hq / 4 head groups times the split count),
 // so that few sequences still fill the GPU and many do not pay for a merge per
 // small split; 16 .. 256 pages per split.
 void decode_split_plan(int B, int Hq, int max_blocks, int *nsplit, int *pages_per_split) {
-    const long groups = (long)B * ((Hq + 1) / 2);
+    const long groups = (long)B * ((Hq + 3) / 4);
     long want = (dec::TARGET_SPLIT_CTAS + groups - 1) / groups;
     if (want < 1) want = 1;
     long pps = (max_blocks + want - 1) / want;
@@ -350,8 +364,8 @@ void decode_split_plan(int B, int Hq, int max_blocks, int *nsplit, int *pages_pe
 
 cudaError_t launch_decode(const CUtensorMap &mk, const CUtensorMap &mv, const DecodeParams &p,
                           cudaStream_t stream) {
-    // Heads per CTA: 2 when the group size is even, else 1.
-    const int GH = (p.G % 2 == 0) ? 2 : 1;
+    // Heads per CTA: 4, 2 or 1, the largest dividing the group size.
+    const int GH = (p.G % 4 == 0) ? 4 : (p.G % 2 == 0) ? 2 : 1;
     dim3 grid(p.Hq / GH, p.nsplit, p.B);
     const int smem = (int)dec::SMEM_BYTES;
     static thread_local int configured_device = -1;
@@ -359,10 +373,15 @@ cudaError_t launch_decode(const CUtensorMap &mk, const CUtensorMap &mv, const De
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (configured_device != dev) {
-        e = cudaFuncSetAttribute(dec::split_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        e = cudaFuncSetAttribute(dec::split_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(dec::split_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(dec::split_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         // Three CTAs of ~74 KiB per SM need the largest shared-memory carveout.
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(dec::split_kernel<4>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                     cudaSharedmemCarveoutMaxShared);
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(dec::split_kernel<2>, cudaFuncAttributePreferredSharedMemoryCarveout,
                                      cudaSharedmemCarveoutMaxShared);
@@ -372,7 +391,9 @@ cudaError_t launch_decode(const CUtensorMap &mk, const CUtensorMap &mv, const De
         if (e != cudaSuccess) return e;
         configured_device = dev;
     }
-    if (GH == 2)
+    if (GH == 4)
+        dec::split_kernel<4><<<grid, dec::NTHREADS, smem, stream>>>(mk, mv, p);
+    else if (GH == 2)
         dec::split_kernel<2><<<grid, dec::NTHREADS, smem, stream>>>(mk, mv, p);
     else
         dec::split_kernel<1><<<grid, dec::NTHREADS, smem, stream>>>(mk, mv, p);

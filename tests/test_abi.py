@@ -77,7 +77,9 @@ def test_fwd_rejects_bad_arguments_before_any_launch(lib, kw, code):
 def test_decode_workspace_is_a_pure_function_of_shape(lib):
     a = A.decode_workspace_bytes(32, 32, 128, 512)
     assert a == A.decode_workspace_bytes(32, 32, 128, 512) and a > 0
-    assert A.decode_workspace_bytes(32, 32, 128, 513) > a
+    # non-decreasing in the table width, and larger once the splits are capped
+    assert A.decode_workspace_bytes(32, 32, 128, 513) >= a
+    assert A.decode_workspace_bytes(32, 32, 128, 8192) > a
     assert A.decode_workspace_bytes(32, 32, 64, 512) == 0
     assert A.decode_workspace_bytes(0, 32, 128, 512) == 0
 
