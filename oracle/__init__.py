@@ -91,6 +91,10 @@ def _load():
                                                 _i64, _i64, _i64, _dbl, _p, _p]
             lib.oracle_round_bf16_rtne.argtypes = [_dbl]
             lib.oracle_round_bf16_rtne.restype = ctypes.c_uint16
+            lib.oracle_round_bf16.argtypes = [_dbl, _int]
+            lib.oracle_round_bf16.restype = ctypes.c_uint16
+            lib.oracle_round_bf16_array.argtypes = [_p, _p, _i64, _int]
+            lib.oracle_round_bf16_array.restype = _int
             for name in ("oracle_attention", "oracle_attention_rows", "oracle_attention_probs_row",
                          "oracle_attention_tiled_rows", "oracle_lse_merge", "oracle_decode_paged"):
                 getattr(lib, name).restype = _int
@@ -226,3 +230,20 @@ def decode_paged(q, k_pages, v_pages, block_table, seqlens, *, scale, page_size=
 def round_bf16_rtne(x: float) -> int:
     """Bit pattern of the bf16 nearest to x, ties to even."""
     return int(_load().oracle_round_bf16_rtne(float(x)))
+
+
+ROUNDING_MODES = {"rtne": 0, "rtna": 1, "rtz": 2}
+
+
+def round_bf16(x: float, mode: str = "rtne") -> int:
+    """Bit pattern of x rounded to bf16: "rtne" (nearest, ties to even), "rtna"
+    (nearest, ties away from zero) or "rtz" (toward zero)."""
+    return int(_load().oracle_round_bf16(float(x), ROUNDING_MODES[mode]))
+
+
+def round_bf16_array(x, mode: str = "rtne") -> np.ndarray:
+    """Element-wise round_bf16 over an array of doubles; uint16 bit patterns, same shape."""
+    xd = np.ascontiguousarray(x, dtype=np.float64)
+    out = np.empty(xd.shape, dtype=np.uint16)
+    _check(_load().oracle_round_bf16_array(_ptr(xd), _ptr(out), xd.size, ROUNDING_MODES[mode]), "round_bf16_array")
+    return out

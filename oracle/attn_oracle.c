@@ -401,16 +401,21 @@ int oracle_decode_paged(const uint16_t *q, const uint16_t *k_pages, const uint16
 }
 
 /*
- * Round a double to the nearest bf16, ties to even (RTNE), returning the bit
+ * Round a double to bf16 in one of the three output rounding modes the
+ * MoonMath HIP kernel page lists for its bf16 output (benchmark and
+ * limitations sections): 0 = RTNE (to nearest, ties to even), 1 = RTNA (to
+ * nearest, ties away from zero), 2 = RTZ (toward zero).  Returns the bit
  * pattern.  Written from the definition of the format (8 exponent bits, 8
- * significant bits): the quantum at the value's binade is 2^(e-8) (never
- * below the subnormal quantum 2^-133), the scaled value is rounded with
- * nearbyint in the default round-to-nearest-even mode, and the result is
- * exactly representable in binary32, whose top 16 bits are the bf16 pattern.
- * One rounding step only, from the double itself.  NaN becomes the quiet NaN
- * 0x7fc0; values past the largest finite bf16 become infinity.
+ * significant bits): the quantum at the value's binade is 2^(e-8) (never below
+ * the subnormal quantum 2^-133); the magnitude divided by the quantum is
+ * rounded to an integer by nearbyint (default mode: ties to even), round
+ * (ties away from zero) or trunc; times the quantum again it is exactly
+ * representable in binary32, whose top 16 bits are the bf16 pattern.  One
+ * rounding step only, from the double itself.  NaN becomes the quiet NaN
+ * 0x7fc0.  Past the largest finite bf16, the nearest modes give infinity and
+ * RTZ gives the largest finite value; an infinite input stays infinite.
  */
-uint16_t oracle_round_bf16_rtne(double x) {
+uint16_t oracle_round_bf16(double x, int mode) {
     if (isnan(x)) return 0x7fc0u;
     uint16_t sign = signbit(x) ? 0x8000u : 0u;
     double ax = fabs(x);
@@ -422,10 +427,22 @@ uint16_t oracle_round_bf16_rtne(double x) {
         frexp(ax, &e); /* ax = m * 2^e, m in [0.5, 1) */
         int qexp = e - 8;
         if (qexp < -133) qexp = -133;
-        r = ldexp(nearbyint(ldexp(ax, -qexp)), qexp);
+        double units = ldexp(ax, -qexp);
+        double n = mode == 1 ? round(units) : mode == 2 ? trunc(units) : nearbyint(units);
+        r = ldexp(n, qexp);
+        if (mode == 2 && r > 0x1.fep127) r = 0x1.fep127; /* RTZ never overflows */
     }
     float f = (float)r; /* exact, or +inf past the bf16 range */
     uint32_t u;
     memcpy(&u, &f, sizeof u);
     return (uint16_t)(sign | (uint16_t)(u >> 16));
+}
+
+uint16_t oracle_round_bf16_rtne(double x) { return oracle_round_bf16(x, 0); }
+
+/* Element-wise oracle_round_bf16 over n doubles. */
+int oracle_round_bf16_array(const double *x, uint16_t *out, int64_t n, int mode) {
+    if (mode < 0 || mode > 2) return ORACLE_BAD_ARG;
+    for (int64_t i = 0; i < n; ++i) out[i] = oracle_round_bf16(x[i], mode);
+    return ORACLE_OK;
 }

@@ -331,6 +331,60 @@ def test_bf16_rtne_ties_go_to_even():
     assert oracle.round_bf16_rtne(float("inf")) == 0x7F80
 
 
+def _random_float32(seed, n=20000):
+    g = torch.Generator().manual_seed(seed)
+    x = torch.randn(n, generator=g, dtype=torch.float32) * torch.exp(torch.randn(n, generator=g) * 8)
+    extra = torch.tensor([1e-39, -3e-40, 1.5e-45, 3.3e38, -3.39e38, 0.0, -0.0], dtype=torch.float32)
+    return torch.cat([x, extra]).numpy()
+
+
+def test_bf16_rtz_is_truncation_of_the_float32_pattern():
+    # For a binary32 value, dropping the low 16 bits of its pattern is rounding
+    # the magnitude toward zero at bf16 precision.
+    x = _random_float32(51)
+    want = (x.view(np.uint32) >> 16).astype(np.uint16)
+    np.testing.assert_array_equal(oracle.round_bf16_array(x.astype(np.float64), "rtz"), want)
+
+
+def test_bf16_rtna_is_half_unit_added_to_the_float32_magnitude():
+    # Adding half a bf16 unit (0x8000) to the magnitude bits and dropping the low
+    # 16 bits rounds to nearest with ties away from zero (a carry moves the exponent).
+    x = _random_float32(52)
+    u = x.view(np.uint32).astype(np.uint64)
+    want = (((u & 0x7FFFFFFF) + 0x8000) >> 16).astype(np.uint16) | ((u >> 16) & 0x8000).astype(np.uint16)
+    np.testing.assert_array_equal(oracle.round_bf16_array(x.astype(np.float64), "rtna"), want)
+
+
+def test_bf16_rtne_array_matches_torch():
+    x = _random_float32(53)
+    want = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    np.testing.assert_array_equal(oracle.round_bf16_array(x.astype(np.float64), "rtne"), want)
+    assert all(oracle.round_bf16(float(t), "rtne") == oracle.round_bf16_rtne(float(t)) for t in x[:200])
+
+
+@pytest.mark.parametrize("x,rtne,rtna,rtz", [
+    (1.0 + 2.0 ** -8, 0x3F80, 0x3F81, 0x3F80),            # tie below an odd neighbour
+    (1.0 + 3 * 2.0 ** -8, 0x3F82, 0x3F82, 0x3F81),        # tie below an even neighbour
+    (-(1.0 + 2.0 ** -8), 0xBF80, 0xBF81, 0xBF80),         # sign-symmetric
+    (64.25, 0x4280, 0x4281, 0x4280),                      # quarter steps at 64: spacing 0.5
+    (-64.75, 0xC282, 0xC282, 0xC281),
+    (1.0 + 2.0 ** -8 + 2.0 ** -40, 0x3F81, 0x3F81, 0x3F80),  # just above a tie: one rounding, from the double
+    (1.0 + 2.0 ** -8 - 2.0 ** -40, 0x3F80, 0x3F80, 0x3F80),  # just below
+    (3.0e38, 0x7F62, 0x7F62, 0x7F61),
+    (3.4e38, 0x7F80, 0x7F80, 0x7F7F),                     # past the largest bf16: RTZ saturates
+    (1e300, 0x7F80, 0x7F80, 0x7F7F),
+    (float("inf"), 0x7F80, 0x7F80, 0x7F80),
+    (float("-inf"), 0xFF80, 0xFF80, 0xFF80),
+    (float("nan"), 0x7FC0, 0x7FC0, 0x7FC0),
+    (2.0 ** -133, 0x0001, 0x0001, 0x0001),                # smallest bf16 subnormal
+    (1.5 * 2.0 ** -133, 0x0002, 0x0002, 0x0001),          # subnormal tie
+])
+def test_bf16_modes_hand_worked(x, rtne, rtna, rtz):
+    assert oracle.round_bf16(x, "rtne") == rtne
+    assert oracle.round_bf16(x, "rtna") == rtna
+    assert oracle.round_bf16(x, "rtz") == rtz
+
+
 # ---------------------------------------------------------------- mutation tests
 
 MUTATIONS = {
@@ -364,6 +418,45 @@ def _pin_suite():
         except AssertionError:
             failures.append(fn)
     return failures
+
+
+ROUNDING_MUTATIONS = {
+    "rtna_ties_to_even": ("mode == 1 ? round(units)", "mode == 1 ? nearbyint(units)"),
+    "rtz_rounds_to_nearest": ("mode == 2 ? trunc(units)", "mode == 2 ? round(units)"),
+    "rtz_overflows": ("if (mode == 2 && r > 0x1.fep127) r = 0x1.fep127;", ";"),
+    "quantum_off_by_one": ("int qexp = e - 8;", "int qexp = e - 9;"),
+}
+
+
+def _rounding_pin_suite():
+    failures = []
+    cases = [(1.0 + 2.0 ** -8, 0x3F80, 0x3F81, 0x3F80), (1.0 + 3 * 2.0 ** -8, 0x3F82, 0x3F82, 0x3F81),
+             (3.4e38, 0x7F80, 0x7F80, 0x7F7F), (64.25, 0x4280, 0x4281, 0x4280), (1e300, 0x7F80, 0x7F80, 0x7F7F)]
+    for fn in (test_bf16_rtz_is_truncation_of_the_float32_pattern,
+               test_bf16_rtna_is_half_unit_added_to_the_float32_magnitude,
+               test_bf16_rtne_array_matches_torch,
+               *[(lambda c=c: test_bf16_modes_hand_worked(*c)) for c in cases]):
+        try:
+            fn()
+        except AssertionError:
+            failures.append(fn)
+    return failures
+
+
+@pytest.mark.skipif(shutil.which("gcc") is None, reason="needs gcc")
+@pytest.mark.parametrize("name", sorted(ROUNDING_MUTATIONS))
+def test_planted_rounding_mistake_is_caught(name, tmp_path):
+    src = open(os.path.join(os.path.dirname(oracle.__file__), "attn_oracle.c")).read()
+    old, new = ROUNDING_MUTATIONS[name]
+    assert old in src, f"mutation anchor for {name} not found"
+    bad = tmp_path / "bad.c"
+    bad.write_text(src.replace(old, new, 1))
+    so = tmp_path / "libbad.so"
+    subprocess.run(["gcc", "-O1", "-fopenmp", "-shared", "-fPIC", "-o", str(so), str(bad), "-lm"], check=True)
+    with oracle.use_library(str(so)):
+        failures = _rounding_pin_suite()
+    assert failures, f"no pin caught the planted mistake {name}"
+    assert not _rounding_pin_suite()
 
 
 @pytest.mark.skipif(shutil.which("gcc") is None, reason="needs gcc")
