@@ -51,6 +51,7 @@ def load():
             fwd_args = [_p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _i, _f, _p]
             lib.attn_fwd.argtypes = fwd_args
             lib.attn_fwd_simple.argtypes = fwd_args
+            lib.attn_fwd_rounded.argtypes = fwd_args[:-1] + [_i, _p]
             lib.attn_fwd_workspace_bytes.argtypes = [_i, _i, _i, _i, _i, _i, _i]
             lib.attn_fwd_workspace_bytes.restype = _sz
             lib.attn_set_workspace.argtypes = [_p, _sz]
@@ -62,7 +63,7 @@ def load():
             lib.attn_decode_paged_noalloc.argtypes = [_p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i,
                                                       _f, _p]
             lib.attn_decode_paged_noalloc.restype = _i
-            lib.attn_lse_merge.argtypes = [_p, _p, _p, _p, _i, _i, _i, _p]
+            lib.attn_lse_merge.argtypes = [_p, _p, _p, _p, _i, _i, _i, _i, _p]
             lib.attn_get_device_status.argtypes = [_p, ctypes.POINTER(_i)]
             lib.attn_set_wait_budget_ns.argtypes = [_u64]
             lib.attn_debug_inject.argtypes = [_i]
@@ -70,7 +71,7 @@ def load():
             lib.attn_status_string.argtypes = [_i]
             lib.attn_status_string.restype = ctypes.c_char_p
             lib.attn_version.restype = _i
-            for name in ("attn_fwd", "attn_fwd_simple", "attn_decode_paged", "attn_lse_merge",
+            for name in ("attn_fwd", "attn_fwd_simple", "attn_fwd_rounded", "attn_decode_paged", "attn_lse_merge",
                          "attn_get_device_status", "attn_set_wait_budget_ns", "attn_debug_inject",
                          "attn_selftest_umma"):
                 getattr(lib, name).restype = _i
@@ -111,7 +112,10 @@ def _dims(q, k, layout):
     return B, Hq, Hkv, Sq, Sk, d
 
 
-def _fwd_call(fn_name, q, k, v, causal, scale, layout, out, lse, stream):
+ROUNDING = {"rtne": 0, "rtna": 1, "rtz": 2}
+
+
+def _fwd_call(fn_name, q, k, v, causal, scale, layout, out, lse, stream, rounding="rtne"):
     lib = load()
     for t, n in ((q, "q"), (k, "k"), (v, "v")):
         _dev_tensor(t, n, torch.bfloat16)
@@ -127,18 +131,29 @@ def _fwd_call(fn_name, q, k, v, causal, scale, layout, out, lse, stream):
     elif lse is not False:
         _dev_tensor(lse, "lse", torch.float32)
     lse_ptr = None if lse is False else lse.data_ptr()
-    rc = getattr(lib, fn_name)(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse_ptr, B, Hq, Hkv, Sq,
-                               Sk, d, LAYOUTS[layout], int(bool(causal)), float(scale), _stream(stream))
+    args = [q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse_ptr, B, Hq, Hkv, Sq, Sk, d, LAYOUTS[layout],
+            int(bool(causal)), float(scale)]
+    if rounding != "rtne":
+        if fn_name != "attn_fwd":
+            raise ValueError(f"{fn_name} rounds its output to nearest even only")
+        fn_name = "attn_fwd_rounded"
+        args.append(ROUNDING[rounding])
+    rc = getattr(lib, fn_name)(*args, _stream(stream))
     _check(rc, fn_name)
     return out, (None if lse is False else lse)
 
 
-def fwd(q, k, v, *, causal=False, scale=None, layout="bshd", out=None, lse=None, stream=None):
+def fwd(q, k, v, *, causal=False, scale=None, layout="bshd", out=None, lse=None, stream=None, rounding="rtne"):
     """Fused exact attention forward: returns (out bf16 in q's layout, lse fp32 [B, Hq, Sq]).
 
-    Pass ``lse=False`` to skip the log-sum-exp output.
+    Pass ``lse=False`` to skip the log-sum-exp output.  ``rounding`` selects how
+    the fp32 result is rounded to the bf16 output: "rtne" (nearest, ties to
+    even; C entry point attn_fwd), "rtna" (nearest, ties away from zero) or
+    "rtz" (toward zero), the latter two through attn_fwd_rounded.
     """
-    return _fwd_call("attn_fwd", q, k, v, causal, scale, layout, out, lse, stream)
+    if rounding not in ROUNDING:
+        raise ValueError(f"rounding must be one of {sorted(ROUNDING)}, got {rounding!r}")
+    return _fwd_call("attn_fwd", q, k, v, causal, scale, layout, out, lse, stream, rounding)
 
 
 def fwd_simple(q, k, v, *, causal=False, scale=None, layout="bshd", out=None, lse=None, stream=None):
@@ -234,8 +249,13 @@ def decode_paged_noalloc(q, k_pages, v_pages, block_table, seqlens, *, scale=Non
     return out, (None if lse is False else lse)
 
 
-def lse_merge(o_parts, lse_parts, *, out=None, lse=None, stream=None):
-    """Merge key-range partials: o_parts [rows, nsplit, d] fp32, lse_parts [rows, nsplit] fp32."""
+def lse_merge(o_parts, lse_parts, *, out=None, lse=None, stream=None, rounding="rtne"):
+    """Merge key-range partials: o_parts [rows, nsplit, d] fp32, lse_parts [rows, nsplit] fp32.
+
+    ``rounding`` ("rtne", "rtna" or "rtz") selects the fp32 -> bf16 rounding of out.
+    """
+    if rounding not in ROUNDING:
+        raise ValueError(f"rounding must be one of {sorted(ROUNDING)}, got {rounding!r}")
     lib = load()
     _dev_tensor(o_parts, "o_parts", torch.float32)
     _dev_tensor(lse_parts, "lse_parts", torch.float32)
@@ -245,7 +265,7 @@ def lse_merge(o_parts, lse_parts, *, out=None, lse=None, stream=None):
     if lse is None:
         lse = torch.empty((rows,), device=o_parts.device, dtype=torch.float32)
     rc = lib.attn_lse_merge(o_parts.data_ptr(), lse_parts.data_ptr(), out.data_ptr(), lse.data_ptr(), rows, nsplit,
-                            d, _stream(stream))
+                            d, ROUNDING[rounding], _stream(stream))
     _check(rc, "attn_lse_merge")
     return out, lse
 

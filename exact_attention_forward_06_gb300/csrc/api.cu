@@ -135,6 +135,8 @@ attn_status_t check_fwd_args(const void *q, const void *k, const void *v, const 
     return ATTN_OK;
 }
 
+bool valid_round_mode(int m) { return m == ATTN_ROUND_RTNE || m == ATTN_ROUND_RTNA || m == ATTN_ROUND_RTZ; }
+
 attn_status_t fill_prefill_params(attn::PrefillParams *p, const DeviceInfo *di, float *lse, int B, int Hq,
                                   int Hkv, int Sq, int Sk, int layout, int causal, float scale) {
     p->B = B;
@@ -152,6 +154,7 @@ attn_status_t fill_prefill_params(attn::PrefillParams *p, const DeviceInfo *di, 
     p->status = di->status;
     p->budget_ns = budget();
     p->inject = 0;
+    p->round_mode = ATTN_ROUND_RTNE;
     p->n_full_units = attn::prefill_num_units(*p);
     p->split_units = 0;
     p->split_parts = 1;
@@ -164,14 +167,17 @@ attn_status_t fill_prefill_params(attn::PrefillParams *p, const DeviceInfo *di, 
 
 extern "C" {
 
-attn_status_t attn_fwd(const void *q, const void *k, const void *v, void *out, float *lse, int B, int Hq, int Hkv,
-                       int Sq, int Sk, int d, int layout, int causal, float scale, void *stream) {
+attn_status_t attn_fwd_rounded(const void *q, const void *k, const void *v, void *out, float *lse, int B, int Hq,
+                               int Hkv, int Sq, int Sk, int d, int layout, int causal, float scale, int round_mode,
+                               void *stream) {
     attn_status_t st = check_fwd_args(q, k, v, out, lse, B, Hq, Hkv, Sq, Sk, d, layout, scale);
     if (st != ATTN_OK) return st;
+    if (!valid_round_mode(round_mode)) return ATTN_ERR_INVALID_ARG;
     DeviceInfo *di = nullptr;
     if ((st = device_info(&di)) != ATTN_OK) return st;
     attn::PrefillParams p;
     fill_prefill_params(&p, di, lse, B, Hq, Hkv, Sq, Sk, layout, causal, scale);
+    p.round_mode = round_mode;
     p.inject = g_inject.exchange(0);
     const bool bhsd = p.bhsd != 0;
     CUtensorMap mq, mk, mv, mo;
@@ -202,6 +208,12 @@ attn_status_t attn_fwd(const void *q, const void *k, const void *v, void *out, f
         return ATTN_ERR_CUDA;
     if (attn::launch_prefill_merge(out, p, static_cast<cudaStream_t>(stream)) != cudaSuccess) return ATTN_ERR_CUDA;
     return ATTN_OK;
+}
+
+attn_status_t attn_fwd(const void *q, const void *k, const void *v, void *out, float *lse, int B, int Hq, int Hkv,
+                       int Sq, int Sk, int d, int layout, int causal, float scale, void *stream) {
+    return attn_fwd_rounded(q, k, v, out, lse, B, Hq, Hkv, Sq, Sk, d, layout, causal, scale, ATTN_ROUND_RTNE,
+                            stream);
 }
 
 size_t attn_fwd_workspace_bytes(int B, int Hq, int Hkv, int Sq, int Sk, int d, int causal) {
@@ -302,8 +314,9 @@ attn_status_t attn_decode_paged(const void *q, const void *k_pages, const void *
 }
 
 attn_status_t attn_lse_merge(const float *o_parts, const float *lse_parts, void *out, float *lse, int rows,
-                             int nsplit, int d, void *stream) {
+                             int nsplit, int d, int round_mode, void *stream) {
     if (!o_parts || !lse_parts || !out) return ATTN_ERR_INVALID_ARG;
+    if (!valid_round_mode(round_mode)) return ATTN_ERR_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(o_parts) & 3u) || (reinterpret_cast<uintptr_t>(lse_parts) & 3u) ||
         !aligned16(out) || (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)))
         return ATTN_ERR_INVALID_ARG;
@@ -312,7 +325,8 @@ attn_status_t attn_lse_merge(const float *o_parts, const float *lse_parts, void 
     attn_status_t st;
     DeviceInfo *di = nullptr;
     if ((st = device_info(&di)) != ATTN_OK) return st;
-    if (attn::launch_lse_merge(o_parts, lse_parts, out, lse, rows, nsplit, static_cast<cudaStream_t>(stream)) !=
+    if (attn::launch_lse_merge(o_parts, lse_parts, out, lse, rows, nsplit, round_mode,
+                               static_cast<cudaStream_t>(stream)) !=
         cudaSuccess)
         return ATTN_ERR_CUDA;
     return ATTN_OK;

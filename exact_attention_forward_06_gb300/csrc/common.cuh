@@ -88,4 +88,35 @@ __device__ __forceinline__ Coord4 coord4(bool bhsd, int c, int h, int s, int b) 
     return bhsd ? Coord4{c, s, h, b} : Coord4{c, h, s, b};
 }
 
+// ---------------------------------------------------------------------------
+// Rounding of fp32 results to the bf16 output: the three modes the MoonMath
+// HIP kernel page measures its bf16 output in (benchmark section).
+enum RoundMode : int {
+    kRoundRTNE = 0,  // to nearest, ties to even
+    kRoundRTNA = 1,  // to nearest, ties away from zero
+    kRoundRTZ = 2,   // toward zero
+};
+
+// Ties-away rounding on the bit pattern: adding half a bf16 unit (0x8000) to
+// the magnitude bits carries into the kept 16 bits exactly when the dropped
+// part is at least half a unit; a carry out of the significand moves the
+// exponent, and past the largest finite bf16 it reaches infinity.
+static __device__ __forceinline__ uint32_t bf16_bits_rna(float x) {
+    const uint32_t u = __float_as_uint(x);
+    const uint32_t mag = u & 0x7fffffffu;
+    if (mag > 0x7f800000u) return (u >> 16) | 0x40u;  // NaN stays a quiet NaN
+    return ((mag + 0x8000u) >> 16) | ((u >> 16) & 0x8000u);
+}
+
+// Two fp32 values to packed bf16 (lo in the low half) in the given mode.
+static __device__ __forceinline__ uint32_t pack_bf16x2_mode(float lo, float hi, int mode) {
+    if (mode == kRoundRTZ) return ptx::pack_bf16x2_rz(lo, hi);
+    if (mode == kRoundRTNA) return bf16_bits_rna(lo) | (bf16_bits_rna(hi) << 16);
+    return ptx::pack_bf16x2(lo, hi);
+}
+
+static __device__ __forceinline__ uint16_t bf16_bits_mode(float x, int mode) {
+    return (uint16_t)(pack_bf16x2_mode(x, 0.f, mode) & 0xffffu);
+}
+
 }  // namespace attn

@@ -326,8 +326,8 @@ __global__ void __launch_bounds__(NTHREADS, 3)
 // One CTA per row, one thread per head-dim element; splits merged in order.
 __global__ void __launch_bounds__(D) merge_kernel(const float *__restrict__ o_parts,
                                                   const float *__restrict__ lse_parts,
-                                                  __nv_bfloat16 *__restrict__ out, float *__restrict__ lse,
-                                                  int nsplit) {
+                                                  uint16_t *__restrict__ out, float *__restrict__ lse,
+                                                  int nsplit, int round_mode) {
     const int64_t r = blockIdx.x;
     const int e = threadIdx.x;
     const float *ls = lse_parts + r * nsplit;
@@ -341,7 +341,7 @@ __global__ void __launch_bounds__(D) merge_kernel(const float *__restrict__ o_pa
             o = fmaf(w, o_parts[(r * nsplit + s) * D + e], o);
         }
     }
-    out[r * D + e] = __float2bfloat16_rn(total > 0.f ? o / total : 0.f);
+    out[r * D + e] = bf16_bits_mode(total > 0.f ? o / total : 0.f, round_mode);
     if (e == 0 && lse != nullptr) lse[r] = total > 0.f ? M + ptx::lg2(total) * LN2 : -INFINITY;
 }
 
@@ -399,13 +399,13 @@ cudaError_t launch_decode(const CUtensorMap &mk, const CUtensorMap &mv, const De
         dec::split_kernel<1><<<grid, dec::NTHREADS, smem, stream>>>(mk, mv, p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    return launch_lse_merge(p.o_part, p.lse_part, p.out, p.lse, p.B * p.Hq, p.nsplit, stream);
+    return launch_lse_merge(p.o_part, p.lse_part, p.out, p.lse, p.B * p.Hq, p.nsplit, kRoundRTNE, stream);
 }
 
 cudaError_t launch_lse_merge(const float *o_parts, const float *lse_parts, void *out, float *lse, int rows,
-                             int nsplit, cudaStream_t stream) {
-    dec::merge_kernel<<<rows, dec::D, 0, stream>>>(o_parts, lse_parts, static_cast<__nv_bfloat16 *>(out), lse,
-                                                   nsplit);
+                             int nsplit, int round_mode, cudaStream_t stream) {
+    dec::merge_kernel<<<rows, dec::D, 0, stream>>>(o_parts, lse_parts, static_cast<uint16_t *>(out), lse, nsplit,
+                                                   round_mode);
     return cudaGetLastError();
 }
 

@@ -492,7 +492,7 @@ __device__ void softmax_wg(const PrefillParams &p, const Unit &w, const SmemLayo
                 float2 x = __fmul2_rn(make_float2(__uint_as_float(o[2 * i]), __uint_as_float(o[2 * i + 1])),
                                       make_float2(inv, inv));
                 if (!(l_run > 0.f)) x = make_float2(0.f, 0.f);
-                wv[i] = ptx::pack_bf16x2(x.x, x.y);
+                wv[i] = pack_bf16x2_mode(x.x, x.y, p.round_mode);
             }
             // 32 columns = 64 bytes = four 16-byte chunks of the 128-B swizzled row.
             uint8_t *rowp = stage + (ch >> 1) * HALF_BYTES + r * 128;
@@ -678,7 +678,7 @@ __global__ void __launch_bounds__(D) merge_kernel(__nv_bfloat16 *__restrict__ ou
         }
     }
     const int64_t off = p.bhsd ? (((int64_t)w.b * p.Hq + h) * p.Sq + s) * D : (((int64_t)w.b * p.Sq + s) * p.Hq + h) * D;
-    out[off + e] = __float2bfloat16_rn(total > 0.f ? o / total : 0.f);
+    reinterpret_cast<uint16_t *>(out)[off + e] = bf16_bits_mode(total > 0.f ? o / total : 0.f, p.round_mode);
     if (e == 0 && p.lse != nullptr)
         p.lse[((int64_t)w.b * p.Hq + h) * p.Sq + s] = total > 0.f ? M + ptx::lg2(total) * LN2 : -INFINITY;
 }

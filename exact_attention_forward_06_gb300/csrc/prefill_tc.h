@@ -19,6 +19,7 @@ struct PrefillParams {
     unsigned *status;  // device status word [code, site]
     uint64_t budget_ns;
     int inject;        // 1: producer issues nothing (fault-injection test)
+    int round_mode;    // RoundMode of the bf16 output (epilogue and merge)
     // Tail split: units [0, n_full_units) run whole; each of the following
     // split_units units is cut into split_parts key ranges, one CTA each, whose
     // fp32 partials go to ws_o [split_units*256][split_parts][128] and
@@ -63,7 +64,7 @@ void decode_split_plan(int B, int Hq, int max_blocks, int *nsplit, int *pages_pe
 cudaError_t launch_decode(const CUtensorMap &mk, const CUtensorMap &mv, const DecodeParams &p,
                           cudaStream_t stream);
 cudaError_t launch_lse_merge(const float *o_parts, const float *lse_parts, void *out, float *lse, int rows,
-                             int nsplit, cudaStream_t stream);
+                             int nsplit, int round_mode, cudaStream_t stream);
 
 // Tensor-core layout self-test.
 cudaError_t launch_selftest_umma(const CUtensorMap &ma, const CUtensorMap &mb, const void *a, float *c, int mode,

@@ -305,5 +305,12 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return r;
 }
 
+// The same conversion rounding toward zero.
+__device__ __forceinline__ uint32_t pack_bf16x2_rz(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rz.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
 }  // namespace ptx
 }  // namespace attn

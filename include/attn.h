@@ -23,7 +23,8 @@
  *     j <= i + Sk - Sq;
  *   - a row that sees no key gets O = 0 and lse = -inf;
  *   - lse is the natural log of the sum of exp of the *scaled* scores;
- *   - O is rounded to bf16 round-to-nearest-even.
+ *   - O is rounded to bf16 round-to-nearest-even, unless a call selects one of
+ *     the other two output rounding modes (attn_fwd_rounded).
  *
  * Conventions for every entry point:
  *   - Pointers named q, k, v, out, lse, k_pages, v_pages, block_table, seqlens,
@@ -67,6 +68,14 @@ typedef enum {
     ATTN_LAYOUT_BHSD = 1        /* [B][H][S][d] */
 } attn_layout_t;
 
+/* Rounding of the fp32 result to the bf16 output (the three modes of the
+ * MoonMath HIP kernel page's benchmark section). */
+typedef enum {
+    ATTN_ROUND_RTNE = 0,        /* to nearest, ties to even (the default) */
+    ATTN_ROUND_RTNA = 1,        /* to nearest, ties away from zero */
+    ATTN_ROUND_RTZ = 2          /* toward zero; never overflows to infinity */
+} attn_round_t;
+
 /*
  * attn_fwd -- fused exact attention forward (prefill), tcgen05 + TMA kernel.
  *
@@ -84,6 +93,24 @@ typedef enum {
 attn_status_t attn_fwd(const void *q, const void *k, const void *v, void *out, float *lse,
                        int B, int Hq, int Hkv, int Sq, int Sk, int d,
                        int layout, int causal, float scale, void *stream);
+
+/*
+ * attn_fwd_rounded -- attn_fwd with a selectable rounding of the output.
+ *
+ * The MoonMath HIP kernel page (benchmark and limitations sections) runs its
+ * bf16 forward kernel in three rounding modes, RTNE, RTNA and RTZ, each with
+ * its own rule for the bf16 output.  round_mode (an attn_round_t) selects
+ * how each element of O, computed in fp32, is rounded to bf16; attn_fwd is
+ * this call with ATTN_ROUND_RTNE.  The mode changes nothing but that last
+ * conversion (in the kernel's epilogue and in the tail-split merge): the
+ * fp32 value before it, lse, and the internal bf16 rounding of the
+ * probabilities before the P V product (always to nearest even) are the same
+ * in every mode.  Other arguments, errors and determinism as attn_fwd; a
+ * round_mode outside the enum returns ATTN_ERR_INVALID_ARG.
+ */
+attn_status_t attn_fwd_rounded(const void *q, const void *k, const void *v, void *out, float *lse,
+                               int B, int Hq, int Hkv, int Sq, int Sk, int d,
+                               int layout, int causal, float scale, int round_mode, void *stream);
 
 /*
  * attn_fwd_workspace_bytes -- device workspace that lets attn_fwd split the
@@ -198,11 +225,12 @@ attn_status_t attn_decode_paged_noalloc(const void *q, const void *k_pages, cons
  * in a fixed split order (deterministic).  Rows whose partials are all -inf
  * get out = 0 and lse = -inf.
  * o_parts: fp32 [rows][nsplit][d], each partial normalised within its range.
- * lse_parts: fp32 [rows][nsplit].  out: bf16 [rows][d].  lse: fp32 [rows] or NULL.
- * d must be 128; nsplit >= 1.
+ * lse_parts: fp32 [rows][nsplit].  out: bf16 [rows][d], rounded from fp32 in
+ * round_mode (an attn_round_t; anything else is ATTN_ERR_INVALID_ARG).
+ * lse: fp32 [rows] or NULL.  d must be 128; nsplit >= 1.
  */
 attn_status_t attn_lse_merge(const float *o_parts, const float *lse_parts, void *out, float *lse,
-                             int rows, int nsplit, int d, void *stream);
+                             int rows, int nsplit, int d, int round_mode, void *stream);
 
 /*
  * attn_get_device_status -- synchronise `stream`, then read and clear the

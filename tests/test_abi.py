@@ -103,9 +103,23 @@ def test_decode_rejects_bad_arguments_before_any_launch(lib, kw, code):
 
 
 def test_merge_rejects_bad_arguments(lib):
-    assert lib.attn_lse_merge(None, 16, 16, None, 4, 2, 128, None) == 1
-    assert lib.attn_lse_merge(16, 16, 16, None, 0, 2, 128, None) == 1
-    assert lib.attn_lse_merge(16, 16, 16, None, 4, 2, 64, None) == 2
+    assert lib.attn_lse_merge(None, 16, 16, None, 4, 2, 128, 0, None) == 1
+    assert lib.attn_lse_merge(16, 16, 16, None, 0, 2, 128, 0, None) == 1
+    assert lib.attn_lse_merge(16, 16, 16, None, 4, 2, 64, 0, None) == 2
+    assert lib.attn_lse_merge(16, 16, 16, None, 4, 2, 128, 3, None) == 1     # no such rounding mode
+    assert lib.attn_lse_merge(16, 16, 16, None, 4, 2, 128, -1, None) == 1
+
+
+@pytest.mark.parametrize("kw,code", [(dict(q=None), 1), (dict(d=64), 2), (dict(mode=3), 1), (dict(mode=-1), 1)])
+def test_fwd_rounded_validates_before_any_launch(lib, kw, code):
+    a = dict(q=16, mode=1, d=128)
+    a.update(kw)
+    assert lib.attn_fwd_rounded(a["q"], 16, 16, 16, None, 1, 2, 2, 8, 8, a["d"], 0, 0, 0.1, a["mode"], None) == code
+
+
+def test_python_rounding_names_are_checked(lib):
+    with pytest.raises(ValueError):
+        A.fwd(None, None, None, rounding="rtn")
 
 
 def test_debug_controls(lib):
