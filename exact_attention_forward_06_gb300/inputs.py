@@ -77,6 +77,64 @@ class DecodeWorkload:
         return dataclasses.replace(self, **kw)
 
 
+@dataclasses.dataclass(frozen=True)
+class VarlenWorkload:
+    """A packed variable-length batch: sequence b owns rows cu_q[b] .. cu_q[b+1]-1
+    of q [total_q, Hq, d] and rows cu_k[b] .. cu_k[b+1]-1 of k, v [total_k, Hkv, d].
+
+    Query lengths are drawn U[len_lo, len_hi] (or given in lens_q); key lengths
+    equal them unless lens_k is given (cross-attention per sequence)."""
+    name: str
+    B: int
+    Hq: int
+    Hkv: int
+    len_lo: int = 1
+    len_hi: int = 1
+    causal: bool = False
+    seed: int = 0
+    lens_q: tuple = None
+    lens_k: tuple = None
+    d: int = 128
+    pad_q: int = 0   # unused rows after the last sequence (outputs there are left alone)
+
+    @property
+    def scale(self) -> float:
+        return float(torch.tensor(1.0 / math.sqrt(self.d), dtype=torch.float32).item())
+
+    def lengths(self):
+        gen = torch.Generator().manual_seed(self.seed)
+        if self.lens_q is None:
+            lq = torch.randint(self.len_lo, self.len_hi + 1, (self.B,), generator=gen, dtype=torch.int64).tolist()
+        else:
+            lq = list(self.lens_q)
+        lk = list(lq) if self.lens_k is None else list(self.lens_k)
+        assert len(lq) == self.B and len(lk) == self.B
+        return lq, lk
+
+    @property
+    def flops(self) -> float:
+        """4 * Hq * d * Lq * Lk per sequence, halved when causal (the dense convention)."""
+        lq, lk = self.lengths()
+        f = sum(4.0 * self.Hq * self.d * a * b for a, b in zip(lq, lk))
+        return f / 2 if self.causal else f
+
+
+def make_varlen(w: VarlenWorkload):
+    """(q [total_q, Hq, d], k, v [total_k, Hkv, d] CPU bf16, cu_q, cu_k [B+1] int32)."""
+    lq, lk = w.lengths()
+    cu_q = torch.zeros(w.B + 1, dtype=torch.int32)
+    cu_k = torch.zeros(w.B + 1, dtype=torch.int32)
+    cu_q[1:] = torch.cumsum(torch.tensor(lq, dtype=torch.int64), 0).to(torch.int32)
+    cu_k[1:] = torch.cumsum(torch.tensor(lk, dtype=torch.int64), 0).to(torch.int32)
+    gen = torch.Generator().manual_seed(w.seed + 1000)
+    total_q = int(cu_q[-1]) + w.pad_q
+    total_k = int(cu_k[-1])
+    q = _randn_bf16((total_q, w.Hq, w.d), gen)
+    k = _randn_bf16((max(total_k, 1), w.Hkv, w.d), gen)
+    v = _randn_bf16((max(total_k, 1), w.Hkv, w.d), gen)
+    return q, k, v, cu_q, cu_k
+
+
 # The five workloads: a tiny BHSD case, GQA causal, long MQA causal with
 # peaked rows, ragged non-causal self- and cross-attention, and paged decode.
 TINY_BHSD = PrefillWorkload("tiny_bhsd_1x2x256", 1, 2, 2, 256, 256, layout="bhsd", seed=1)
@@ -88,6 +146,10 @@ RAGGED_CROSS = PrefillWorkload("ragged_cross_2x12_32760x512", 2, 12, 12, 32760, 
 PAGED_DECODE = DecodeWorkload("paged_decode_32seq_32q8kv")
 
 PREFILL_WORKLOADS = {w.name: w for w in (TINY_BHSD, GQA_CAUSAL, MQA_CAUSAL, RAGGED_SELF, RAGGED_CROSS)}
+# A packed batch of 16 GQA sequences of mixed lengths, causal (the varlen case).
+VARLEN_CAUSAL = VarlenWorkload("varlen_causal_16seq_32q8kv", 16, 32, 8, len_lo=256, len_hi=8192, causal=True,
+                               seed=6)
+VARLEN_WORKLOADS = {VARLEN_CAUSAL.name: VARLEN_CAUSAL}
 
 
 def _randn_bf16(shape, gen: torch.Generator) -> torch.Tensor:

@@ -146,6 +146,40 @@ def attention(q, k, v, *, B, Hq, Hkv, Sq, Sk, d=128, layout="bshd", causal=False
     return out, lse
 
 
+def attention_varlen(q, k, v, cu_q, cu_k, *, Hq, Hkv, d=128, causal=False, scale, seqs=None):
+    """A packed variable-length batch, one sequence at a time.
+
+    q [total_q, Hq, d], k and v [total_k, Hkv, d] (bf16); sequence b owns rows
+    cu_q[b] .. cu_q[b+1]-1 of q and cu_k[b] .. cu_k[b+1]-1 of k and v, and its
+    rows attend only to its own keys: each sequence is the plain attention
+    above with B = 1, Sq = its query length and Sk = its key length (causal
+    alignment bottom-right within the sequence).  A sequence with queries but
+    no keys gives O = 0 and lse = -inf (a row that sees no key).
+
+    Returns (out [total_q, Hq, d] float64, lse [Hq, total_q] float64); rows
+    that belong to no sequence (or to a sequence not in `seqs`, when given)
+    are NaN.
+    """
+    cu_q = [int(x) for x in cu_q]
+    cu_k = [int(x) for x in cu_k]
+    total_q = q.shape[0]
+    out = np.full((total_q, Hq, d), np.nan)
+    lse = np.full((Hq, total_q), np.nan)
+    for b in (range(len(cu_q) - 1) if seqs is None else seqs):
+        q0, q1, k0, k1 = cu_q[b], cu_q[b + 1], cu_k[b], cu_k[b + 1]
+        if q1 == q0:
+            continue
+        if k1 == k0:
+            out[q0:q1] = 0.0
+            lse[:, q0:q1] = -np.inf
+            continue
+        o_b, l_b = attention(q[q0:q1][None], k[k0:k1][None], v[k0:k1][None], B=1, Hq=Hq, Hkv=Hkv,
+                             Sq=q1 - q0, Sk=k1 - k0, d=d, causal=causal, scale=scale)
+        out[q0:q1] = o_b[0]
+        lse[:, q0:q1] = l_b[0]
+    return out, lse
+
+
 def attention_rows(q, k, v, rows, *, B, Hq, Hkv, Sq, Sk, d=128, layout="bshd", causal=False,
                    scale, key_range=None):
     """Selected rows (an [n, 3] array of (b, h, i)), optionally over keys [lo, hi).

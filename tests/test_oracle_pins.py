@@ -100,6 +100,47 @@ def test_matches_torch_sdpa_fp64(B, Hq, Hkv, Sq, Sk, causal, layout):
     np.testing.assert_allclose(out, ref, rtol=1e-10, atol=1e-12)
 
 
+# ---------------------------------------------------------------- packed variable-length batches
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_varlen_matches_sdpa_per_sequence(causal):
+    d, Hq, Hkv = 32, 4, 2
+    lq, lk = (5, 0, 17, 1, 33, 6), (9, 4, 17, 1, 20, 0)
+    w = inputs.VarlenWorkload("v", len(lq), Hq, Hkv, causal=causal, seed=13, lens_q=lq, lens_k=lk, d=d, pad_q=3)
+    q, k, v, cu_q, cu_k = inputs.make_varlen(w)
+    scale = 1.0 / math.sqrt(d)
+    out, lse = oracle.attention_varlen(q, k, v, cu_q, cu_k, Hq=Hq, Hkv=Hkv, d=d, causal=causal, scale=scale)
+    for b in range(len(lq)):
+        q0, k0 = int(cu_q[b]), int(cu_k[b])
+        if lq[b] == 0:
+            continue
+        o_b = out[q0:q0 + lq[b]]
+        if lk[b] == 0:
+            assert (o_b == 0).all() and (lse[:, q0:q0 + lq[b]] == -np.inf).all()
+            continue
+        ref = _sdpa_reference(q[q0:q0 + lq[b]][None], k[k0:k0 + lk[b]][None], v[k0:k0 + lk[b]][None], causal,
+                              scale)[0]
+        # causal rows that see no key (i < Lq - Lk) are O = 0, lse = -inf; SDPA gives NaN there
+        blind = max(0, lq[b] - lk[b]) if causal else 0
+        np.testing.assert_allclose(o_b[blind:], ref[blind:], rtol=1e-10, atol=1e-12)
+        assert (o_b[:blind] == 0).all() and (lse[:, q0:q0 + blind] == -np.inf).all()
+        assert np.isfinite(lse[:, q0 + blind:q0 + lq[b]]).all()
+    assert np.isnan(out[-3:]).all() and np.isnan(lse[:, -3:]).all()   # rows of no sequence
+
+
+def test_varlen_equal_lengths_is_the_dense_batch():
+    B, L, Hq, Hkv, d = 3, 20, 4, 2, 16
+    w = inputs.PrefillWorkload("t", B, Hq, Hkv, L, L, d=d, causal=True, seed=14)
+    q, k, v = inputs.make_prefill(w)
+    scale = 0.25
+    dense_o, dense_l = oracle.attention(q, k, v, B=B, Hq=Hq, Hkv=Hkv, Sq=L, Sk=L, d=d, causal=True, scale=scale)
+    cu = torch.arange(0, (B + 1) * L, L, dtype=torch.int32)
+    vo, vl = oracle.attention_varlen(q.reshape(B * L, Hq, d), k.reshape(B * L, Hkv, d), v.reshape(B * L, Hkv, d),
+                                     cu, cu, Hq=Hq, Hkv=Hkv, d=d, causal=True, scale=scale)
+    np.testing.assert_array_equal(vo, dense_o.reshape(B * L, Hq, d))
+    np.testing.assert_array_equal(vl, dense_l.transpose(1, 0, 2).reshape(Hq, B * L))
+
+
 # ---------------------------------------------------------------- closed forms
 
 def test_identical_keys_give_mean_of_v():
