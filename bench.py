@@ -155,6 +155,78 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+# ---------------------------------------------------------------------------- prefill cases
+
+class DenseCase:
+    """A dense batch (attn_fwd): B sequences of equal lengths in BSHD or BHSD."""
+
+    def __init__(self, w):
+        self.w = w
+        self.name = w.name
+        self.flops = w.flops
+        self.host = inputs.make_prefill(w)
+        self.lse_shape = (w.B, w.Hq, w.Sq)
+        self.config = {"B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "Sq": w.Sq, "Sk": w.Sk, "d": w.d, "layout": w.layout,
+                       "causal": w.causal}
+        self.flop_note = "4*B*Hq*Sq*Sk*d" + ("/2" if w.causal else "")
+        self.api = "exact_attention_forward_06_gb300.fwd (C ABI attn_fwd)"
+
+    def units(self):
+        return prefill_units(self.w)
+
+    def workspace_bytes(self, A):
+        w = self.w
+        return A.fwd_workspace_bytes(w.B, w.Hq, w.Hkv, w.Sq, w.Sk, w.d, w.causal)
+
+    def call(self, A, dev_in, out, lse, stream):
+        q, k, v = dev_in
+        w = self.w
+        A.fwd(q, k, v, causal=w.causal, scale=w.scale, layout=w.layout, out=out, lse=lse, stream=stream)
+
+    def oracle_sample(self, seconds, seed):
+        q_h, k_h, v_h = self.host
+        return _oracle_sample(self.w, q_h, k_h, v_h, seconds, seed)
+
+
+class VarlenCase:
+    """A packed batch of variable-length sequences (attn_fwd_varlen)."""
+
+    def __init__(self, w):
+        self.w = w
+        self.name = w.name
+        self.flops = w.flops
+        self.host = inputs.make_varlen(w)
+        self.lq, self.lk = w.lengths()
+        total_q = self.host[0].shape[0]
+        self.lse_shape = (w.Hq, total_q)
+        self.config = {"B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "total_q": total_q, "total_k": self.host[1].shape[0],
+                       "lengths": f"U[{w.len_lo},{w.len_hi}] seed {w.seed}", "max_seqlen": max(self.lq), "d": w.d,
+                       "layout": "thd (packed)", "causal": w.causal}
+        self.flop_note = "sum over sequences of 4*Hq*Lq*Lk*d" + ("/2" if w.causal else "")
+        self.api = "exact_attention_forward_06_gb300.fwd_varlen (C ABI attn_fwd_varlen)"
+
+    def units(self):
+        return None   # units differ in size: no per-unit traffic figure
+
+    def workspace_bytes(self, A):
+        return 0
+
+    def call(self, A, dev_in, out, lse, stream):
+        q, k, v, cu_q, cu_k = dev_in
+        w = self.w
+        A.fwd_varlen(q, k, v, cu_q, cu_k, max_seqlen_q=max(self.lq), max_seqlen_k=max(self.lk), causal=w.causal,
+                     scale=w.scale, out=out, lse=lse, stream=stream)
+
+    def oracle_sample(self, seconds, seed):
+        return _oracle_sample_varlen(self, seconds, seed)
+
+
+def make_case(name):
+    if name in inputs.VARLEN_WORKLOADS:
+        return VarlenCase(inputs.VARLEN_WORKLOADS[name])
+    return DenseCase(inputs.PREFILL_WORKLOADS[name])
+
+
 # ---------------------------------------------------------------------------- our arm
 
 def run_ours(args, rank, world, local_rank):
@@ -163,27 +235,26 @@ def run_ours(args, rank, world, local_rank):
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
     peaks, peak_src = load_peaks()
-    wp = inputs.PREFILL_WORKLOADS[args.workload]
+    case = make_case(args.workload)
     wd = inputs.PAGED_DECODE
 
     # Inputs (seeded, synthetic), resident on the device.
-    q_h, k_h, v_h = inputs.make_prefill(wp)
-    q, k, v = (t.to(dev) for t in (q_h, k_h, v_h))
-    out = torch.empty_like(q)
-    lse = torch.empty((wp.B, wp.Hq, wp.Sq), device=dev, dtype=torch.float32)
+    dev_in = [t.to(dev) for t in case.host]
+    out = torch.empty_like(dev_in[0])
+    lse = torch.empty(case.lse_shape, device=dev, dtype=torch.float32)
     dq_h, kp_h, vp_h, table_h, lens_h = inputs.make_decode(wd)
     dq, kp, vp, table, lens = (t.to(dev) for t in (dq_h, kp_h, vp_h, table_h, lens_h))
     dout = torch.empty_like(dq)
     dlse = torch.empty((wd.B, wd.Hq), device=dev, dtype=torch.float32)
     ws = torch.empty(A.decode_workspace_bytes(wd.B, wd.Hq, wd.d, wd.max_blocks), device=dev, dtype=torch.uint8)
     # Workspace for the prefill's tail split, when the shape gets one on this device.
-    fws_bytes = A.fwd_workspace_bytes(wp.B, wp.Hq, wp.Hkv, wp.Sq, wp.Sk, wp.d, wp.causal)
+    fws_bytes = case.workspace_bytes(A)
     fws = torch.empty(fws_bytes, device=dev, dtype=torch.uint8) if fws_bytes else None
     A.set_workspace(fws)
     stream = torch.cuda.current_stream(dev)
 
     def prefill():
-        A.fwd(q, k, v, causal=wp.causal, scale=wp.scale, layout=wp.layout, out=out, lse=lse, stream=stream)
+        case.call(A, dev_in, out, lse, stream)
 
     def decode():
         A.decode_paged(dq, kp, vp, table, lens, scale=wd.scale, out=dout, lse=dlse, workspace=ws, stream=stream)
@@ -223,17 +294,17 @@ def run_ours(args, rank, world, local_rank):
     decode_ms = reduce_max_over_ranks(decode_ms)
 
     # End to end through the public API: pinned host inputs -> device -> result back to pinned host.
-    e2e = run_e2e(A, wp, q_h, k_h, v_h, dev, stream, args)
+    e2e = run_e2e(A, case, dev, stream, args)
 
     if rank != 0:
         return None
-    flops = wp.flops
+    flops = case.flops
     tflops = world * flops / (prefill_ms * 1e-3) / 1e12
     per_launch_tflops = flops / (prefill_ms * 1e-3) / 1e12
     kv_bytes = inputs.decode_kv_bytes(lens_h.tolist(), wd.Hkv, wd.d)
     dec_gbs_launch = kv_bytes / (decode_ms * 1e-3) / 1e9
-    n_units = prefill_units(wp)
-    traffic = traffic_for("prefill_kernel", PREFILL_KERNEL_SRC, n_units)
+    n_units = case.units()
+    traffic = traffic_for("prefill_kernel", PREFILL_KERNEL_SRC, n_units) if n_units else None
     dec_traffic = traffic_for("decode_split_kernel", DECODE_KERNEL_SRC, sum(int(x) for x in lens_h.tolist()))
     clk = clocks.summary()
     line = {
@@ -249,8 +320,7 @@ def run_ours(args, rank, world, local_rank):
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic (seeded randn, bf16)",
-        "config": {"workload": wp.name, "B": wp.B, "Hq": wp.Hq, "Hkv": wp.Hkv, "Sq": wp.Sq, "Sk": wp.Sk,
-                   "d": wp.d, "layout": wp.layout, "causal": wp.causal,
+        "config": {"workload": case.name, **case.config,
                    "decode_workload": wd.name, "decode_B": wd.B, "decode_Hq": wd.Hq, "decode_Hkv": wd.Hkv,
                    "decode_lengths": f"U[{wd.len_lo},{wd.len_hi}] seed {wd.seed}, sum {int(lens_h.sum())}",
                    "page_size": wd.page_size, "l2": "inputs larger than L2 (no flush)",
@@ -262,7 +332,7 @@ def run_ours(args, rank, world, local_rank):
                      "frac": round(per_launch_tflops / peaks["bf16_tflops"], 4),
                      "traffic": traffic, "peak_source": f"{peak_src} bf16_tflops (burst)",
                      "kernel": "attn::g1::prefill_kernel",
-                     "algorithmic": f"{flops:.4g} flop per launch (4*B*Hq*Sq*Sk*d/2)"},
+                     "algorithmic": f"{flops:.4g} flop per launch ({case.flop_note})"},
         "decode": {"value": round(dec_gbs_launch * world, 1), "unit": "GB/s", "ms_per_launch": round(decode_ms, 4),
                    "roofline": {"bound": "hbm", "achieved": round(dec_gbs_launch, 1), "peak": peaks["hbm_gbs"],
                                 "unit": "GB/s", "frac": round(dec_gbs_launch / peaks["hbm_gbs"], 4),
@@ -274,7 +344,7 @@ def run_ours(args, rank, world, local_rank):
         "clocks": clk,
     }
     if not args.no_cpu_baseline and world == 1:
-        line["cpu_baseline"] = cpu_baseline(wp, q_h, k_h, v_h, seconds=args.cpu_seconds)
+        line["cpu_baseline"] = cpu_baseline(case, seconds=args.cpu_seconds)
     return line
 
 
@@ -287,21 +357,18 @@ def prefill_units(w):
     return w.B * w.Hq * ((n_m + 1) // 2)
 
 
-def run_e2e(A, w, q_h, k_h, v_h, dev, stream, args):
-    qp, kp, vp = (t.pin_memory() for t in (q_h, k_h, v_h))
-    q = torch.empty_like(qp, device=dev)
-    k = torch.empty_like(kp, device=dev)
-    v = torch.empty_like(vp, device=dev)
-    out_h = torch.empty_like(qp).pin_memory()
-    lse_h = torch.empty((w.B, w.Hq, w.Sq), dtype=torch.float32).pin_memory()
-    out = torch.empty_like(q)
-    lse = torch.empty((w.B, w.Hq, w.Sq), device=dev, dtype=torch.float32)
+def run_e2e(A, case, dev, stream, args):
+    pinned = [t.pin_memory() for t in case.host]
+    dev_in = [torch.empty_like(t, device=dev) for t in pinned]
+    out_h = torch.empty_like(pinned[0]).pin_memory()
+    lse_h = torch.empty(case.lse_shape, dtype=torch.float32).pin_memory()
+    out = torch.empty_like(dev_in[0])
+    lse = torch.empty(case.lse_shape, device=dev, dtype=torch.float32)
 
     def step():
-        q.copy_(qp, non_blocking=True)
-        k.copy_(kp, non_blocking=True)
-        v.copy_(vp, non_blocking=True)
-        A.fwd(q, k, v, causal=w.causal, scale=w.scale, layout=w.layout, out=out, lse=lse, stream=stream)
+        for d_t, h_t in zip(dev_in, pinned):
+            d_t.copy_(h_t, non_blocking=True)
+        case.call(A, dev_in, out, lse, stream)
         out_h.copy_(out, non_blocking=True)
         lse_h.copy_(lse, non_blocking=True)
 
@@ -318,11 +385,11 @@ def run_e2e(A, w, q_h, k_h, v_h, dev, stream, args):
     torch.cuda.synchronize(dev)
     ms = reduce_max_over_ranks(s.elapsed_time(e) / n)
     world = _world()
-    h2d = sum(t.numel() * t.element_size() for t in (qp, kp, vp))
+    h2d = sum(t.numel() * t.element_size() for t in pinned)
     d2h = out_h.numel() * out_h.element_size() + lse_h.numel() * lse_h.element_size()
-    return {"value": round(world * w.flops / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+    return {"value": round(world * case.flops / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 4),
-            "api": "exact_attention_forward_06_gb300.fwd (C ABI attn_fwd) with pinned host copies"}
+            "api": f"{case.api} with pinned host copies"}
 
 
 # ---------------------------------------------------------------------------- CPU oracle arms
@@ -359,26 +426,60 @@ def _oracle_sample(w, q_h, k_h, v_h, seconds, seed):
     return _row_flops(w, rows), dt, n
 
 
-def cpu_baseline(w, q_h, k_h, v_h, seconds):
+def _oracle_sample_varlen(case, seconds, seed):
+    """Uniformly drawn (sequence, head, row) triples of a packed batch, each row
+    through the oracle over its own sequence."""
+    import numpy as np
     import oracle
-    flops, dt, n = _oracle_sample(w, q_h, k_h, v_h, seconds, seed=1)
+    w = case.w
+    q_h, k_h, v_h, cu_q, cu_k = case.host
+    rng = np.random.default_rng(seed)
+    weights = np.array(case.lq, dtype=np.float64) / sum(case.lq)
+
+    def run(n):
+        seqs = rng.choice(w.B, size=n, p=weights)
+        flops = 0
+        for b in np.unique(seqs):
+            m = int((seqs == b).sum())
+            Lq, Lk = case.lq[b], case.lk[b]
+            q0, k0 = int(cu_q[b]), int(cu_k[b])
+            rows = np.stack([np.zeros(m, np.int64), rng.integers(0, w.Hq, m), rng.integers(0, Lq, m)], 1)
+            oracle.attention_rows(q_h[q0:q0 + Lq][None], k_h[k0:k0 + Lk][None], v_h[k0:k0 + Lk][None], rows, B=1,
+                                  Hq=w.Hq, Hkv=w.Hkv, Sq=Lq, Sk=Lk, d=w.d, causal=w.causal, scale=w.scale)
+            for i in rows[:, 2]:
+                nk = min(Lk, int(i) + 1 + Lk - Lq) if w.causal else Lk
+                flops += 4 * w.d * max(0, nk)
+        return flops
+
+    t0 = time.perf_counter()
+    probe_n = max(8, oracle.num_threads())
+    run(probe_n)
+    dt = time.perf_counter() - t0
+    n = max(probe_n, int(probe_n * seconds / max(dt, 1e-3)))
+    t0 = time.perf_counter()
+    flops = run(n)
+    return flops, time.perf_counter() - t0, n
+
+
+def cpu_baseline(case, seconds):
+    import oracle
+    flops, dt, n = case.oracle_sample(seconds, seed=1)
     return {"value": round(flops / dt / 1e12, 6), "unit": "TFLOP/s", "cores": oracle.num_threads(),
             "kind": "oracle",
-            "sample": f"{n} uniformly drawn query rows of {w.name} (fp64 C oracle, OpenMP), {dt:.1f} s"}
+            "sample": f"{n} uniformly drawn query rows of {case.name} (fp64 C oracle, OpenMP), {dt:.1f} s"}
 
 
 def run_reference(args, rank, world):
     import oracle
     if rank != 0:
         return None
-    w = inputs.PREFILL_WORKLOADS[args.workload]
-    q_h, k_h, v_h = inputs.make_prefill(w)
+    case = make_case(args.workload)
     per_step = max(1.0, min(6.0, 60.0 / max(1, args.steps + args.warmup)))
     for i in range(args.warmup):
-        _oracle_sample(w, q_h, k_h, v_h, per_step / 2, seed=100 + i)
+        case.oracle_sample(per_step / 2, seed=100 + i)
     tot_flops, tot_t, tot_rows = 0, 0.0, 0
     for i in range(args.steps):
-        f, dt, n = _oracle_sample(w, q_h, k_h, v_h, per_step, seed=i)
+        f, dt, n = case.oracle_sample(per_step, seed=i)
         tot_flops += f
         tot_t += dt
         tot_rows += n
@@ -389,11 +490,10 @@ def run_reference(args, rank, world):
         "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(1e3 * tot_t / args.steps, 2), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded randn, bf16 inputs)",
-        "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "Sq": w.Sq, "Sk": w.Sk, "d": w.d,
-                   "layout": w.layout, "causal": w.causal},
+        "config": {"workload": case.name, **case.config},
         "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": oracle.num_threads(),
                          "kind": "oracle",
-                         "sample": f"{tot_rows} uniformly drawn query rows of {w.name} over {args.steps} steps"},
+                         "sample": f"{tot_rows} uniformly drawn query rows of {case.name} over {args.steps} steps"},
         "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
     }
@@ -411,7 +511,8 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default=inputs.GQA_CAUSAL.name, choices=sorted(inputs.PREFILL_WORKLOADS))
+    ap.add_argument("--workload", default=inputs.GQA_CAUSAL.name,
+                    choices=sorted(inputs.PREFILL_WORKLOADS) + sorted(inputs.VARLEN_WORKLOADS))
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)

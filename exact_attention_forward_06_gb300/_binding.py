@@ -52,6 +52,8 @@ def load():
             lib.attn_fwd.argtypes = fwd_args
             lib.attn_fwd_simple.argtypes = fwd_args
             lib.attn_fwd_rounded.argtypes = fwd_args[:-1] + [_i, _p]
+            lib.attn_fwd_varlen.argtypes = [_p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _i, _i, _f,
+                                            _i, _p]
             lib.attn_fwd_workspace_bytes.argtypes = [_i, _i, _i, _i, _i, _i, _i]
             lib.attn_fwd_workspace_bytes.restype = _sz
             lib.attn_set_workspace.argtypes = [_p, _sz]
@@ -71,7 +73,8 @@ def load():
             lib.attn_status_string.argtypes = [_i]
             lib.attn_status_string.restype = ctypes.c_char_p
             lib.attn_version.restype = _i
-            for name in ("attn_fwd", "attn_fwd_simple", "attn_fwd_rounded", "attn_decode_paged", "attn_lse_merge",
+            for name in ("attn_fwd", "attn_fwd_simple", "attn_fwd_rounded", "attn_fwd_varlen", "attn_decode_paged",
+                         "attn_lse_merge",
                          "attn_get_device_status", "attn_set_wait_budget_ns", "attn_debug_inject",
                          "attn_selftest_umma"):
                 getattr(lib, name).restype = _i
@@ -154,6 +157,51 @@ def fwd(q, k, v, *, causal=False, scale=None, layout="bshd", out=None, lse=None,
     if rounding not in ROUNDING:
         raise ValueError(f"rounding must be one of {sorted(ROUNDING)}, got {rounding!r}")
     return _fwd_call("attn_fwd", q, k, v, causal, scale, layout, out, lse, stream, rounding)
+
+
+def fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, *, max_seqlen_q=None, max_seqlen_k=None, causal=False,
+               scale=None, out=None, lse=None, stream=None, rounding="rtne"):
+    """Attention over a packed batch of variable-length sequences.
+
+    q [total_q, Hq, d], k and v [total_k, Hkv, d] bf16; cu_seqlens_q/k int32 [B+1]
+    on the device.  Returns (out [total_q, Hq, d] bf16, lse [Hq, total_q] fp32).
+    max_seqlen_q/k bound the sequence lengths; when omitted they are read from
+    the offsets, which copies them to the host (a synchronisation).  Rows of
+    ``out``/``lse`` outside every sequence are left as given.
+    """
+    lib = load()
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _dev_tensor(t, n, torch.bfloat16)
+    _dev_tensor(cu_seqlens_q, "cu_seqlens_q", torch.int32)
+    _dev_tensor(cu_seqlens_k, "cu_seqlens_k", torch.int32)
+    if rounding not in ROUNDING:
+        raise ValueError(f"rounding must be one of {sorted(ROUNDING)}, got {rounding!r}")
+    if q.dim() != 3 or k.dim() != 3 or k.shape != v.shape:
+        raise ValueError("q must be [total_q, Hq, d] and k, v [total_k, Hkv, d]")
+    total_q, Hq, d = q.shape
+    total_k, Hkv, _ = k.shape
+    B = cu_seqlens_q.numel() - 1
+    if cu_seqlens_k.numel() != B + 1 or B < 1:
+        raise ValueError("cu_seqlens_q and cu_seqlens_k must both have B + 1 entries, B >= 1")
+    if max_seqlen_q is None:
+        max_seqlen_q = max(1, int(torch.diff(cu_seqlens_q).max()))
+    if max_seqlen_k is None:
+        max_seqlen_k = max(1, int(torch.diff(cu_seqlens_k).max()))
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((Hq, total_q), device=q.device, dtype=torch.float32)
+    elif lse is not False:
+        _dev_tensor(lse, "lse", torch.float32)
+    lse_ptr = None if lse is False else lse.data_ptr()
+    rc = lib.attn_fwd_varlen(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse_ptr,
+                             cu_seqlens_q.data_ptr(), cu_seqlens_k.data_ptr(), B, Hq, Hkv, total_q, total_k,
+                             int(max_seqlen_q), int(max_seqlen_k), d, int(bool(causal)), float(scale),
+                             ROUNDING[rounding], _stream(stream))
+    _check(rc, "attn_fwd_varlen")
+    return out, (None if lse is False else lse)
 
 
 def fwd_simple(q, k, v, *, causal=False, scale=None, layout="bshd", out=None, lse=None, stream=None):

@@ -160,6 +160,11 @@ attn_status_t fill_prefill_params(attn::PrefillParams *p, const DeviceInfo *di, 
     p->split_parts = 1;
     p->ws_o = nullptr;
     p->ws_lse = nullptr;
+    p->cu_q = nullptr;
+    p->cu_k = nullptr;
+    p->total_q = 0;
+    p->total_k = 0;
+    p->out = nullptr;
     return ATTN_OK;
 }
 
@@ -214,6 +219,42 @@ attn_status_t attn_fwd(const void *q, const void *k, const void *v, void *out, f
                        int Sq, int Sk, int d, int layout, int causal, float scale, void *stream) {
     return attn_fwd_rounded(q, k, v, out, lse, B, Hq, Hkv, Sq, Sk, d, layout, causal, scale, ATTN_ROUND_RTNE,
                             stream);
+}
+
+attn_status_t attn_fwd_varlen(const void *q, const void *k, const void *v, void *out, float *lse,
+                              const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k, int B, int Hq, int Hkv,
+                              int total_q, int total_k, int max_seqlen_q, int max_seqlen_k, int d, int causal,
+                              float scale, int round_mode, void *stream) {
+    if (!cu_seqlens_q || !cu_seqlens_k) return ATTN_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(cu_seqlens_q) & 3u) || (reinterpret_cast<uintptr_t>(cu_seqlens_k) & 3u))
+        return ATTN_ERR_INVALID_ARG;
+    // The packed tensors are checked as one dense [1][total][H][d] batch.
+    attn_status_t st = check_fwd_args(q, k, v, out, lse, 1, Hq, Hkv, total_q, total_k, d, ATTN_LAYOUT_BSHD, scale);
+    if (st != ATTN_OK) return st;
+    if (B < 1 || max_seqlen_q < 1 || max_seqlen_k < 1 || max_seqlen_q > total_q || max_seqlen_k > total_k)
+        return ATTN_ERR_INVALID_ARG;
+    if (!valid_round_mode(round_mode)) return ATTN_ERR_INVALID_ARG;
+    DeviceInfo *di = nullptr;
+    if ((st = device_info(&di)) != ATTN_OK) return st;
+    attn::PrefillParams p;
+    fill_prefill_params(&p, di, lse, B, Hq, Hkv, max_seqlen_q, max_seqlen_k, ATTN_LAYOUT_BSHD, causal, scale);
+    p.round_mode = round_mode;
+    p.cu_q = cu_seqlens_q;
+    p.cu_k = cu_seqlens_k;
+    p.total_q = total_q;
+    p.total_k = total_k;
+    p.out = out;
+    p.inject = g_inject.exchange(0);
+    const int64_t units = p.pair_heads ? (int64_t)B * Hkv * (p.G / 2) * p.n_m : (int64_t)B * Hq * ((p.n_m + 1) / 2);
+    if (units > 0x7fffffff) return ATTN_ERR_INVALID_ARG;
+    p.n_full_units = (int)units;
+    CUtensorMap mq, mk, mv, mo;
+    if (!make_map_4d(&mq, q, false, 1, total_q, Hq, d, 128) || !make_map_4d(&mk, k, false, 1, total_k, Hkv, d, 128) ||
+        !make_map_4d(&mv, v, false, 1, total_k, Hkv, d, 128) || !make_map_4d(&mo, out, false, 1, total_q, Hq, d, 128))
+        return ATTN_ERR_CUDA;
+    if (attn::launch_prefill(mq, mk, mv, mo, p, (int)units, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return ATTN_ERR_CUDA;
+    return ATTN_OK;
 }
 
 size_t attn_fwd_workspace_bytes(int B, int Hq, int Hkv, int Sq, int Sk, int d, int causal) {

@@ -29,6 +29,7 @@ enum WaitSite : unsigned {
     kSiteDecodeEmpty = 9,
     kSiteSelftest = 10,
     kSiteDecodeTable = 11,
+    kSiteVarlenOffsets = 12,
 };
 
 // First error wins; the site is informative only.

@@ -110,7 +110,26 @@ struct Unit {
     int j_lo;    // first K/V tile (absolute)
     int part;    // key-range part of a split unit, -1 for a whole unit
     int ws_row;  // first workspace row of a split unit (256 rows per unit)
+    int Sq, Sk;  // lengths of this unit's sequence (a packed batch: its own)
+    int q0, k0;  // first row of the sequence in q and in k, v (0 when dense)
+    int tb;      // batch coordinate of the TMA boxes (0 in a packed batch)
 };
+
+// K/V tile count of a unit from its rows and its sequence's lengths: every
+// tile for a non-causal unit; for a causal one, up to the tile holding the
+// last key its lowest row may see (bottom-right alignment).
+__host__ __device__ __forceinline__ void unit_kv_range(const PrefillParams &p, Unit &w) {
+    const int n_full = (w.Sk + BN - 1) / BN;
+    if (p.causal) {
+        int last_row = w.s0[0] + BM - 1;
+        if (w.s0[1] < w.Sq) last_row = last_row > w.s0[1] + BM - 1 ? last_row : w.s0[1] + BM - 1;
+        last_row = last_row < w.Sq - 1 ? last_row : w.Sq - 1;
+        const int lim = last_row + w.Sk - w.Sq;  // last visible key of the lowest row
+        w.n_kv = lim < 0 ? 0 : (n_full < lim / BN + 1 ? n_full : lim / BN + 1);
+    } else {
+        w.n_kv = n_full;
+    }
+}
 
 // Heads, rows and K/V tile count of work unit u (two 128-row Q tiles).
 __host__ __device__ __forceinline__ Unit unit_coords(const PrefillParams &p, int u) {
@@ -141,16 +160,12 @@ __host__ __device__ __forceinline__ Unit unit_coords(const PrefillParams &p, int
         w.s0[0] = mp * 2 * BM;
         w.s0[1] = mp * 2 * BM + BM;
     }
-    const int n_full = (p.Sk + BN - 1) / BN;
-    if (p.causal) {
-        int last_row = w.s0[0] + BM - 1;
-        if (w.s0[1] < p.Sq) last_row = last_row > w.s0[1] + BM - 1 ? last_row : w.s0[1] + BM - 1;
-        last_row = last_row < p.Sq - 1 ? last_row : p.Sq - 1;
-        const int lim = last_row + p.Sk - p.Sq;  // last visible key of the lowest row
-        w.n_kv = lim < 0 ? 0 : (n_full < lim / BN + 1 ? n_full : lim / BN + 1);
-    } else {
-        w.n_kv = n_full;
-    }
+    w.Sq = p.Sq;
+    w.Sk = p.Sk;
+    w.q0 = 0;
+    w.k0 = 0;
+    w.tb = w.b;
+    unit_kv_range(p, w);
     w.j_lo = 0;
     w.part = -1;
     w.ws_row = 0;
@@ -160,6 +175,24 @@ __host__ __device__ __forceinline__ Unit unit_coords(const PrefillParams &p, int
 // The unit (and key range) CTA number cta works on.  CTAs past the whole
 // units are the parts of the tail units, part-major within a unit.
 __device__ __forceinline__ Unit decode_unit(const PrefillParams &p, int cta) {
+    if (p.cu_q != nullptr) {
+        // Packed batch: the unit's rows and keys are those of sequence w.b.
+        // Offsets that are out of order or out of range, or lengths past the
+        // stated maxima, are reported and the unit does nothing.
+        Unit w = unit_coords(p, cta);
+        const int q0 = p.cu_q[w.b], q1 = p.cu_q[w.b + 1];
+        const int k0 = p.cu_k[w.b], k1 = p.cu_k[w.b + 1];
+        const bool bad = q0 < 0 || q1 < q0 || q1 > p.total_q || k0 < 0 || k1 < k0 || k1 > p.total_k ||
+                         q1 - q0 > p.Sq || k1 - k0 > p.Sk;
+        if (bad && threadIdx.x == 0) report_status(p.status, kStatusDeviceBounds, kSiteVarlenOffsets);
+        w.Sq = bad ? 0 : q1 - q0;
+        w.Sk = bad ? 0 : k1 - k0;
+        w.q0 = bad ? 0 : q0;
+        w.k0 = bad ? 0 : k0;
+        w.tb = 0;
+        unit_kv_range(p, w);
+        return w;
+    }
     if (cta < p.n_full_units) return unit_coords(p, cta);
     const int v = cta - p.n_full_units;
     const int su = v / p.split_parts;
@@ -194,8 +227,8 @@ __device__ void producer(const PrefillParams &p, const Unit &w, const SmemLayout
     const uint64_t pol_q = ptx::policy_evict_first();
     const uint64_t pol_kv = ptx::policy_evict_last();
     ptx::mbar_arrive_expect_tx(sm.q_full(), 2 * TILE_BYTES);
-    load_tile(mq, sm.q_tile(0), sm.q_full(), p.bhsd, w.h[0], w.s0[0], w.b, pol_q);
-    load_tile(mq, sm.q_tile(1), sm.q_full(), p.bhsd, w.h[1], w.s0[1], w.b, pol_q);
+    load_tile(mq, sm.q_tile(0), sm.q_full(), p.bhsd, w.h[0], w.q0 + w.s0[0], w.tb, pol_q);
+    load_tile(mq, sm.q_tile(1), sm.q_full(), p.bhsd, w.h[1], w.q0 + w.s0[1], w.tb, pol_q);
     const int total = 2 * w.n_kv;
     int issued = 0;
     for (int n = 0; n < total; ++n) {
@@ -203,8 +236,8 @@ __device__ void producer(const PrefillParams &p, const Unit &w, const SmemLayout
         const int round = n / NSLOT;
         if (round > 0 && !wait_bounded(sm.kv_empty(slot), (round - 1) & 1, wc, kSiteProducerEmpty)) break;
         ptx::mbar_arrive_expect_tx(sm.kv_full(slot), TILE_BYTES);
-        load_tile((n & 1) ? mv : mk, sm.slot(slot), sm.kv_full(slot), p.bhsd, w.g, (w.j_lo + (n >> 1)) * BN, w.b,
-                  pol_kv);
+        load_tile((n & 1) ? mv : mk, sm.slot(slot), sm.kv_full(slot), p.bhsd, w.g, w.k0 + (w.j_lo + (n >> 1)) * BN,
+                  w.tb, pol_kv);
         ++issued;
     }
     // On the way out make sure no copy is still writing into shared memory.
@@ -348,9 +381,11 @@ __device__ void softmax_wg(const PrefillParams &p, const Unit &w, const SmemLayo
     const uint32_t tS = lanes + TM_S;     // shared score buffer
     const uint32_t tP = lanes + tm_p(t);  // this tile's bf16 P
     const uint32_t tO = lanes + tm_o(t);  // this tile's O accumulator
-    const int s0 = w.s0[t];
-    const int lim_row = p.causal ? min(s0 + r + p.Sk - p.Sq, p.Sk - 1) : p.Sk - 1;
-    const int lim_tile = p.causal ? min(s0 + p.Sk - p.Sq, p.Sk - 1) : p.Sk - 1;
+    // Selects, not a runtime index: an indexed Unit array would live in local memory.
+    const int s0 = t ? w.s0[1] : w.s0[0];
+    const int head = t ? w.h[1] : w.h[0];
+    const int lim_row = p.causal ? min(s0 + r + w.Sk - w.Sq, w.Sk - 1) : w.Sk - 1;
+    const int lim_tile = p.causal ? min(s0 + w.Sk - w.Sq, w.Sk - 1) : w.Sk - 1;
     const float sl2 = p.scale_log2;
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
@@ -504,16 +539,30 @@ __device__ void softmax_wg(const PrefillParams &p, const Unit &w, const SmemLayo
             }
         }
         const int srow = s0 + r;
-        if (p.lse != nullptr && srow < p.Sq) {
+        if (p.lse != nullptr && srow < w.Sq) {
             const float lse = l_run > 0.f ? (m_run + ptx::lg2(l_run)) * LN2 : -INFINITY;
-            p.lse[((int64_t)w.b * p.Hq + w.h[t]) * p.Sq + srow] = lse;
+            const int64_t li = p.cu_q != nullptr ? (int64_t)head * p.total_q + w.q0 + srow
+                                                 : ((int64_t)w.b * p.Hq + head) * p.Sq + srow;
+            p.lse[li] = lse;
         }
     }
     ptx::fence_proxy_async_smem();
     ptx::named_bar_sync(1 + t, 128);
-    if (quarter == 0 && lane == 0 && s0 < p.Sq && w.part < 0 && !*wc.abort_flag) {
-        const Coord4 lo = coord4(p.bhsd, 0, w.h[t], s0, w.b);
-        const Coord4 hi = coord4(p.bhsd, 64, w.h[t], s0, w.b);
+    if (p.cu_q != nullptr && s0 + BM > w.Sq) {
+        // Last row block of a packed sequence: a full box would spill into the
+        // next sequence's rows, so each thread stores its own row (if valid)
+        // from the swizzled staging tile.
+        if (s0 + r < w.Sq && !*wc.abort_flag) {
+            uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.out) +
+                                                   ((int64_t)(w.q0 + s0 + r) * p.Hq + head) * D);
+#pragma unroll
+            for (int c = 0; c < 16; ++c)
+                dst[c] = *reinterpret_cast<const uint4 *>(stage + (c >> 3) * HALF_BYTES + r * 128 +
+                                                           (((c & 7) ^ (r & 7)) << 4));
+        }
+    } else if (quarter == 0 && lane == 0 && s0 < w.Sq && w.part < 0 && !*wc.abort_flag) {
+        const Coord4 lo = coord4(p.bhsd, 0, head, w.q0 + s0, w.tb);
+        const Coord4 hi = coord4(p.bhsd, 64, head, w.q0 + s0, w.tb);
         ptx::tma_store_4d(mo, stage, lo.c0, lo.c1, lo.c2, lo.c3);
         ptx::tma_store_4d(mo, stage + HALF_BYTES, hi.c0, hi.c1, hi.c2, hi.c3);
         ptx::bulk_commit_group();
@@ -536,6 +585,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const Unit w = decode_unit(p, blockIdx.x);
+    // A unit whose rows all lie past its sequence's end (packed batches, whose
+    // grid is sized by the longest sequence) has nothing to do.
+    if (w.s0[0] >= w.Sq) return;
 
     if (threadIdx.x == 0) {
         ptx::mbar_init(sm.q_full(), 1);
@@ -662,9 +714,9 @@ __global__ void __launch_bounds__(D) merge_kernel(__nv_bfloat16 *__restrict__ ou
     const int t = (row / BM) & 1;
     const int r = row % BM;
     const Unit w = unit_coords(p, p.n_full_units + su);
-    const int s = w.s0[t] + r;
+    const int s = (t ? w.s0[1] : w.s0[0]) + r;
     if (s >= p.Sq) return;
-    const int h = w.h[t];
+    const int h = t ? w.h[1] : w.h[0];
     const int e = threadIdx.x;
     const float *ls = p.ws_lse + (int64_t)row * p.split_parts;
     float M = -INFINITY;

@@ -8,7 +8,7 @@
 namespace attn {
 
 struct PrefillParams {
-    int B, Hq, Hkv, Sq, Sk;
+    int B, Hq, Hkv, Sq, Sk;  // a packed batch: Sq, Sk = the largest sequence lengths
     int G;             // Hq / Hkv
     int causal;        // bottom-right causal mask
     int bhsd;          // 1: tensors are [B][H][S][d]; 0: [B][S][H][d]
@@ -29,6 +29,14 @@ struct PrefillParams {
     int split_parts;
     float *ws_o;
     float *ws_lse;
+    // Packed variable-length batch (cu_q == nullptr for a dense batch):
+    // sequence b owns rows cu_q[b] .. cu_q[b+1]-1 of q [total_q][Hq][d] and
+    // cu_k[b] .. cu_k[b+1]-1 of k, v [total_k][Hkv][d]; lse is [Hq][total_q].
+    // Partial last row blocks are stored row by row through out.
+    const int *cu_q;
+    const int *cu_k;
+    int total_q, total_k;
+    void *out;
 };
 
 int prefill_smem_bytes();

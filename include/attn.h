@@ -113,6 +113,37 @@ attn_status_t attn_fwd_rounded(const void *q, const void *k, const void *v, void
                                int layout, int causal, float scale, int round_mode, void *stream);
 
 /*
+ * attn_fwd_varlen -- attn_fwd over a packed batch of variable-length
+ * sequences (the "variable-length batches" the MoonMath HIP kernel page lists
+ * among its kernel's limitations; here they are supported).
+ *
+ * q:   bf16 [total_q][Hq][d], the B sequences' query rows back to back.
+ * k,v: bf16 [total_k][Hkv][d], the sequences' key/value rows back to back.
+ * cu_seqlens_q, cu_seqlens_k: DEVICE int32 [B+1]; sequence b owns rows
+ *      cu_seqlens_q[b] .. cu_seqlens_q[b+1]-1 of q and out, and rows
+ *      cu_seqlens_k[b] .. cu_seqlens_k[b+1]-1 of k and v.  Offsets must be
+ *      non-decreasing and within [0, total]; lengths may be 0.
+ * max_seqlen_q, max_seqlen_k: upper bounds of the sequences' lengths (the
+ *      grid is sized by max_seqlen_q); 1 <= max_seqlen <= total.
+ * out: bf16 [total_q][Hq][d] (written for the rows of every sequence; rows
+ *      that belong to no sequence are not touched).
+ * lse: fp32 [Hq][total_q] (same rows written), or NULL.
+ * Each sequence is exactly attn_fwd with B = 1, Sq and Sk its own lengths:
+ * its rows see only its own keys, and causal != 0 applies the bottom-right
+ * causal mask within the sequence.  A sequence with queries and no keys gets
+ * O = 0 and lse = -inf.  d must be 128; Hq a multiple of Hkv; round_mode as
+ * in attn_fwd_rounded.  The offsets live on the device and are not read on
+ * the host: a kernel that finds them out of order, out of range or past the
+ * stated maxima records ATTN_ERR_DEVICE_BOUNDS in the device status word and
+ * leaves that sequence's rows untouched.  No tail split; deterministic.
+ */
+attn_status_t attn_fwd_varlen(const void *q, const void *k, const void *v, void *out, float *lse,
+                              const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,
+                              int B, int Hq, int Hkv, int total_q, int total_k,
+                              int max_seqlen_q, int max_seqlen_k, int d,
+                              int causal, float scale, int round_mode, void *stream);
+
+/*
  * attn_fwd_workspace_bytes -- device workspace that lets attn_fwd split the
  * key ranges of its last wave of work units (the Flash-Decoding style tail
  * split of the MoonMath page: the partial results are merged by log-sum-exp)

@@ -133,3 +133,21 @@ def test_fwd_workspace_query_and_registration_validate(lib):
     assert lib.attn_fwd_workspace_bytes(1, 3, 2, 8, 8, 128, 0) == 0
     assert lib.attn_fwd_workspace_bytes(1, 2, 2, 8, 8, 64, 0) == 0
     assert lib.attn_set_workspace(264, 1024) == 1     # not 256-byte aligned
+
+
+def _varlen(lib, **kw):
+    a = dict(q=16, k=16, v=16, out=16, lse=None, cq=64, ck=64, B=2, Hq=4, Hkv=2, tq=100, tk=100, mq=60, mk=60,
+             d=128, causal=0, scale=0.1, mode=0)
+    a.update(kw)
+    return lib.attn_fwd_varlen(a["q"], a["k"], a["v"], a["out"], a["lse"], a["cq"], a["ck"], a["B"], a["Hq"],
+                               a["Hkv"], a["tq"], a["tk"], a["mq"], a["mk"], a["d"], a["causal"], a["scale"],
+                               a["mode"], None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(cq=None), 1), (dict(ck=None), 1), (dict(cq=66), 1), (dict(q=24), 1), (dict(B=0), 1),
+    (dict(tq=0), 1), (dict(tk=0), 1), (dict(mq=0), 1), (dict(mq=101), 1), (dict(mk=101), 1),
+    (dict(Hq=3), 1), (dict(d=64), 2), (dict(mode=5), 1), (dict(scale=float("nan")), 1),
+])
+def test_fwd_varlen_rejects_bad_arguments_before_any_launch(lib, kw, code):
+    assert _varlen(lib, **kw) == code
