@@ -209,6 +209,80 @@ def make_decode(w: DecodeWorkload, seqlens=None):
     return q, k_pages, v_pages, table, lens.to(torch.int32)
 
 
+@dataclasses.dataclass(frozen=True)
+class PagedPrefillWorkload:
+    """Chunked prefill against a paged KV cache: sequence b has a cache of
+    Lk = context + chunk tokens (the chunk's own keys already appended) in
+    16-token pages, and a packed query chunk of its last `chunk` tokens."""
+    name: str
+    B: int
+    Hq: int
+    Hkv: int
+    chunk_lo: int = 1
+    chunk_hi: int = 1
+    ctx_lo: int = 0
+    ctx_hi: int = 0
+    causal: bool = True
+    seed: int = 0
+    d: int = 128
+    page_size: int = 16
+    max_blocks: int = 512
+    chunks: tuple = None     # explicit chunk lengths (overrides the draw)
+    contexts: tuple = None   # explicit context lengths (overrides the draw)
+
+    @property
+    def scale(self) -> float:
+        return float(torch.tensor(1.0 / math.sqrt(self.d), dtype=torch.float32).item())
+
+    def lengths(self):
+        """(chunk lengths Lq, cache lengths Lk) per sequence."""
+        gen = torch.Generator().manual_seed(self.seed)
+        lq = torch.randint(self.chunk_lo, self.chunk_hi + 1, (self.B,), generator=gen).tolist()
+        ctx = torch.randint(self.ctx_lo, self.ctx_hi + 1, (self.B,), generator=gen).tolist()
+        if self.chunks is not None:
+            lq = list(self.chunks)
+        if self.contexts is not None:
+            ctx = list(self.contexts)
+        return lq, [a + c for a, c in zip(lq, ctx)]
+
+    @property
+    def flops(self) -> float:
+        """4 * Hq * d per visible (query, key) pair; causal counts Lq*(Lk-Lq) + Lq^2/2 pairs."""
+        lq, lk = self.lengths()
+        pairs = sum((a * (b - a) + a * a / 2) if self.causal else a * b for a, b in zip(lq, lk))
+        return 4.0 * self.Hq * self.d * pairs
+
+
+def make_paged_prefill(w: PagedPrefillWorkload):
+    """(q [total_q, Hq, d], k_pages, v_pages [P, page, Hkv, d], block_table [B, max_blocks] int32 (-1 padded),
+    seqlens_k [B] int32, cu_q [B+1] int32), CPU tensors.  Physical page ids are a seeded permutation."""
+    lq, lk = w.lengths()
+    if max(lk) > w.page_size * w.max_blocks:
+        raise ValueError("a sequence is longer than the block table allows")
+    gen = torch.Generator().manual_seed(w.seed + 2000)
+    npages = [(L + w.page_size - 1) // w.page_size for L in lk]
+    total = max(1, sum(npages))
+    perm = torch.randperm(total, generator=gen).to(torch.int32)
+    table = torch.full((w.B, w.max_blocks), -1, dtype=torch.int32)
+    off = 0
+    for b, n in enumerate(npages):
+        table[b, :n] = perm[off:off + n]
+        off += n
+    cu_q = torch.zeros(w.B + 1, dtype=torch.int32)
+    cu_q[1:] = torch.cumsum(torch.tensor(lq, dtype=torch.int64), 0).to(torch.int32)
+    q = _randn_bf16((max(1, int(cu_q[-1])), w.Hq, w.d), gen)
+    k_pages = _randn_bf16((total, w.page_size, w.Hkv, w.d), gen)
+    v_pages = _randn_bf16((total, w.page_size, w.Hkv, w.d), gen)
+    return q, k_pages, v_pages, table, torch.tensor(lk, dtype=torch.int32), cu_q
+
+
 def decode_kv_bytes(seqlens, Hkv: int, d: int) -> int:
     """Algorithmic K+V bytes one decode pass must read: 2 tensors * 2 B * Hkv * d per token."""
     return int(sum(int(L) for L in seqlens)) * Hkv * d * 2 * 2
+
+
+# Chunked prefill of 16 GQA sequences against a paged cache: chunks of
+# U[256, 2048] new tokens on contexts of U[0, 6144] cached tokens, causal.
+PAGED_PREFILL = PagedPrefillWorkload("paged_prefill_16seq_32q8kv", 16, 32, 8, chunk_lo=256, chunk_hi=2048,
+                                     ctx_lo=0, ctx_hi=6144, seed=7)
+PAGED_PREFILL_WORKLOADS = {PAGED_PREFILL.name: PAGED_PREFILL}

@@ -180,6 +180,50 @@ def attention_varlen(q, k, v, cu_q, cu_k, *, Hq, Hkv, d=128, causal=False, scale
     return out, lse
 
 
+def gather_pages(pages, block_table_row, L, page_size=16):
+    """The first L tokens of one sequence out of a page pool [num_pages, page_size, H, d]:
+    token t lives in slot t % page_size of page block_table_row[t // page_size].
+    Returns [L, H, d] in the pool's dtype; raises if a needed table entry is out of range."""
+    idx = np.arange(L)
+    phys = np.asarray(block_table_row, dtype=np.int64)[idx // page_size]
+    if L and (phys.min() < 0 or phys.max() >= pages.shape[0]):
+        raise ValueError("block table entry outside the page pool")
+    return pages[phys, idx % page_size]
+
+
+def attention_paged(q, k_pages, v_pages, block_table, seqlens_k, cu_q, *, Hq, Hkv, d=128, causal=False, scale,
+                    page_size=16, seqs=None):
+    """Prefill of packed query chunks against a paged KV cache.
+
+    Sequence b has seqlens_k[b] cached keys, key t at slot t % 16 of page
+    block_table[b][t // 16] of the pools, and query rows cu_q[b] .. cu_q[b+1]-1
+    of q [total_q, Hq, d]; causal alignment is bottom-right (the chunk is the
+    cache's last tokens).  Each sequence is gathered into contiguous K, V and
+    run through the plain attention above.  Returns (out [total_q, Hq, d],
+    lse [Hq, total_q]) in float64, NaN for rows of no sequence."""
+    cu_q = [int(x) for x in cu_q]
+    lens = [int(x) for x in seqlens_k]
+    bt = np.asarray(block_table)
+    total_q = q.shape[0]
+    out = np.full((total_q, Hq, d), np.nan)
+    lse = np.full((Hq, total_q), np.nan)
+    for b in (range(len(lens)) if seqs is None else seqs):
+        q0, q1, Lk = cu_q[b], cu_q[b + 1], lens[b]
+        if q1 == q0:
+            continue
+        if Lk == 0:
+            out[q0:q1] = 0.0
+            lse[:, q0:q1] = -np.inf
+            continue
+        k_b = gather_pages(k_pages, bt[b], Lk, page_size)
+        v_b = gather_pages(v_pages, bt[b], Lk, page_size)
+        o_b, l_b = attention(q[q0:q1][None], k_b[None], v_b[None], B=1, Hq=Hq, Hkv=Hkv, Sq=q1 - q0, Sk=Lk, d=d,
+                             causal=causal, scale=scale)
+        out[q0:q1] = o_b[0]
+        lse[:, q0:q1] = l_b[0]
+    return out, lse
+
+
 def attention_rows(q, k, v, rows, *, B, Hq, Hkv, Sq, Sk, d=128, layout="bshd", causal=False,
                    scale, key_range=None):
     """Selected rows (an [n, 3] array of (b, h, i)), optionally over keys [lo, hi).

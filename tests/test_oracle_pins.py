@@ -141,6 +141,60 @@ def test_varlen_equal_lengths_is_the_dense_batch():
     np.testing.assert_array_equal(vl, dense_l.transpose(1, 0, 2).reshape(Hq, B * L))
 
 
+# ---------------------------------------------------------------- prefill against a paged cache
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_paged_prefill_of_one_token_is_decode(causal):
+    # a chunk of one query per sequence sees its whole cache either way: it is
+    # the decode step, which the C oracle gathers from the pages on its own
+    w = inputs.PagedPrefillWorkload("p", 5, 4, 2, chunks=(1,) * 5, contexts=(0, 15, 16, 40, 100), seed=15,
+                                    max_blocks=8, d=32)
+    q, kp, vp, table, lens, cu_q = inputs.make_paged_prefill(w)
+    out, lse = oracle.attention_paged(q, kp, vp, table, lens, cu_q, Hq=4, Hkv=2, d=32, causal=causal, scale=0.2)
+    ref_o, ref_l = oracle.decode_paged(q, kp, vp, table, lens, scale=0.2)
+    np.testing.assert_allclose(out, ref_o, rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(lse.T, ref_l, rtol=1e-12, atol=1e-13)
+
+
+def test_paged_prefill_equals_attention_on_the_scattered_cache():
+    # scatter contiguous K, V into pages through a shuffled table; the paged
+    # prefill must equal plain attention on the contiguous tensors
+    d, Hq, Hkv, ps = 16, 4, 2, 16
+    lq, lk = (7, 20, 1), (30, 20, 17)
+    g = torch.Generator().manual_seed(16)
+    npages = [(L + ps - 1) // ps for L in lk]
+    perm = torch.randperm(sum(npages) + 3, generator=g)          # three unused pages
+    kp = torch.randn(sum(npages) + 3, ps, Hkv, d, generator=g).to(torch.bfloat16)
+    vp = torch.randn(sum(npages) + 3, ps, Hkv, d, generator=g).to(torch.bfloat16)
+    table = torch.full((3, 4), -1, dtype=torch.int32)
+    ks, vs, off = [], [], 0
+    for b, L in enumerate(lk):
+        k_b = torch.randn(L, Hkv, d, generator=g).to(torch.bfloat16)
+        v_b = torch.randn(L, Hkv, d, generator=g).to(torch.bfloat16)
+        for t in range(L):
+            page = int(perm[off + t // ps])
+            table[b, t // ps] = page
+            kp[page, t % ps] = k_b[t]
+            vp[page, t % ps] = v_b[t]
+        off += npages[b]
+        ks.append(k_b)
+        vs.append(v_b)
+    q = torch.randn(sum(lq), Hq, d, generator=g).to(torch.bfloat16)
+    cu_q = torch.tensor([0, 7, 27, 28], dtype=torch.int32)
+    out, lse = oracle.attention_paged(q, kp, vp, table, torch.tensor(lk), cu_q, Hq=Hq, Hkv=Hkv, d=d, causal=True,
+                                      scale=0.3)
+    for b in range(3):
+        q0 = int(cu_q[b])
+        ref = _sdpa_reference(q[q0:q0 + lq[b]][None], ks[b][None], vs[b][None], True, 0.3)[0]
+        np.testing.assert_allclose(out[q0:q0 + lq[b]], ref, rtol=1e-10, atol=1e-12)
+
+
+def test_paged_gather_rejects_a_bad_table_entry():
+    kp = torch.zeros(2, 16, 1, 8, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        oracle.gather_pages(kp, [0, 5], 20)
+
+
 # ---------------------------------------------------------------- closed forms
 
 def test_identical_keys_give_mean_of_v():
