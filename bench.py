@@ -221,7 +221,36 @@ class VarlenCase:
         return _oracle_sample_varlen(self, seconds, seed)
 
 
+class PagedCase(VarlenCase):
+    """Chunked prefill against a paged KV cache (attn_fwd_paged)."""
+
+    def __init__(self, w):
+        self.w = w
+        self.name = w.name
+        self.flops = w.flops
+        self.host = inputs.make_paged_prefill(w)
+        self.lq, self.lk = w.lengths()
+        total_q = self.host[0].shape[0]
+        self.lse_shape = (w.Hq, total_q)
+        self.config = {"B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "total_q": total_q,
+                       "chunks": f"U[{w.chunk_lo},{w.chunk_hi}]", "contexts": f"U[{w.ctx_lo},{w.ctx_hi}]",
+                       "seed": w.seed, "cache_tokens": sum(self.lk), "page_size": w.page_size, "d": w.d,
+                       "layout": "thd chunks, paged cache", "causal": w.causal}
+        self.flop_note = "4*Hq*d per visible pair; causal pairs Lq*(Lk-Lq) + Lq^2/2 per sequence"
+        self.api = "exact_attention_forward_06_gb300.fwd_paged (C ABI attn_fwd_paged)"
+
+    def call(self, A, dev_in, out, lse, stream):
+        q, kp, vp, table, lens, cu_q = dev_in
+        A.fwd_paged(q, kp, vp, table, lens, cu_q, max_seqlen_q=max(self.lq), causal=self.w.causal,
+                    scale=self.w.scale, out=out, lse=lse, stream=stream)
+
+    def oracle_sample(self, seconds, seed):
+        return _oracle_sample_paged(self, seconds, seed)
+
+
 def make_case(name):
+    if name in inputs.PAGED_PREFILL_WORKLOADS:
+        return PagedCase(inputs.PAGED_PREFILL_WORKLOADS[name])
     if name in inputs.VARLEN_WORKLOADS:
         return VarlenCase(inputs.VARLEN_WORKLOADS[name])
     return DenseCase(inputs.PREFILL_WORKLOADS[name])
@@ -461,6 +490,46 @@ def _oracle_sample_varlen(case, seconds, seed):
     return flops, time.perf_counter() - t0, n
 
 
+def _oracle_sample_paged(case, seconds, seed):
+    """Uniformly drawn (sequence, head, chunk row) triples, each through the
+    oracle over its sequence's keys gathered from the pages."""
+    import numpy as np
+    import oracle
+    w = case.w
+    q_h, kp, vp, table, lens, cu_q = case.host
+    rng = np.random.default_rng(seed)
+    weights = np.array(case.lq, dtype=np.float64) / sum(case.lq)
+    gathered = {}
+
+    def run(n):
+        seqs = rng.choice(w.B, size=n, p=weights)
+        flops = 0
+        for b in np.unique(seqs):
+            m = int((seqs == b).sum())
+            Lq, Lk = case.lq[b], case.lk[b]
+            q0 = int(cu_q[b])
+            if b not in gathered:
+                gathered[b] = (oracle.gather_pages(kp, table[b], Lk), oracle.gather_pages(vp, table[b], Lk))
+            k_b, v_b = gathered[b]
+            rows = np.stack([np.zeros(m, np.int64), rng.integers(0, w.Hq, m), rng.integers(0, Lq, m)], 1)
+            oracle.attention_rows(q_h[q0:q0 + Lq][None], k_b[None], v_b[None], rows, B=1, Hq=w.Hq, Hkv=w.Hkv,
+                                  Sq=Lq, Sk=Lk, d=w.d, causal=w.causal, scale=w.scale)
+            for i in rows[:, 2]:
+                nk = min(Lk, int(i) + 1 + Lk - Lq) if w.causal else Lk
+                flops += 4 * w.d * max(0, nk)
+        return flops
+
+    probe_n = max(8, oracle.num_threads())
+    run(probe_n)                       # gathers every drawn sequence once
+    t0 = time.perf_counter()
+    run(probe_n)
+    dt = time.perf_counter() - t0
+    n = max(probe_n, int(probe_n * seconds / max(dt, 1e-3)))
+    t0 = time.perf_counter()
+    flops = run(n)
+    return flops, time.perf_counter() - t0, n
+
+
 def cpu_baseline(case, seconds):
     import oracle
     flops, dt, n = case.oracle_sample(seconds, seed=1)
@@ -512,7 +581,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=inputs.GQA_CAUSAL.name,
-                    choices=sorted(inputs.PREFILL_WORKLOADS) + sorted(inputs.VARLEN_WORKLOADS))
+                    choices=sorted(inputs.PREFILL_WORKLOADS) + sorted(inputs.VARLEN_WORKLOADS) +
+                    sorted(inputs.PAGED_PREFILL_WORKLOADS))
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)

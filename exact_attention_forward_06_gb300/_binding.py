@@ -54,6 +54,8 @@ def load():
             lib.attn_fwd_rounded.argtypes = fwd_args[:-1] + [_i, _p]
             lib.attn_fwd_varlen.argtypes = [_p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _i, _i, _f,
                                             _i, _p]
+            lib.attn_fwd_paged.argtypes = [_p, _p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _i, _i, _i,
+                                           _f, _i, _p]
             lib.attn_fwd_workspace_bytes.argtypes = [_i, _i, _i, _i, _i, _i, _i]
             lib.attn_fwd_workspace_bytes.restype = _sz
             lib.attn_set_workspace.argtypes = [_p, _sz]
@@ -73,7 +75,8 @@ def load():
             lib.attn_status_string.argtypes = [_i]
             lib.attn_status_string.restype = ctypes.c_char_p
             lib.attn_version.restype = _i
-            for name in ("attn_fwd", "attn_fwd_simple", "attn_fwd_rounded", "attn_fwd_varlen", "attn_decode_paged",
+            for name in ("attn_fwd", "attn_fwd_simple", "attn_fwd_rounded", "attn_fwd_varlen", "attn_fwd_paged",
+                         "attn_decode_paged",
                          "attn_lse_merge",
                          "attn_get_device_status", "attn_set_wait_budget_ns", "attn_debug_inject",
                          "attn_selftest_umma"):
@@ -201,6 +204,48 @@ def fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, *, max_seqlen_q=None, max_se
                              int(max_seqlen_q), int(max_seqlen_k), d, int(bool(causal)), float(scale),
                              ROUNDING[rounding], _stream(stream))
     _check(rc, "attn_fwd_varlen")
+    return out, (None if lse is False else lse)
+
+
+def fwd_paged(q, k_pages, v_pages, block_table, seqlens_k, cu_seqlens_q, *, max_seqlen_q=None, causal=True,
+              scale=None, out=None, lse=None, stream=None, rounding="rtne"):
+    """Prefill of packed query chunks against a paged KV cache (chunked prefill).
+
+    q [total_q, Hq, d] bf16; k_pages, v_pages [num_pages, 16, Hkv, d] bf16; block_table [B, max_blocks]
+    int32; seqlens_k [B] int32 (cache lengths, chunk included); cu_seqlens_q [B+1] int32 -- all on the
+    device.  Returns (out [total_q, Hq, d] bf16, lse [Hq, total_q] fp32).  max_seqlen_q, when omitted,
+    is read from the offsets (a synchronisation).
+    """
+    lib = load()
+    for t, n in ((q, "q"), (k_pages, "k_pages"), (v_pages, "v_pages")):
+        _dev_tensor(t, n, torch.bfloat16)
+    for t, n in ((block_table, "block_table"), (seqlens_k, "seqlens_k"), (cu_seqlens_q, "cu_seqlens_q")):
+        _dev_tensor(t, n, torch.int32)
+    if rounding not in ROUNDING:
+        raise ValueError(f"rounding must be one of {sorted(ROUNDING)}, got {rounding!r}")
+    if q.dim() != 3 or k_pages.dim() != 4 or k_pages.shape != v_pages.shape:
+        raise ValueError("q must be [total_q, Hq, d] and the pools [num_pages, 16, Hkv, d]")
+    total_q, Hq, d = q.shape
+    num_pages, page_size, Hkv, _ = k_pages.shape
+    B = seqlens_k.numel()
+    if cu_seqlens_q.numel() != B + 1 or block_table.dim() != 2 or block_table.shape[0] != B:
+        raise ValueError("cu_seqlens_q must have B + 1 entries and block_table B rows")
+    if max_seqlen_q is None:
+        max_seqlen_q = max(1, int(torch.diff(cu_seqlens_q).max()))
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((Hq, total_q), device=q.device, dtype=torch.float32)
+    elif lse is not False:
+        _dev_tensor(lse, "lse", torch.float32)
+    lse_ptr = None if lse is False else lse.data_ptr()
+    rc = lib.attn_fwd_paged(q.data_ptr(), k_pages.data_ptr(), v_pages.data_ptr(), block_table.data_ptr(),
+                            seqlens_k.data_ptr(), cu_seqlens_q.data_ptr(), out.data_ptr(), lse_ptr, B, Hq, Hkv,
+                            total_q, int(max_seqlen_q), d, page_size, num_pages, block_table.shape[1],
+                            int(bool(causal)), float(scale), ROUNDING[rounding], _stream(stream))
+    _check(rc, "attn_fwd_paged")
     return out, (None if lse is False else lse)
 
 

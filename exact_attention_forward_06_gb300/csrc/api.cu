@@ -119,6 +119,21 @@ bool make_map_pool(CUtensorMap *m, const void *ptr, int num_pages, int Hkv, int 
     return r == CUDA_SUCCESS;
 }
 
+// 3-D map over a page pool [P][16][Hkv][d] for the tensor-core prefill:
+// dims {d, Hkv, 16P}, box = 64 head-dim elements (128 B, 128-byte swizzle) x
+// one page of one KV head (16 rows).
+bool make_map_pool_sw128(CUtensorMap *m, const void *ptr, int num_pages, int Hkv, int d) {
+    const cuuint64_t e = 2;
+    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)Hkv, (cuuint64_t)num_pages * 16};
+    cuuint64_t strides[2] = {(cuuint64_t)d * e, (cuuint64_t)Hkv * d * e};
+    cuuint32_t box[3] = {64, 1, 16};
+    const cuuint32_t es[3] = {1, 1, 1};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box, es,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 attn_status_t check_fwd_args(const void *q, const void *k, const void *v, const void *out, const float *lse,
                              int B, int Hq, int Hkv, int Sq, int Sk, int d, int layout, float scale) {
     if (!q || !k || !v || !out) return ATTN_ERR_INVALID_ARG;
@@ -165,6 +180,10 @@ attn_status_t fill_prefill_params(attn::PrefillParams *p, const DeviceInfo *di, 
     p->total_q = 0;
     p->total_k = 0;
     p->out = nullptr;
+    p->block_table = nullptr;
+    p->seqlens_k = nullptr;
+    p->max_blocks = 0;
+    p->num_pages = 0;
     return ATTN_OK;
 }
 
@@ -251,6 +270,50 @@ attn_status_t attn_fwd_varlen(const void *q, const void *k, const void *v, void 
     CUtensorMap mq, mk, mv, mo;
     if (!make_map_4d(&mq, q, false, 1, total_q, Hq, d, 128) || !make_map_4d(&mk, k, false, 1, total_k, Hkv, d, 128) ||
         !make_map_4d(&mv, v, false, 1, total_k, Hkv, d, 128) || !make_map_4d(&mo, out, false, 1, total_q, Hq, d, 128))
+        return ATTN_ERR_CUDA;
+    if (attn::launch_prefill(mq, mk, mv, mo, p, (int)units, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return ATTN_ERR_CUDA;
+    return ATTN_OK;
+}
+
+attn_status_t attn_fwd_paged(const void *q, const void *k_pages, const void *v_pages, const int32_t *block_table,
+                             const int32_t *seqlens_k, const int32_t *cu_seqlens_q, void *out, float *lse, int B,
+                             int Hq, int Hkv, int total_q, int max_seqlen_q, int d, int page_size, int num_pages,
+                             int max_blocks_per_seq, int causal, float scale, int round_mode, void *stream) {
+    if (!block_table || !seqlens_k || !cu_seqlens_q) return ATTN_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(block_table) & 3u) || (reinterpret_cast<uintptr_t>(seqlens_k) & 3u) ||
+        (reinterpret_cast<uintptr_t>(cu_seqlens_q) & 3u))
+        return ATTN_ERR_INVALID_ARG;
+    if (num_pages < 1 || max_blocks_per_seq < 1 || (int64_t)num_pages * 16 > 0x7fffffff ||
+        (int64_t)max_blocks_per_seq * 16 > 0x7fffffff)
+        return ATTN_ERR_INVALID_ARG;
+    // q, out: one dense [1][total_q][Hq][d] batch; the pools as [1][16P][Hkv][d].
+    attn_status_t st = check_fwd_args(q, k_pages, v_pages, out, lse, 1, Hq, Hkv, total_q, num_pages * 16, d,
+                                      ATTN_LAYOUT_BSHD, scale);
+    if (st != ATTN_OK) return st;
+    if (page_size != 16) return ATTN_ERR_UNSUPPORTED;
+    if (B < 1 || max_seqlen_q < 1 || max_seqlen_q > total_q) return ATTN_ERR_INVALID_ARG;
+    if (!valid_round_mode(round_mode)) return ATTN_ERR_INVALID_ARG;
+    DeviceInfo *di = nullptr;
+    if ((st = device_info(&di)) != ATTN_OK) return st;
+    attn::PrefillParams p;
+    fill_prefill_params(&p, di, lse, B, Hq, Hkv, max_seqlen_q, max_blocks_per_seq * 16, ATTN_LAYOUT_BSHD, causal,
+                        scale);
+    p.round_mode = round_mode;
+    p.cu_q = cu_seqlens_q;
+    p.total_q = total_q;
+    p.out = out;
+    p.block_table = block_table;
+    p.seqlens_k = seqlens_k;
+    p.max_blocks = max_blocks_per_seq;
+    p.num_pages = num_pages;
+    p.inject = g_inject.exchange(0);
+    const int64_t units = p.pair_heads ? (int64_t)B * Hkv * (p.G / 2) * p.n_m : (int64_t)B * Hq * ((p.n_m + 1) / 2);
+    if (units > 0x7fffffff) return ATTN_ERR_INVALID_ARG;
+    p.n_full_units = (int)units;
+    CUtensorMap mq, mk, mv, mo;
+    if (!make_map_4d(&mq, q, false, 1, total_q, Hq, d, 128) || !make_map_pool_sw128(&mk, k_pages, num_pages, Hkv, d) ||
+        !make_map_pool_sw128(&mv, v_pages, num_pages, Hkv, d) || !make_map_4d(&mo, out, false, 1, total_q, Hq, d, 128))
         return ATTN_ERR_CUDA;
     if (attn::launch_prefill(mq, mk, mv, mo, p, (int)units, static_cast<cudaStream_t>(stream)) != cudaSuccess)
         return ATTN_ERR_CUDA;

@@ -30,6 +30,8 @@ enum WaitSite : unsigned {
     kSiteSelftest = 10,
     kSiteDecodeTable = 11,
     kSiteVarlenOffsets = 12,
+    kSitePagedTable = 13,
+    kSiteSoftmaxV = 14,
 };
 
 // First error wins; the site is informative only.

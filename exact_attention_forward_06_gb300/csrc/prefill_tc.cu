@@ -175,6 +175,21 @@ __host__ __device__ __forceinline__ Unit unit_coords(const PrefillParams &p, int
 // The unit (and key range) CTA number cta works on.  CTAs past the whole
 // units are the parts of the tail units, part-major within a unit.
 __device__ __forceinline__ Unit decode_unit(const PrefillParams &p, int cta) {
+    if (p.block_table != nullptr) {
+        // Query chunk of sequence w.b against its paged cache.
+        Unit w = unit_coords(p, cta);
+        const int q0 = p.cu_q[w.b], q1 = p.cu_q[w.b + 1];
+        const int Lk = p.seqlens_k[w.b];
+        const bool bad = q0 < 0 || q1 < q0 || q1 > p.total_q || q1 - q0 > p.Sq || Lk < 0 || Lk > p.max_blocks * 16;
+        if (bad && threadIdx.x == 0) report_status(p.status, kStatusDeviceBounds, kSiteVarlenOffsets);
+        w.Sq = bad ? 0 : q1 - q0;
+        w.Sk = bad ? 0 : Lk;
+        w.q0 = bad ? 0 : q0;
+        w.k0 = 0;
+        w.tb = 0;
+        unit_kv_range(p, w);
+        return w;
+    }
     if (p.cu_q != nullptr) {
         // Packed batch: the unit's rows and keys are those of sequence w.b.
         // Offsets that are out of order or out of range, or lengths past the
@@ -231,13 +246,44 @@ __device__ void producer(const PrefillParams &p, const Unit &w, const SmemLayout
     load_tile(mq, sm.q_tile(1), sm.q_full(), p.bhsd, w.h[1], w.q0 + w.s0[1], w.tb, pol_q);
     const int total = 2 * w.n_kv;
     int issued = 0;
+    int page_row[BN / 16];  // paged K/V: first pool row of each page of the current tile
     for (int n = 0; n < total; ++n) {
         const int slot = n % NSLOT;
         const int round = n / NSLOT;
+        if (p.block_table != nullptr && (n & 1) == 0) {
+            // The tile's eight pages (read before waiting for the slot, so the
+            // table loads overlap the wait).  Pages past the sequence's last
+            // one, and bad entries (reported), get a row past the pool: the
+            // copy then fills zeros.
+            const int page0 = (w.j_lo + (n >> 1)) * (BN / 16);
+            const int n_pages = (w.Sk + 15) / 16;
+            const int *row = p.block_table + (int64_t)w.b * p.max_blocks;
+#pragma unroll
+            for (int i = 0; i < BN / 16; ++i) {
+                const int phys = page0 + i < n_pages ? row[page0 + i] : -1;
+                const bool ok_page = phys >= 0 && phys < p.num_pages;
+                if (!ok_page && page0 + i < n_pages) report_status(p.status, kStatusDeviceBounds, kSitePagedTable);
+                page_row[i] = ok_page ? phys * 16 : p.num_pages * 16;
+            }
+        }
         if (round > 0 && !wait_bounded(sm.kv_empty(slot), (round - 1) & 1, wc, kSiteProducerEmpty)) break;
         ptx::mbar_arrive_expect_tx(sm.kv_full(slot), TILE_BYTES);
-        load_tile((n & 1) ? mv : mk, sm.slot(slot), sm.kv_full(slot), p.bhsd, w.g, w.k0 + (w.j_lo + (n >> 1)) * BN,
-                  w.tb, pol_kv);
+        if (p.block_table != nullptr) {
+            // One 16-row box per page and half: page i fills rows 16i .. 16i+15
+            // of the tile (2 KiB per half, 1024-byte aligned, so the 128-byte
+            // swizzle matches the one a single 128-row box would give).
+            const CUtensorMap *map = (n & 1) ? mv : mk;
+            uint8_t *dst = sm.slot(slot);
+#pragma unroll
+            for (int i = 0; i < BN / 16; ++i) {
+                ptx::tma_load_3d_hint(dst + i * 2048, map, sm.kv_full(slot), 0, w.g, page_row[i], pol_kv);
+                ptx::tma_load_3d_hint(dst + HALF_BYTES + i * 2048, map, sm.kv_full(slot), 64, w.g, page_row[i],
+                                      pol_kv);
+            }
+        } else {
+            load_tile((n & 1) ? mv : mk, sm.slot(slot), sm.kv_full(slot), p.bhsd, w.g,
+                      w.k0 + (w.j_lo + (n >> 1)) * BN, w.tb, pol_kv);
+        }
         ++issued;
     }
     // On the way out make sure no copy is still writing into shared memory.
@@ -482,6 +528,29 @@ __device__ void softmax_wg(const PrefillParams &p, const Unit &w, const SmemLayo
         ptx::tmem_wait_st();
         l_run = l_run * alpha + rowsum;
         m_run = m_new;
+        if (t == 0 && p.cu_q != nullptr && kbase + BN > w.Sk) {
+            // Last tile of a packed or paged sequence: the V rows past its end
+            // hold other data (the next sequence's rows, or whatever a page's
+            // unused slots contain).  Their P is 0, but 0 * NaN is NaN, so this
+            // group zeroes those rows in shared memory once the tile has
+            // landed, before releasing its P; the other group's P V is issued
+            // after this group's, so it reads the zeros as well.
+            const int item = 2 * j + 1;
+            uint8_t *vt = sm.slot(item % NSLOT);
+            if (!wait_bounded(sm.kv_full(item % NSLOT), (uint32_t)((item / NSLOT) & 1), wc, kSiteSoftmaxV)) {
+                ok = false;
+                break;
+            }
+            if (kbase + r >= w.Sk) {
+                const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    reinterpret_cast<uint4 *>(vt + r * 128)[c] = z;
+                    reinterpret_cast<uint4 *>(vt + HALF_BYTES + r * 128)[c] = z;
+                }
+            }
+            ptx::fence_proxy_async_smem();
+        }
         warp_arrive(sm.p_full(t), lane);
     }
 

@@ -37,6 +37,14 @@ struct PrefillParams {
     const int *cu_k;
     int total_q, total_k;
     void *out;
+    // Paged K/V (block_table == nullptr: K and V are tensors): sequence b has
+    // seqlens_k[b] keys, key t in slot t % 16 of page block_table[b][t / 16]
+    // of the pools [num_pages][16][Hkv][d]; the maps for K and V are then 3-D
+    // maps over the pools with one 16-row page per box.  Queries are packed
+    // as above (cu_q); cu_k is unused.
+    const int *block_table;
+    const int *seqlens_k;
+    int max_blocks, num_pages;
 };
 
 int prefill_smem_bytes();

@@ -144,6 +144,39 @@ attn_status_t attn_fwd_varlen(const void *q, const void *k, const void *v, void 
                               int causal, float scale, int round_mode, void *stream);
 
 /*
+ * attn_fwd_paged -- prefill of packed query chunks against a paged KV cache
+ * (chunked prefill): the 16-token pages and int32 block_table of the ROCm port
+ * page ("Vendor-Agnostic 多查询推理优化") combined with the causal tiling of
+ * the reverse-engineering page (观点一 tiling strategy).
+ *
+ * q:   bf16 [total_q][Hq][d]; sequence b's query chunk is rows
+ *      cu_seqlens_q[b] .. cu_seqlens_q[b+1]-1 (DEVICE int32 [B+1]).
+ * k_pages, v_pages: bf16 [num_pages][16][Hkv][d] page pools.
+ * block_table: DEVICE int32 [B][max_blocks_per_seq]; entry p of row b is the
+ *      pool page holding keys 16p .. 16p+15 of sequence b; entries past the
+ *      sequence's last page are never read.
+ * seqlens_k: DEVICE int32 [B], the keys in each sequence's cache, the chunk's
+ *      own keys included (the chunk is the cache's last Lq tokens).
+ * out: bf16 [total_q][Hq][d]; lse: fp32 [Hq][total_q] or NULL (rows of every
+ *      chunk written, others untouched).
+ * Sequence b computes attn_fwd with B = 1 over its chunk and its gathered
+ * keys; causal != 0 applies the bottom-right mask (query i of a chunk of Lq
+ * sees keys j <= i + Lk - Lq).  Slots past a sequence's length in its last
+ * page may hold anything, NaN included: they never reach the result.
+ * page_size must be 16 and d 128; max_seqlen_q bounds the chunk lengths.
+ * Out-of-order query offsets, lengths past max_seqlen_q or the table, and
+ * table entries outside [0, num_pages) are recorded as ATTN_ERR_DEVICE_BOUNDS
+ * in the device status word (a bad page reads as zeros; a bad sequence is
+ * skipped).  Deterministic.
+ */
+attn_status_t attn_fwd_paged(const void *q, const void *k_pages, const void *v_pages,
+                             const int32_t *block_table, const int32_t *seqlens_k,
+                             const int32_t *cu_seqlens_q, void *out, float *lse,
+                             int B, int Hq, int Hkv, int total_q, int max_seqlen_q, int d,
+                             int page_size, int num_pages, int max_blocks_per_seq,
+                             int causal, float scale, int round_mode, void *stream);
+
+/*
  * attn_fwd_workspace_bytes -- device workspace that lets attn_fwd split the
  * key ranges of its last wave of work units (the Flash-Decoding style tail
  * split of the MoonMath page: the partial results are merged by log-sum-exp)

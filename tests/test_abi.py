@@ -151,3 +151,21 @@ def _varlen(lib, **kw):
 ])
 def test_fwd_varlen_rejects_bad_arguments_before_any_launch(lib, kw, code):
     assert _varlen(lib, **kw) == code
+
+
+def _paged(lib, **kw):
+    a = dict(q=16, kp=16, vp=16, bt=64, sl=64, cq=64, out=16, lse=None, B=2, Hq=4, Hkv=2, tq=100, mq=60, d=128,
+             page=16, npages=10, maxb=4, causal=1, scale=0.1, mode=0)
+    a.update(kw)
+    return lib.attn_fwd_paged(a["q"], a["kp"], a["vp"], a["bt"], a["sl"], a["cq"], a["out"], a["lse"], a["B"],
+                              a["Hq"], a["Hkv"], a["tq"], a["mq"], a["d"], a["page"], a["npages"], a["maxb"],
+                              a["causal"], a["scale"], a["mode"], None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(bt=None), 1), (dict(sl=None), 1), (dict(cq=None), 1), (dict(bt=66), 1), (dict(kp=24), 1),
+    (dict(B=0), 1), (dict(tq=0), 1), (dict(mq=0), 1), (dict(mq=101), 1), (dict(npages=0), 1), (dict(maxb=0), 1),
+    (dict(Hq=3), 1), (dict(d=64), 2), (dict(page=32), 2), (dict(mode=3), 1), (dict(scale=-1.0), 1),
+])
+def test_fwd_paged_rejects_bad_arguments_before_any_launch(lib, kw, code):
+    assert _paged(lib, **kw) == code
