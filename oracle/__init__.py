@@ -305,6 +305,28 @@ def decode_paged(q, k_pages, v_pages, block_table, seqlens, *, scale, page_size=
     return out, lse
 
 
+def decode_paged_append(q, k_new, v_new, k_pages, v_pages, block_table, seqlens, *, scale, page_size=16):
+    """Append one token per sequence to a paged cache, then decode over it.
+
+    k_new, v_new [B, Hkv, d] are written at position L = seqlens[b] of sequence
+    b, i.e. slot L % page_size of page block_table[b][L // page_size]; then each
+    query attends over the L + 1 keys.  Returns (out [B, Hq, d], lse [B, Hq],
+    k_pages', v_pages') with the pools as copies after the append."""
+    kp = k_pages.clone()
+    vp = v_pages.clone()
+    lens = [int(x) for x in seqlens]
+    bt = np.asarray(block_table)
+    for b, L in enumerate(lens):
+        page = int(bt[b][L // page_size])
+        if page < 0 or page >= kp.shape[0]:
+            raise ValueError("block table has no page for the appended token")
+        kp[page, L % page_size] = k_new[b]
+        vp[page, L % page_size] = v_new[b]
+    out, lse = decode_paged(q, kp, vp, block_table, np.asarray(lens, dtype=np.int32) + 1, scale=scale,
+                            page_size=page_size)
+    return out, lse, kp, vp
+
+
 def round_bf16_rtne(x: float) -> int:
     """Bit pattern of the bf16 nearest to x, ties to even."""
     return int(_load().oracle_round_bf16_rtne(float(x)))

@@ -195,6 +195,32 @@ def test_paged_gather_rejects_a_bad_table_entry():
         oracle.gather_pages(kp, [0, 5], 20)
 
 
+# ---------------------------------------------------------------- append + decode
+
+def test_append_then_decode_writes_one_slot_and_attends_over_it():
+    d, Hq, Hkv = 16, 4, 2
+    w = inputs.DecodeWorkload("a", B=4, Hq=Hq, Hkv=Hkv, d=d, max_blocks=4, seed=17)
+    lens = [0, 15, 16, 40]
+    q, kp, vp, table, sl = inputs.make_decode(w, seqlens=[L + 1 for L in lens])   # pages for L + 1 tokens
+    g = torch.Generator().manual_seed(18)
+    k_new = torch.randn(4, Hkv, d, generator=g).to(torch.bfloat16)
+    v_new = torch.randn(4, Hkv, d, generator=g).to(torch.bfloat16)
+    out, lse, kp2, vp2 = oracle.decode_paged_append(q, k_new, v_new, kp, vp, table, lens, scale=0.25)
+    changed = (kp2.view(torch.int16) != kp.view(torch.int16)).any(dim=(2, 3))
+    for b, L in enumerate(lens):
+        # the gathered cache's token L is the new one, and nothing else moved
+        assert torch.equal(oracle.gather_pages(kp2, table[b], L + 1)[L], k_new[b])
+        assert torch.equal(oracle.gather_pages(vp2, table[b], L + 1)[L], v_new[b])
+        assert torch.equal(oracle.gather_pages(kp2, table[b], L), oracle.gather_pages(kp, table[b], L))
+    assert int(changed.sum()) <= len(lens)
+    # attention over L + 1 keys, checked against SDPA on the gathered keys
+    for b, L in enumerate(lens):
+        kb = oracle.gather_pages(kp2, table[b], L + 1)[None]
+        vb = oracle.gather_pages(vp2, table[b], L + 1)[None]
+        ref = _sdpa_reference(q[b][None, None], kb, vb, False, 0.25)[0, 0]
+        np.testing.assert_allclose(out[b], ref, rtol=1e-10, atol=1e-12)
+
+
 # ---------------------------------------------------------------- closed forms
 
 def test_identical_keys_give_mean_of_v():
