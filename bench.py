@@ -324,6 +324,8 @@ def run_ours(args, rank, world, local_rank):
 
     # End to end through the public API: pinned host inputs -> device -> result back to pinned host.
     e2e = run_e2e(A, case, dev, stream, args)
+    # The fused append + decode step on the same decode workload (timed on its own, outside the step).
+    dec_append = run_decode_append(A, wd, lens_h, dev, stream, args)
 
     if rank != 0:
         return None
@@ -368,6 +370,7 @@ def run_ours(args, rank, world, local_rank):
                                 "traffic": dec_traffic, "peak_source": f"{peak_src} hbm_gbs",
                                 "kernel": "attn::dec::split_kernel + merge_kernel",
                                 "algorithmic": f"{kv_bytes} B K+V per launch (4096 B per token)"}},
+        "decode_append": dec_append,
         "e2e": e2e,
         "gpu_launches": (4 if fws_bytes else 3) * K,
         "clocks": clk,
@@ -384,6 +387,42 @@ def prefill_units(w):
     if G % 2 == 0:
         return w.B * w.Hkv * (G // 2) * n_m
     return w.B * w.Hq * ((n_m + 1) // 2)
+
+
+def run_decode_append(A, wd, lens_h, dev, stream, args):
+    """The fused append + decode call on the decode workload's lengths: a pool
+    with pages for L + 1 tokens, the new token appended at position L."""
+    q_h, kp_h, vp_h, table_h, _ = inputs.make_decode(wd, seqlens=(lens_h + 1).tolist())
+    g = torch.Generator().manual_seed(wd.seed + 7)
+    k_new = torch.randn(wd.B, wd.Hkv, wd.d, generator=g).to(torch.bfloat16).to(dev)
+    v_new = torch.randn(wd.B, wd.Hkv, wd.d, generator=g).to(torch.bfloat16).to(dev)
+    q, kp, vp, table, lens = (t.to(dev) for t in (q_h, kp_h, vp_h, table_h, lens_h))
+    out = torch.empty_like(q)
+    lse = torch.empty((wd.B, wd.Hq), device=dev, dtype=torch.float32)
+    ws = torch.empty(A.decode_workspace_bytes(wd.B, wd.Hq, wd.d, wd.max_blocks), device=dev, dtype=torch.uint8)
+
+    def call():
+        A.decode_paged_append(q, k_new, v_new, kp, vp, table, lens, scale=wd.scale, out=out, lse=lse, workspace=ws,
+                              stream=stream)
+
+    for _ in range(args.warmup):
+        call()
+    torch.cuda.synchronize(dev)
+    n = max(3, args.steps)
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record(stream)
+    for _ in range(n):
+        call()
+    e.record(stream)
+    torch.cuda.synchronize(dev)
+    code, site = A.device_status()
+    if code != 0:
+        raise RuntimeError(f"device status {code} at site {site} in the fused append")
+    ms = reduce_max_over_ranks(s.elapsed_time(e) / n)
+    kv_bytes = inputs.decode_kv_bytes((lens_h + 1).tolist(), wd.Hkv, wd.d)
+    return {"value": round(_world() * kv_bytes / (ms * 1e-3) / 1e9, 1), "unit": "GB/s", "ms_per_launch": round(ms, 4),
+            "kernel": "attn::dec::split_kernel (fused append) + merge_kernel",
+            "algorithmic": f"{kv_bytes} B K+V per launch (L+1 keys per sequence)"}
 
 
 def run_e2e(A, case, dev, stream, args):

@@ -64,6 +64,9 @@ def load():
             lib.attn_decode_workspace_bytes.restype = _sz
             lib.attn_decode_paged.argtypes = [_p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _f, _p,
                                               _sz, _p]
+            lib.attn_decode_paged_append.argtypes = [_p, _p, _p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i,
+                                                     _i, _f, _p, _sz, _p]
+            lib.attn_decode_paged_append.restype = _i
             lib.attn_decode_paged_noalloc.argtypes = [_p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i,
                                                       _f, _p]
             lib.attn_decode_paged_noalloc.restype = _i
@@ -306,6 +309,39 @@ def decode_paged(q, k_pages, v_pages, block_table, seqlens, *, scale=None, out=N
                                max_blocks, float(scale), workspace.data_ptr(), workspace.numel(),
                                _stream(stream))
     _check(rc, "attn_decode_paged")
+    return out, (None if lse is False else lse)
+
+
+def decode_paged_append(q, k_new, v_new, k_pages, v_pages, block_table, seqlens, *, scale=None, out=None, lse=None,
+                        workspace=None, stream=None):
+    """Append k_new/v_new [B, Hkv, d] at position seqlens[b] of each sequence's pages and decode over the
+    seqlens[b] + 1 keys, in one launch.  seqlens (the lengths before the append) is not modified.
+    Returns (out [B, Hq, d] bf16, lse [B, Hq] fp32); k_pages and v_pages are updated in place."""
+    lib = load()
+    for t, n in ((q, "q"), (k_new, "k_new"), (v_new, "v_new"), (k_pages, "k_pages"), (v_pages, "v_pages")):
+        _dev_tensor(t, n, torch.bfloat16)
+    _dev_tensor(block_table, "block_table", torch.int32)
+    _dev_tensor(seqlens, "seqlens", torch.int32)
+    B, Hq, d = q.shape
+    num_pages, page_size, Hkv, _ = k_pages.shape
+    if k_new.shape != (B, Hkv, d) or v_new.shape != (B, Hkv, d):
+        raise ValueError("k_new and v_new must be [B, Hkv, d]")
+    max_blocks = block_table.shape[1]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, Hq), device=q.device, dtype=torch.float32)
+    need = decode_workspace_bytes(B, Hq, d, max_blocks)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), device=q.device, dtype=torch.uint8)
+    lse_ptr = None if lse is False else lse.data_ptr()
+    rc = lib.attn_decode_paged_append(q.data_ptr(), k_new.data_ptr(), v_new.data_ptr(), k_pages.data_ptr(),
+                                      v_pages.data_ptr(), block_table.data_ptr(), seqlens.data_ptr(), out.data_ptr(),
+                                      lse_ptr, B, Hq, Hkv, d, page_size, num_pages, max_blocks, float(scale),
+                                      workspace.data_ptr(), workspace.numel(), _stream(stream))
+    _check(rc, "attn_decode_paged_append")
     return out, (None if lse is False else lse)
 
 

@@ -369,10 +369,11 @@ size_t attn_decode_workspace_bytes(int B, int Hq, int d, int max_blocks_per_seq)
     return o_bytes + l_bytes;
 }
 
-attn_status_t attn_decode_paged(const void *q, const void *k_pages, const void *v_pages,
-                                const int32_t *block_table, const int32_t *seqlens, void *out, float *lse, int B,
-                                int Hq, int Hkv, int d, int page_size, int num_pages, int max_blocks_per_seq,
-                                float scale, void *workspace, size_t workspace_bytes, void *stream) {
+static attn_status_t decode_impl(const void *q, const void *k_new, const void *v_new, const void *k_pages,
+                                 const void *v_pages, const int32_t *block_table, const int32_t *seqlens, void *out,
+                                 float *lse, int B, int Hq, int Hkv, int d, int page_size, int num_pages,
+                                 int max_blocks_per_seq, float scale, void *workspace, size_t workspace_bytes,
+                                 void *stream) {
     if (!q || !k_pages || !v_pages || !block_table || !seqlens || !out) return ATTN_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(k_pages) || !aligned16(v_pages) || !aligned16(out)) return ATTN_ERR_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(block_table) & 3u) || (reinterpret_cast<uintptr_t>(seqlens) & 3u))
@@ -413,8 +414,30 @@ attn_status_t attn_decode_paged(const void *q, const void *k_pages, const void *
     p.scale_log2 = (float)((double)scale * 1.4426950408889634);
     p.status = di->status;
     p.budget_ns = budget();
+    p.k_new = k_new;
+    p.v_new = v_new;
+    p.k_pool = const_cast<void *>(k_pages);
+    p.v_pool = const_cast<void *>(v_pages);
     if (attn::launch_decode(mk, mv, p, static_cast<cudaStream_t>(stream)) != cudaSuccess) return ATTN_ERR_CUDA;
     return ATTN_OK;
+}
+
+attn_status_t attn_decode_paged(const void *q, const void *k_pages, const void *v_pages,
+                                const int32_t *block_table, const int32_t *seqlens, void *out, float *lse, int B,
+                                int Hq, int Hkv, int d, int page_size, int num_pages, int max_blocks_per_seq,
+                                float scale, void *workspace, size_t workspace_bytes, void *stream) {
+    return decode_impl(q, nullptr, nullptr, k_pages, v_pages, block_table, seqlens, out, lse, B, Hq, Hkv, d,
+                       page_size, num_pages, max_blocks_per_seq, scale, workspace, workspace_bytes, stream);
+}
+
+attn_status_t attn_decode_paged_append(const void *q, const void *k_new, const void *v_new, void *k_pages,
+                                       void *v_pages, const int32_t *block_table, const int32_t *seqlens, void *out,
+                                       float *lse, int B, int Hq, int Hkv, int d, int page_size, int num_pages,
+                                       int max_blocks_per_seq, float scale, void *workspace, size_t workspace_bytes,
+                                       void *stream) {
+    if (!k_new || !v_new || !aligned16(k_new) || !aligned16(v_new)) return ATTN_ERR_INVALID_ARG;
+    return decode_impl(q, k_new, v_new, k_pages, v_pages, block_table, seqlens, out, lse, B, Hq, Hkv, d, page_size,
+                       num_pages, max_blocks_per_seq, scale, workspace, workspace_bytes, stream);
 }
 
 attn_status_t attn_lse_merge(const float *o_parts, const float *lse_parts, void *out, float *lse, int rows,

@@ -32,6 +32,7 @@ enum WaitSite : unsigned {
     kSiteVarlenOffsets = 12,
     kSitePagedTable = 13,
     kSiteSoftmaxV = 14,
+    kSiteAppendSlot = 15,
 };
 
 // First error wins; the site is informative only.

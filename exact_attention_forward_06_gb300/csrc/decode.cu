@@ -105,14 +105,16 @@ __global__ void __launch_bounds__(NTHREADS, 3)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
-    int L = p.seqlens[b];
-    L = max(0, min(L, p.max_blocks * PAGE));
+    const int L_raw = p.seqlens[b];
+    const int L = max(0, min(L_raw, p.max_blocks * PAGE));
     const int npages = (L + PAGE - 1) / PAGE;
     const int page0 = split * p.pages_per_split;
     const int np = max(0, min(p.pages_per_split, npages - page0));
     const int64_t row0 = (int64_t)b * p.Hq + h0;  // first (b, h) row of this CTA
+    // With a fused append, split 0 also attends to the new token (position L).
+    const bool new_token = p.k_new != nullptr && split == 0;
 
-    if (np == 0) {  // nothing to attend to in this split
+    if (np == 0 && !new_token) {  // nothing to attend to in this split
         for (int i = threadIdx.x; i < GH * D; i += NTHREADS)
             p.o_part[((row0 + i / D) * p.nsplit + split) * D + (i % D)] = 0.f;
         if (threadIdx.x < GH) p.lse_part[(row0 + threadIdx.x) * p.nsplit + split] = -INFINITY;
@@ -136,6 +138,27 @@ __global__ void __launch_bounds__(NTHREADS, 3)
         // The whole warp reads the split's block-table entries in one go, so
         // the copy-issuing lane never waits on a global load per page.
         for (int k = lane; k < np; k += 32) split_pages[k] = p.block_table[(int64_t)b * p.max_blocks + page0 + k];
+        if (new_token && h0 % p.G == 0) {
+            // Fused append: one CTA per (sequence, KV head) writes the new
+            // token's K and V rows (256 B each) into slot L % 16 of page
+            // block_table[b][L / 16].  Another split may be reading that page
+            // right now, but position L lies past the L keys it attends to, so
+            // whichever value it reads there is masked out.
+            const int64_t slot_page = L_raw >= 0 && L_raw < p.max_blocks * PAGE
+                                          ? p.block_table[(int64_t)b * p.max_blocks + L_raw / PAGE]
+                                          : -1;
+            if (slot_page < 0 || slot_page >= p.num_pages) {
+                if (lane == 0) report_status(p.status, kStatusDeviceBounds, kSiteAppendSlot);
+            } else {
+                const int64_t off = ((slot_page * PAGE + L_raw % PAGE) * p.Hkv + g) * D;
+                const int64_t src = ((int64_t)b * p.Hkv + g) * D;
+                const bool is_v = lane >= 16;
+                const uint4 *from = reinterpret_cast<const uint4 *>(
+                    static_cast<const __nv_bfloat16 *>(is_v ? p.v_new : p.k_new) + src);
+                uint4 *to = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(is_v ? p.v_pool : p.k_pool) + off);
+                to[lane & 15] = from[lane & 15];
+            }
+        }
         __syncwarp();
         if (lane == 0) {
             ptx::prefetch_tensormap(&map_k);
@@ -262,6 +285,41 @@ __global__ void __launch_bounds__(NTHREADS, 3)
             }
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(empty + slot);
+        }
+        if (new_token && stream == 0) {
+            // The appended token, read from k_new / v_new rather than the
+            // cache: every token group computes the same score and only
+            // group 0 adds the token to its sums.
+            const int64_t src = ((int64_t)b * p.Hkv + g) * D;
+            const uint4 *kn = reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(p.k_new) + src);
+            const uint4 *vn = reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(p.v_new) + src);
+            float2 kf[8], vf[8];
+            bf16x8_to_float2(kn[ds], kf);
+            bf16x8_to_float2(kn[8 + ds], kf + 4);
+            bf16x8_to_float2(vn[ds], vf);
+            bf16x8_to_float2(vn[8 + ds], vf + 4);
+#pragma unroll
+            for (int h = 0; h < HG; ++h) {
+                float2 d2 = __fmul2_rn(qf[h][0], kf[0]);
+#pragma unroll
+                for (int e = 1; e < 8; ++e) d2 = __ffma2_rn(qf[h][e], kf[e], d2);
+                float sc = d2.x + d2.y;
+                sc += __shfl_xor_sync(0xffffffffu, sc, 1);
+                sc += __shfl_xor_sync(0xffffffffu, sc, 2);
+                sc += __shfl_xor_sync(0xffffffffu, sc, 4);
+                if (sc > m[h] + RESCALE_LOG2) {  // warp-uniform
+                    const float alpha = ptx::ex2(m[h] - sc);
+                    lsum[h] *= alpha;
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) acc[h][e] = __fmul2_rn(acc[h][e], make_float2(alpha, alpha));
+                    m[h] = sc;
+                }
+                const float pr = tg == 0 ? ptx::ex2(sc - m[h]) : 0.f;
+                lsum[h] += pr;
+                const float2 p2 = make_float2(pr, pr);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) acc[h][e] = __ffma2_rn(p2, vf[e], acc[h][e]);
+            }
         }
         // Sum the four token groups (lanes 8 and 16 apart share a slice).
 #pragma unroll

@@ -74,6 +74,12 @@ struct DecodeParams {
     float scale_log2;
     unsigned *status;
     uint64_t budget_ns;
+    // Fused append (k_new == nullptr: none): the token k_new/v_new [B][Hkv][d]
+    // is written at position seqlens[b] of the pools and attended to as well.
+    const void *k_new;
+    const void *v_new;
+    void *k_pool;
+    void *v_pool;
 };
 
 void decode_split_plan(int B, int Hq, int max_blocks, int *nsplit, int *pages_per_split);

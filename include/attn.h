@@ -246,6 +246,33 @@ attn_status_t attn_decode_paged(const void *q, const void *k_pages, const void *
                                 void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * attn_decode_paged_append -- append one token per sequence to the paged
+ * cache and decode over it, in the same launch (the new token's K/V written
+ * into its page while the step's attention runs, as in the reverse-
+ * engineering page's 观点二 decode discussion).
+ *
+ * k_new, v_new: bf16 [B][Hkv][d], the new token's key and value rows.
+ * seqlens: the cache lengths BEFORE the append (read only; the caller
+ *      advances them afterwards).  The token goes to slot seqlens[b] % 16 of
+ *      page block_table[b][seqlens[b] / 16], which must be a valid page (a
+ *      new page for a sequence whose length is a multiple of 16).
+ * k_pages, v_pages: written at exactly those slots (B x Hkv rows each), read
+ *      elsewhere.
+ * Every query attends over its sequence's seqlens[b] + 1 keys, the new one
+ * included; out, lse, the other arguments, the workspace and the errors are
+ * those of attn_decode_paged.  A slot outside the table or the pool is
+ * recorded as ATTN_ERR_DEVICE_BOUNDS and that token is not written (it is
+ * still attended to).  k_new, v_new must not overlap the pools.
+ */
+attn_status_t attn_decode_paged_append(const void *q, const void *k_new, const void *v_new,
+                                       void *k_pages, void *v_pages,
+                                       const int32_t *block_table, const int32_t *seqlens,
+                                       void *out, float *lse,
+                                       int B, int Hq, int Hkv, int d, int page_size,
+                                       int num_pages, int max_blocks_per_seq, float scale,
+                                       void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * ATTN_DECODE_NOALLOC_SCRATCH_BYTES -- capacity of the device array that
  * attn_decode_paged_noalloc keeps its split partials in: 16 MiB, held on every
  * GPU that loads the library until the process exits.

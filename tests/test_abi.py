@@ -169,3 +169,15 @@ def _paged(lib, **kw):
 ])
 def test_fwd_paged_rejects_bad_arguments_before_any_launch(lib, kw, code):
     assert _paged(lib, **kw) == code
+
+
+def test_decode_append_rejects_bad_arguments(lib):
+    args = [16, 16, 16, 16, 16, 64, 64, 16, None, 2, 4, 2, 128, 16, 10, 4, 0.1, 256, 1 << 20, None]
+    assert lib.attn_decode_paged_append(*args[:1], None, *args[2:]) == 1        # no k_new
+    assert lib.attn_decode_paged_append(*args[:2], 24, *args[3:]) == 1          # misaligned v_new
+    bad = list(args)
+    bad[13] = 32                                                                # page size
+    assert lib.attn_decode_paged_append(*bad) == 2
+    bad = list(args)
+    bad[17] = None                                                              # workspace
+    assert lib.attn_decode_paged_append(*bad) == 5
