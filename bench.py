@@ -487,11 +487,17 @@ def _oracle_sample(w, q_h, k_h, v_h, seconds, seed):
     oracle.attention_rows(q_h, k_h, v_h, probe, **kw)
     dt = time.perf_counter() - t0
     n = max(len(probe), int(len(probe) * seconds / max(dt, 1e-3)))
-    rows = rows_of(n)
-    t0 = time.perf_counter()
-    oracle.attention_rows(q_h, k_h, v_h, rows, **kw)
-    dt = time.perf_counter() - t0
-    return _row_flops(w, rows), dt, n
+    for _ in range(2):
+        # the probe over-estimates the time per row (fixed costs); re-size once
+        # if the sample ran well short of `seconds`
+        rows = rows_of(n)
+        t0 = time.perf_counter()
+        oracle.attention_rows(q_h, k_h, v_h, rows, **kw)
+        dt = time.perf_counter() - t0
+        if dt >= 0.5 * seconds:
+            break
+        n = int(n * seconds / max(dt, 1e-3))
+    return _row_flops(w, rows), dt, len(rows)
 
 
 def _oracle_sample_varlen(case, seconds, seed):
