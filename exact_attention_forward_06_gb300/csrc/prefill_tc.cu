@@ -15,8 +15,9 @@
 // query rows.  Warp roles (384 threads, three warpgroups):
 //   warp 0      TMA producer: Q tiles once, then K_j / V_j into a 5-slot ring
 //               of 32 KiB slots (full/empty mbarrier pairs);
-//   warp 1      TMEM allocator and single-thread tcgen05 MMA issuer;
-//   warps 2-3   idle (they complete warpgroup 0, which gives up registers);
+//   warp 1      TMEM allocator and tcgen05 MMA issuer for Q tile 0 (one lane);
+//   warp 2      tcgen05 MMA issuer for Q tile 1 (one lane);
+//   warp 3      idle (it completes warpgroup 0, which gives up registers);
 //   warps 4-7   softmax warpgroup for Q tile 0 (one thread per row);
 //   warps 8-11  softmax warpgroup for Q tile 1.
 // setmaxnreg moves registers from warpgroup 0 (96 each) to the softmax
@@ -24,11 +25,15 @@
 // Tensor memory (512 columns): one fp32 score buffer S that the two tiles use
 // in turn, a bf16 probability buffer P_t per tile (64 columns of packed
 // pairs, read by the P V product straight from tensor memory) and an fp32
-// output accumulator O_t per tile.  The MMA thread issues, for every K/V tile
-// j, S_0(j+1), PV_0(j), S_1(j+1), PV_1(j): while one tile's softmax runs, the
-// tensor core works on the other tile's products, and a softmax releases S as
-// soon as it has loaded its scores (the two-group alternation of the MoonMath
-// page, realised as two Q tiles instead of two wave groups).
+// output accumulator O_t per tile.  Each tile has its own issuing thread,
+// which issues S_t(j+1) then PV_t(j) for every K/V tile j; the score tiles
+// alternate through the shared S buffer (S_0(j), S_1(j), S_0(j+1), ...), each
+// issued as soon as the other tile's softmax has loaded the previous one.
+// While one tile's softmax runs the tensor core works on the other tile's
+// products (the two-group alternation of the MoonMath page, realised as two
+// Q tiles instead of two wave groups), and since an issuing thread is held
+// while its products execute, two of them keep the tensor core fed across
+// each other's waits.
 //
 // Softmax: scores are scaled into the log2 domain (scale * log2 e folded into
 // one FFMA) and exponentiated with ex2.approx.  A row's running max is only
@@ -64,7 +69,7 @@ constexpr uint32_t SMEM_Q0 = 0;
 constexpr uint32_t SMEM_Q1 = TILE_BYTES;
 constexpr uint32_t SMEM_SLOTS = 2 * TILE_BYTES;
 constexpr uint32_t SMEM_TILES = SMEM_SLOTS + NSLOT * TILE_BYTES;
-constexpr int NBARS = 1 + 2 * NSLOT + 2 + 1 + 2 + 2 + 1;
+constexpr int NBARS = 1 + 2 * NSLOT + 2 + 1 + 2 + 2 + 1 + 1;
 constexpr uint32_t SMEM_MISC = 256;
 constexpr uint32_t SMEM_ALIGN = 1024;
 constexpr float RESCALE_LOG2 = 8.0f;  // move the running max only past a 2^8 growth
@@ -91,7 +96,8 @@ struct SmemLayout {
     __device__ uint64_t *kv_full(int s) const { return bars + 1 + s; }
     __device__ uint64_t *kv_empty(int s) const { return bars + 1 + NSLOT + s; }
     __device__ uint64_t *s_full(int t) const { return bars + 1 + 2 * NSLOT + t; }
-    __device__ uint64_t *s_free() const { return bars + 3 + 2 * NSLOT; }
+    // s_free(t): phase j completes when softmax group t has loaded its score tile j.
+    __device__ uint64_t *s_free(int t) const { return t ? bars + 9 + 2 * NSLOT : bars + 3 + 2 * NSLOT; }
     __device__ uint64_t *p_full(int t) const { return bars + 4 + 2 * NSLOT + t; }
     __device__ uint64_t *o_full(int t) const { return bars + 6 + 2 * NSLOT + t; }
     __device__ uint64_t *fin() const { return bars + 8 + 2 * NSLOT; }
@@ -314,61 +320,60 @@ __device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t tmem_p, uint6
     }
 }
 
-// Static issue order S0(0), S1(0), then for every K/V tile j:
-//   S0(j+1), PV0(j), S1(j+1), PV1(j)
-// so the two softmax warpgroups alternate: while one works on its scores the
-// tensor core runs the other tile's P V and next Q K^T.  Every product waits
-// (bounded) on exactly the barriers it needs:
-//   S(n)  -- the n-th score tile, n = 2j + t -- needs K_j and the shared S
-//            buffer released by the softmax that consumed S(n-1) (s_free);
+// One issuing thread per tile (stream t), in the order
+//   S_t(0), then for every K/V tile j:  S_t(j+1), PV_t(j)
+// The score tiles go through one shared S buffer in the order
+// S_0(0), S_1(0), S_0(1), S_1(1), ...: each is issued once the softmax that
+// consumed the one before (the other tile's) has loaded it.  Each group has
+// its own s_free barrier: S_1(j) waits for phase j of s_free(0), S_0(j+1) for
+// phase j of s_free(1).  (A single barrier for both would let a stream that
+// runs ahead pass on the parity of a phase two back.)
+// An issuing thread is held while its products execute, and a P V product
+// waits for its tile's whole softmax; with one stream per tile, neither holds
+// up the other tile's products, and one thread's waits and commits overlap
+// the other's products.
+//   S_t(j)  needs K_j and the other group's s_free (phase j for S_1(j), j-1 for S_0(j));
 //   PV_t(j) needs P_t(j) (p_full[t]) and V_j.
-// Ring slots are released by a commit once both products reading them are issued.
-__device__ void mma_issuer(const Unit &w, const SmemLayout &sm, const WaitCtx &wc, uint32_t tmem_base) {
+// A ring slot takes one release per stream (a commit after the stream's
+// product that reads it).
+template <int T>
+__device__ void mma_stream(const Unit &w, const SmemLayout &sm, const WaitCtx &wc, uint32_t tmem_base) {
     if (w.n_kv == 0) return;  // nothing to multiply (and no Q is loaded)
     if (!wait_bounded(sm.q_full(), 0, wc, kSiteMmaQ)) return;
     ptx::tc_fence_after();
-    const uint64_t q_desc[2] = {ptx::desc_kmajor_sw128(ptx::smem_addr(sm.q_tile(0))),
-                                ptx::desc_kmajor_sw128(ptx::smem_addr(sm.q_tile(1)))};
+    const uint64_t q_desc = ptx::desc_kmajor_sw128(ptx::smem_addr(sm.q_tile(T)));
     const uint32_t slot0 = ptx::smem_addr(sm.slot(0));
     auto slot_of = [](int n) { return n % NSLOT; };
     auto par_of = [](int n) { return (uint32_t)((n / NSLOT) & 1); };
 
-    // One score tile: S_t(j) into the shared buffer.
-    auto do_s = [&](int t, int j) -> bool {
-        const int n = 2 * j + t;  // score tile number
-        const int item = 2 * j;   // ring item holding K_j
-        if (n > 0 && !wait_bounded(sm.s_free(), (uint32_t)((n - 1) & 1), wc, kSiteMmaPoll)) return false;
+    auto do_s = [&](int j) -> bool {
+        const int item = 2 * j;  // ring item holding K_j
+        // the score tile before this one: S_0(j) for S_1(j), S_1(j-1) for S_0(j)
+        const int prev = T == 1 ? j : j - 1;
+        if (prev >= 0 && !wait_bounded(sm.s_free(1 - T), (uint32_t)(prev & 1), wc, kSiteMmaPoll)) return false;
         if (!wait_bounded(sm.kv_full(slot_of(item)), par_of(item), wc, kSiteMmaPoll)) return false;
         ptx::tc_fence_after();
-        issue_s(tmem_base + TM_S, q_desc[t], ptx::desc_kmajor_sw128(slot0 + slot_of(item) * TILE_BYTES));
-        ptx::umma_commit(sm.s_full(t));
-        if (t == 1) ptx::umma_commit(sm.kv_empty(slot_of(item)));  // K_j done
+        issue_s(tmem_base + TM_S, q_desc, ptx::desc_kmajor_sw128(slot0 + slot_of(item) * TILE_BYTES));
+        ptx::umma_commit(sm.s_full(T));
+        ptx::umma_commit(sm.kv_empty(slot_of(item)));  // this stream is done with K_j
         return true;
     };
-    // One P V product: O_t += P_t(j) V_j.
-    auto do_pv = [&](int t, int j) -> bool {
+    auto do_pv = [&](int j) -> bool {
         const int item = 2 * j + 1;  // ring item holding V_j
-        if (!wait_bounded(sm.p_full(t), (uint32_t)(j & 1), wc, kSiteMmaPoll)) return false;
+        if (!wait_bounded(sm.p_full(T), (uint32_t)(j & 1), wc, kSiteMmaPoll)) return false;
         if (!wait_bounded(sm.kv_full(slot_of(item)), par_of(item), wc, kSiteMmaPoll)) return false;
         ptx::tc_fence_after();
-        issue_pv(tmem_base + tm_o(t), tmem_base + tm_p(t),
+        issue_pv(tmem_base + tm_o(T), tmem_base + tm_p(T),
                  ptx::desc_mnmajor_sw128(slot0 + slot_of(item) * TILE_BYTES, HALF_BYTES), j > 0 ? 1u : 0u);
-        ptx::umma_commit(sm.o_full(t));
-        if (t == 1) ptx::umma_commit(sm.kv_empty(slot_of(item)));  // V_j done
+        ptx::umma_commit(sm.o_full(T));
+        ptx::umma_commit(sm.kv_empty(slot_of(item)));  // this stream is done with V_j
         return true;
     };
 
-    // S production is the tight loop: each score tile needs the previous one
-    // loaded out of the shared buffer, so S0(j+1) goes out as soon as tile 1's
-    // softmax has read S1(j), before PV0(j) (which waits for tile 0's whole
-    // softmax).  The P V products fill the gaps.
-    if (!do_s(0, 0) || !do_s(1, 0)) return;
+    if (!do_s(0)) return;
     for (int j = 0; j < w.n_kv; ++j) {
-        const bool more = j + 1 < w.n_kv;
-        if (more && !do_s(0, j + 1)) return;
-        if (!do_pv(0, j)) return;
-        if (more && !do_s(1, j + 1)) return;
-        if (!do_pv(1, j)) return;
+        if (j + 1 < w.n_kv && !do_s(j + 1)) return;
+        if (!do_pv(j)) return;
     }
 }
 
@@ -452,7 +457,7 @@ __device__ void softmax_wg(const PrefillParams &p, const Unit &w, const SmemLayo
             ptx::tmem_wait_ld();
             // The scores are in registers: release the shared S buffer so the
             // other tile's next Q K^T can start while this tile's softmax runs.
-            warp_arrive(sm.s_free(), lane);
+            warp_arrive(sm.s_free(t), lane);
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
                 s[i] = make_float2(__uint_as_float(a[2 * i]), __uint_as_float(a[2 * i + 1]));
@@ -528,13 +533,13 @@ __device__ void softmax_wg(const PrefillParams &p, const Unit &w, const SmemLayo
         ptx::tmem_wait_st();
         l_run = l_run * alpha + rowsum;
         m_run = m_new;
-        if (t == 0 && p.cu_q != nullptr && kbase + BN > w.Sk) {
+        if (p.cu_q != nullptr && kbase + BN > w.Sk) {
             // Last tile of a packed or paged sequence: the V rows past its end
             // hold other data (the next sequence's rows, or whatever a page's
-            // unused slots contain).  Their P is 0, but 0 * NaN is NaN, so this
+            // unused slots contain).  Their P is 0, but 0 * NaN is NaN, so each
             // group zeroes those rows in shared memory once the tile has
-            // landed, before releasing its P; the other group's P V is issued
-            // after this group's, so it reads the zeros as well.
+            // landed, before releasing its P (the two streams' P V products
+            // are not ordered; both groups write the same zeros).
             const int item = 2 * j + 1;
             uint8_t *vt = sm.slot(item % NSLOT);
             if (!wait_bounded(sm.kv_full(item % NSLOT), (uint32_t)((item / NSLOT) & 1), wc, kSiteSoftmaxV)) {
@@ -662,7 +667,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         ptx::mbar_init(sm.q_full(), 1);
         for (int s = 0; s < NSLOT; ++s) {
             ptx::mbar_init(sm.kv_full(s), 1);
-            ptx::mbar_init(sm.kv_empty(s), 1);
+            ptx::mbar_init(sm.kv_empty(s), 2);  // one release per issuing stream
         }
         // Softmax-side barriers take one arrival per warp (lane 0, after the
         // warp's tcgen05 fence and __syncwarp).
@@ -671,8 +676,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             ptx::mbar_init(sm.p_full(t), 4);
             ptx::mbar_init(sm.o_full(t), 1);
         }
-        ptx::mbar_init(sm.s_free(), 4);
-        ptx::mbar_init(sm.fin(), 1);
+        ptx::mbar_init(sm.s_free(0), 4);
+        ptx::mbar_init(sm.s_free(1), 4);
+        ptx::mbar_init(sm.fin(), 2);  // one commit per issuing stream
         *sm.abort_flag() = 0;
         ptx::fence_mbar_init();
         ptx::prefetch_tensormap(&map_q);
@@ -694,11 +700,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         ptx::setmaxnreg_dec<REGS_CONTROL>();
         if (warp == 0) {
             if (lane == 0) producer(p, w, sm, wc, &map_q, &map_k, &map_v);
-        } else if (warp == 1) {
+        } else if (warp == 1 || warp == 2) {
             if (lane == 0) {
-                mma_issuer(w, sm, wc, tmem_base);
-                // Whatever happened, wait until every product issued has
-                // completed before tensor memory is released.
+                if (warp == 1)
+                    mma_stream<0>(w, sm, wc, tmem_base);
+                else
+                    mma_stream<1>(w, sm, wc, tmem_base);
+                // Whatever happened, wait until every product issued (by
+                // either stream) has completed before tensor memory is released.
                 ptx::umma_commit(sm.fin());
                 drain_wait(sm.fin(), 0, wc);
             }
