@@ -66,6 +66,24 @@ static __device__ __forceinline__ bool wait_bounded(uint64_t *bar, uint32_t pari
     }
 }
 
+// Wait by polling with the non-blocking test (the issuing threads, whose
+// reaction time is on the critical path).
+static __device__ __forceinline__ bool wait_spin(uint64_t *bar, uint32_t parity, const WaitCtx &w, unsigned site) {
+    if (ptx::mbar_test(bar, parity)) return true;
+    const uint64_t t0 = ptx::globaltimer();
+    for (uint32_t it = 1;; ++it) {
+        if (ptx::mbar_test(bar, parity)) return true;
+        if ((it & 63u) == 0) {
+            if (*w.abort_flag) return false;
+            if (ptx::globaltimer() - t0 > w.budget_ns) {
+                *w.abort_flag = 1;
+                report_status(w.status, kStatusTimeout, site);
+                return false;
+            }
+        }
+    }
+}
+
 // Wait for completion of an operation this thread itself started (a copy or
 // an MMA in flight), ignoring the abort flag: used on the way out so that no
 // asynchronous write into shared or tensor memory outlives the CTA.  Still

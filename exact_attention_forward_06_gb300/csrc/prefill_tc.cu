@@ -339,7 +339,7 @@ __device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t tmem_p, uint6
 template <int T>
 __device__ void mma_stream(const Unit &w, const SmemLayout &sm, const WaitCtx &wc, uint32_t tmem_base) {
     if (w.n_kv == 0) return;  // nothing to multiply (and no Q is loaded)
-    if (!wait_bounded(sm.q_full(), 0, wc, kSiteMmaQ)) return;
+    if (!wait_spin(sm.q_full(), 0, wc, kSiteMmaQ)) return;
     ptx::tc_fence_after();
     const uint64_t q_desc = ptx::desc_kmajor_sw128(ptx::smem_addr(sm.q_tile(T)));
     const uint32_t slot0 = ptx::smem_addr(sm.slot(0));
@@ -350,8 +350,8 @@ __device__ void mma_stream(const Unit &w, const SmemLayout &sm, const WaitCtx &w
         const int item = 2 * j;  // ring item holding K_j
         // the score tile before this one: S_0(j) for S_1(j), S_1(j-1) for S_0(j)
         const int prev = T == 1 ? j : j - 1;
-        if (prev >= 0 && !wait_bounded(sm.s_free(1 - T), (uint32_t)(prev & 1), wc, kSiteMmaPoll)) return false;
-        if (!wait_bounded(sm.kv_full(slot_of(item)), par_of(item), wc, kSiteMmaPoll)) return false;
+        if (prev >= 0 && !wait_spin(sm.s_free(1 - T), (uint32_t)(prev & 1), wc, kSiteMmaPoll)) return false;
+        if (!wait_spin(sm.kv_full(slot_of(item)), par_of(item), wc, kSiteMmaPoll)) return false;
         ptx::tc_fence_after();
         issue_s(tmem_base + TM_S, q_desc, ptx::desc_kmajor_sw128(slot0 + slot_of(item) * TILE_BYTES));
         ptx::umma_commit(sm.s_full(T));
@@ -360,8 +360,8 @@ __device__ void mma_stream(const Unit &w, const SmemLayout &sm, const WaitCtx &w
     };
     auto do_pv = [&](int j) -> bool {
         const int item = 2 * j + 1;  // ring item holding V_j
-        if (!wait_bounded(sm.p_full(T), (uint32_t)(j & 1), wc, kSiteMmaPoll)) return false;
-        if (!wait_bounded(sm.kv_full(slot_of(item)), par_of(item), wc, kSiteMmaPoll)) return false;
+        if (!wait_spin(sm.p_full(T), (uint32_t)(j & 1), wc, kSiteMmaPoll)) return false;
+        if (!wait_spin(sm.kv_full(slot_of(item)), par_of(item), wc, kSiteMmaPoll)) return false;
         ptx::tc_fence_after();
         issue_pv(tmem_base + tm_o(T), tmem_base + tm_p(T),
                  ptx::desc_mnmajor_sw128(slot0 + slot_of(item) * TILE_BYTES, HALF_BYTES), j > 0 ? 1u : 0u);
