@@ -355,6 +355,8 @@ __global__ void __launch_bounds__(NTHREADS, 3)
         }
     }
     __syncthreads();
+    // The merge kernel may be scheduled now; it waits for this grid to finish.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (*abort_flag) return;
     // Merge the page streams: thread = head-dim element, loop over heads.
     if (threadIdx.x < D) {
@@ -386,6 +388,9 @@ __global__ void __launch_bounds__(D) merge_kernel(const float *__restrict__ o_pa
                                                   const float *__restrict__ lse_parts,
                                                   uint16_t *__restrict__ out, float *__restrict__ lse,
                                                   int nsplit, int round_mode) {
+    // Launched as a programmatic dependent of the split kernel: wait here
+    // until that grid has completed and its partials are visible.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int64_t r = blockIdx.x;
     const int e = threadIdx.x;
     const float *ls = lse_parts + r * nsplit;
@@ -462,9 +467,21 @@ cudaError_t launch_decode(const CUtensorMap &mk, const CUtensorMap &mv, const De
 
 cudaError_t launch_lse_merge(const float *o_parts, const float *lse_parts, void *out, float *lse, int rows,
                              int nsplit, int round_mode, cudaStream_t stream) {
-    dec::merge_kernel<<<rows, dec::D, 0, stream>>>(o_parts, lse_parts, static_cast<uint16_t *>(out), lse, nsplit,
-                                                   round_mode);
-    return cudaGetLastError();
+    // Programmatic dependent launch: the merge CTAs are scheduled while the
+    // previous kernel on the stream finishes and wait (griddepcontrol.wait)
+    // for its results, so the launch gap between the two is hidden.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)rows);
+    cfg.blockDim = dim3(dec::D);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, dec::merge_kernel, o_parts, lse_parts, static_cast<uint16_t *>(out), lse, nsplit,
+                              round_mode);
 }
 
 }  // namespace attn

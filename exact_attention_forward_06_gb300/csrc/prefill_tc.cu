@@ -722,6 +722,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
     ptx::tc_fence_before();
     __syncthreads();
+    // A dependent merge kernel may be scheduled now; it waits for this grid.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (warp == 1) {
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem_base, 512);
@@ -787,6 +789,9 @@ namespace g1 {
 // the key-range partials in part order (deterministic) and write the row of O
 // in q's layout, rounded to bf16, and its log-sum-exp.
 __global__ void __launch_bounds__(D) merge_kernel(__nv_bfloat16 *__restrict__ out, const PrefillParams p) {
+    // Launched as a programmatic dependent of the prefill kernel: wait here
+    // until that grid has completed and its partials are visible.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int row = blockIdx.x;  // within the split units
     const int su = row / (2 * BM);
     const int t = (row / BM) & 1;
@@ -817,8 +822,19 @@ __global__ void __launch_bounds__(D) merge_kernel(__nv_bfloat16 *__restrict__ ou
 
 cudaError_t launch_prefill_merge(void *out, const PrefillParams &p, cudaStream_t stream) {
     if (p.split_units == 0) return cudaSuccess;
-    g1::merge_kernel<<<p.split_units * 2 * g1::BM, g1::D, 0, stream>>>(static_cast<__nv_bfloat16 *>(out), p);
-    return cudaGetLastError();
+    // Programmatic dependent launch (see launch_lse_merge): the merge CTAs are
+    // scheduled while the prefill's last CTAs finish.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(p.split_units * 2 * g1::BM));
+    cfg.blockDim = dim3(g1::D);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, g1::merge_kernel, static_cast<__nv_bfloat16 *>(out), p);
 }
 
 }  // namespace attn
