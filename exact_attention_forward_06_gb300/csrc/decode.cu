@@ -163,6 +163,9 @@ __global__ void __launch_bounds__(NTHREADS, 3)
         if (lane == 0) {
             ptx::prefetch_tensormap(&map_k);
             ptx::prefetch_tensormap(&map_v);
+            // Each cache page is read once per step: evict-first keeps the
+            // stream from pushing other work's data out of L2.
+            const uint64_t pol = ptx::policy_evict_first();
             int issued = 0;
             for (int i = 0; i < np; ++i) {
                 const int slot = i % NST;
@@ -177,8 +180,8 @@ __global__ void __launch_bounds__(NTHREADS, 3)
                 } else {
                     stage_bad[slot] = 0;
                     ptx::mbar_arrive_expect_tx(full + slot, STAGE_BYTES);
-                    ptx::tma_load_3d(dst, &map_k, full + slot, 0, g, phys * PAGE);
-                    ptx::tma_load_3d(dst + PAGE_BYTES, &map_v, full + slot, 0, g, phys * PAGE);
+                    ptx::tma_load_3d_hint(dst, &map_k, full + slot, 0, g, phys * PAGE, pol);
+                    ptx::tma_load_3d_hint(dst + PAGE_BYTES, &map_v, full + slot, 0, g, phys * PAGE, pol);
                 }
                 ++issued;
             }

@@ -637,8 +637,11 @@ __device__ void softmax_wg(const PrefillParams &p, const Unit &w, const SmemLayo
     } else if (quarter == 0 && lane == 0 && s0 < w.Sq && w.part < 0 && !*wc.abort_flag) {
         const Coord4 lo = coord4(p.bhsd, 0, head, w.q0 + s0, w.tb);
         const Coord4 hi = coord4(p.bhsd, 64, head, w.q0 + s0, w.tb);
-        ptx::tma_store_4d(mo, stage, lo.c0, lo.c1, lo.c2, lo.c3);
-        ptx::tma_store_4d(mo, stage + HALF_BYTES, hi.c0, hi.c1, hi.c2, hi.c3);
+        // O is written once and not read again here: evict-first, so its dirty
+        // lines leave L2 early instead of crowding out K/V and later work.
+        const uint64_t pol_o = ptx::policy_evict_first();
+        ptx::tma_store_4d_hint(mo, stage, lo.c0, lo.c1, lo.c2, lo.c3, pol_o);
+        ptx::tma_store_4d_hint(mo, stage + HALF_BYTES, hi.c0, hi.c1, hi.c2, hi.c3, pol_o);
         ptx::bulk_commit_group();
         ptx::bulk_wait_group_read0();
     }
