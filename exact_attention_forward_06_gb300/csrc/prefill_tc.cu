@@ -252,49 +252,74 @@ __device__ void producer(const PrefillParams &p, const Unit &w, const SmemLayout
     load_tile(mq, sm.q_tile(1), sm.q_full(), p.bhsd, w.h[1], w.q0 + w.s0[1], w.tb, pol_q);
     const int total = 2 * w.n_kv;
     int issued = 0;
-    int page_row[BN / 16];  // paged K/V: first pool row of each page of the current tile
     for (int n = 0; n < total; ++n) {
         const int slot = n % NSLOT;
         const int round = n / NSLOT;
-        if (p.block_table != nullptr && (n & 1) == 0) {
-            // The tile's eight pages (read before waiting for the slot, so the
-            // table loads overlap the wait).  Pages past the sequence's last
-            // one, and bad entries (reported), get a row past the pool: the
-            // copy then fills zeros.
-            const int page0 = (w.j_lo + (n >> 1)) * (BN / 16);
-            const int n_pages = (w.Sk + 15) / 16;
-            const int *row = p.block_table + (int64_t)w.b * p.max_blocks;
-#pragma unroll
-            for (int i = 0; i < BN / 16; ++i) {
-                const int phys = page0 + i < n_pages ? row[page0 + i] : -1;
-                const bool ok_page = phys >= 0 && phys < p.num_pages;
-                if (!ok_page && page0 + i < n_pages) report_status(p.status, kStatusDeviceBounds, kSitePagedTable);
-                page_row[i] = ok_page ? phys * 16 : p.num_pages * 16;
-            }
-        }
         if (round > 0 && !wait_bounded(sm.kv_empty(slot), (round - 1) & 1, wc, kSiteProducerEmpty)) break;
         ptx::mbar_arrive_expect_tx(sm.kv_full(slot), TILE_BYTES);
-        if (p.block_table != nullptr) {
-            // One 16-row box per page and half: page i fills rows 16i .. 16i+15
-            // of the tile (2 KiB per half, 1024-byte aligned, so the 128-byte
-            // swizzle matches the one a single 128-row box would give).
-            const CUtensorMap *map = (n & 1) ? mv : mk;
-            uint8_t *dst = sm.slot(slot);
-#pragma unroll
-            for (int i = 0; i < BN / 16; ++i) {
-                ptx::tma_load_3d_hint(dst + i * 2048, map, sm.kv_full(slot), 0, w.g, page_row[i], pol_kv);
-                ptx::tma_load_3d_hint(dst + HALF_BYTES + i * 2048, map, sm.kv_full(slot), 64, w.g, page_row[i],
-                                      pol_kv);
-            }
-        } else {
-            load_tile((n & 1) ? mv : mk, sm.slot(slot), sm.kv_full(slot), p.bhsd, w.g,
-                      w.k0 + (w.j_lo + (n >> 1)) * BN, w.tb, pol_kv);
-        }
+        load_tile((n & 1) ? mv : mk, sm.slot(slot), sm.kv_full(slot), p.bhsd, w.g, w.k0 + (w.j_lo + (n >> 1)) * BN,
+                  w.tb, pol_kv);
         ++issued;
     }
     // On the way out make sure no copy is still writing into shared memory.
     drain_wait(sm.q_full(), 0, wc);
     for (int n = max(0, issued - NSLOT); n < issued; ++n) drain_wait(sm.kv_full(n % NSLOT), (n / NSLOT) & 1, wc);
+}
+
+// Paged K/V: the whole warp 0 produces.  A K/V tile is 8 pages; lane i < 8
+// reads table entry i of the tile and issues the two 16-row boxes (one per
+// 64-column half) of page i, so the table loads and the 32 copies of a tile
+// pair go out in parallel instead of one after another from a single lane.
+// Lane 0 arms each barrier before any lane issues into it.  Pages past the
+// sequence's last one, and bad entries (reported), get a row past the pool:
+// the copy then fills zeros.
+__device__ void producer_paged(const PrefillParams &p, const Unit &w, const SmemLayout &sm, const WaitCtx &wc,
+                               int lane, const CUtensorMap *mq, const CUtensorMap *mk, const CUtensorMap *mv) {
+    if (p.inject == 1 || w.n_kv == 0) return;
+    const uint64_t pol_q = ptx::policy_evict_first();
+    const uint64_t pol_kv = ptx::policy_evict_last();
+    if (lane == 0) {
+        ptx::mbar_arrive_expect_tx(sm.q_full(), 2 * TILE_BYTES);
+        load_tile(mq, sm.q_tile(0), sm.q_full(), p.bhsd, w.h[0], w.q0 + w.s0[0], w.tb, pol_q);
+        load_tile(mq, sm.q_tile(1), sm.q_full(), p.bhsd, w.h[1], w.q0 + w.s0[1], w.tb, pol_q);
+    }
+    const int total = 2 * w.n_kv;
+    const int n_pages = (w.Sk + 15) / 16;
+    const int *row = p.block_table + (int64_t)w.b * p.max_blocks;
+    int issued = 0;
+    int page_row = p.num_pages * 16;  // this lane's page of the current tile (lanes < 8)
+    for (int n = 0; n < total; ++n) {
+        const int slot = n % NSLOT;
+        const int round = n / NSLOT;
+        if ((n & 1) == 0 && lane < BN / 16) {
+            const int page = (w.j_lo + (n >> 1)) * (BN / 16) + lane;
+            const int phys = page < n_pages ? row[page] : -1;
+            const bool ok_page = phys >= 0 && phys < p.num_pages;
+            if (!ok_page && page < n_pages) report_status(p.status, kStatusDeviceBounds, kSitePagedTable);
+            page_row = ok_page ? phys * 16 : p.num_pages * 16;
+        }
+        bool ok = true;
+        if (lane == 0) {
+            ok = round == 0 || wait_bounded(sm.kv_empty(slot), (round - 1) & 1, wc, kSiteProducerEmpty);
+            if (ok) ptx::mbar_arrive_expect_tx(sm.kv_full(slot), TILE_BYTES);
+        }
+        if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+        if (lane < BN / 16) {
+            // Page `lane` fills rows 16 lane .. 16 lane + 15 of the tile (2 KiB
+            // per half, 1024-byte aligned, so the 128-byte swizzle matches the
+            // one a single 128-row box gives).
+            const CUtensorMap *map = (n & 1) ? mv : mk;
+            uint8_t *dst = sm.slot(slot) + lane * 2048;
+            ptx::tma_load_3d_hint(dst, map, sm.kv_full(slot), 0, w.g, page_row, pol_kv);
+            ptx::tma_load_3d_hint(dst + HALF_BYTES, map, sm.kv_full(slot), 64, w.g, page_row, pol_kv);
+        }
+        issued = n + 1;
+    }
+    // On the way out make sure no copy is still writing into shared memory.
+    if (lane == 0) {
+        drain_wait(sm.q_full(), 0, wc);
+        for (int n = max(0, issued - NSLOT); n < issued; ++n) drain_wait(sm.kv_full(n % NSLOT), (n / NSLOT) & 1, wc);
+    }
 }
 
 // ------------------------------------------------------------------ MMA issuer
@@ -702,7 +727,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (warp < 4) {
         ptx::setmaxnreg_dec<REGS_CONTROL>();
         if (warp == 0) {
-            if (lane == 0) producer(p, w, sm, wc, &map_q, &map_k, &map_v);
+            if (p.block_table != nullptr)
+                producer_paged(p, w, sm, wc, lane, &map_q, &map_k, &map_v);
+            else if (lane == 0)
+                producer(p, w, sm, wc, &map_q, &map_k, &map_v);
         } else if (warp == 1 || warp == 2) {
             if (lane == 0) {
                 if (warp == 1)
