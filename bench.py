@@ -425,7 +425,41 @@ def run_decode_append(A, wd, lens_h, dev, stream, args):
             "algorithmic": f"{kv_bytes} B K+V per launch (L+1 keys per sequence)"}
 
 
+def run_e2e_host(A, case, dev, stream, args):
+    """End to end through attn_fwd_host: pinned host inputs in, pinned host
+    outputs back, the library's own chunked copy/compute overlap inside."""
+    w = case.w
+    q, k, v = (t.pin_memory() for t in case.host)
+    out_h = torch.empty(q.shape, dtype=torch.bfloat16).pin_memory()
+    lse_h = torch.empty(case.lse_shape, dtype=torch.float32).pin_memory()
+    ws = torch.empty(A.fwd_host_workspace_bytes(w.B, w.Hq, w.Hkv, w.Sq, w.Sk, w.d), device=dev, dtype=torch.uint8)
+
+    def step():
+        A.fwd_host(q, k, v, causal=w.causal, scale=w.scale, layout=w.layout, out=out_h, lse=lse_h, workspace=ws,
+                   stream=stream)
+
+    for _ in range(max(1, args.warmup)):
+        step()
+    torch.cuda.synchronize(dev)
+    n = max(1, args.steps // 2)
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    s.record(stream)
+    for _ in range(n):
+        step()
+    e.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = reduce_max_over_ranks(s.elapsed_time(e) / n)
+    h2d = sum(t.numel() * t.element_size() for t in (q, k, v))
+    d2h = out_h.numel() * out_h.element_size() + lse_h.numel() * lse_h.element_size()
+    return {"value": round(_world() * case.flops / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 4),
+            "api": "exact_attention_forward_06_gb300.fwd_host (C ABI attn_fwd_host: pinned host buffers in and out)"}
+
+
 def run_e2e(A, case, dev, stream, args):
+    if isinstance(case, DenseCase):
+        return run_e2e_host(A, case, dev, stream, args)
     pinned = [t.pin_memory() for t in case.host]
     dev_in = [torch.empty_like(t, device=dev) for t in pinned]
     out_h = torch.empty_like(pinned[0]).pin_memory()

@@ -52,6 +52,10 @@ def load():
             lib.attn_fwd.argtypes = fwd_args
             lib.attn_fwd_simple.argtypes = fwd_args
             lib.attn_fwd_rounded.argtypes = fwd_args[:-1] + [_i, _p]
+            lib.attn_fwd_host.argtypes = fwd_args[:-1] + [_i, _p, _sz, _p]
+            lib.attn_fwd_host.restype = _i
+            lib.attn_fwd_host_workspace_bytes.argtypes = [_i, _i, _i, _i, _i, _i]
+            lib.attn_fwd_host_workspace_bytes.restype = _sz
             lib.attn_fwd_varlen.argtypes = [_p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _i, _i, _f,
                                             _i, _p]
             lib.attn_fwd_paged.argtypes = [_p, _p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _i, _i, _i,
@@ -163,6 +167,48 @@ def fwd(q, k, v, *, causal=False, scale=None, layout="bshd", out=None, lse=None,
     if rounding not in ROUNDING:
         raise ValueError(f"rounding must be one of {sorted(ROUNDING)}, got {rounding!r}")
     return _fwd_call("attn_fwd", q, k, v, causal, scale, layout, out, lse, stream, rounding)
+
+
+def fwd_host_workspace_bytes(B: int, Hq: int, Hkv: int, Sq: int, Sk: int, d: int = 128) -> int:
+    """Device workspace bytes fwd_host needs for this shape."""
+    return int(load().attn_fwd_host_workspace_bytes(B, Hq, Hkv, Sq, Sk, d))
+
+
+def fwd_host(q, k, v, *, causal=False, scale=None, layout="bshd", out=None, lse=None, workspace=None, stream=None,
+             rounding="rtne"):
+    """The forward pass from and to host memory (C entry point attn_fwd_host).
+
+    q, k, v: CPU bf16 tensors (pin them for asynchronous copies); out/lse: CPU
+    tensors to write (allocated pinned when omitted; ``lse=False`` skips it).
+    workspace: a CUDA uint8 tensor of at least fwd_host_workspace_bytes(...)
+    bytes (allocated when omitted).  Returns (out, lse); they are complete once
+    ``stream`` (default: the current stream) has reached this point.
+    """
+    lib = load()
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        if t.device.type != "cpu" or t.dtype != torch.bfloat16 or not t.is_contiguous():
+            raise ValueError(f"{n} must be a contiguous CPU bfloat16 tensor")
+    if rounding not in ROUNDING:
+        raise ValueError(f"rounding must be one of {sorted(ROUNDING)}, got {rounding!r}")
+    if k.shape != v.shape:
+        raise ValueError("k and v must have the same shape")
+    B, Hq, Hkv, Sq, Sk, d = _dims(q, k, layout)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty(q.shape, dtype=torch.bfloat16).pin_memory()
+    if lse is None:
+        lse = torch.empty((B, Hq, Sq), dtype=torch.float32).pin_memory()
+    need = fwd_host_workspace_bytes(B, Hq, Hkv, Sq, Sk, d)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), device="cuda", dtype=torch.uint8)
+    _dev_tensor(workspace, "workspace", torch.uint8)
+    lse_ptr = None if lse is False else lse.data_ptr()
+    rc = lib.attn_fwd_host(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse_ptr, B, Hq, Hkv, Sq, Sk, d,
+                           LAYOUTS[layout], int(bool(causal)), float(scale), ROUNDING[rounding], workspace.data_ptr(),
+                           workspace.numel(), _stream(stream))
+    _check(rc, "attn_fwd_host")
+    return out, (None if lse is False else lse)
 
 
 def fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, *, max_seqlen_q=None, max_seqlen_k=None, causal=False,

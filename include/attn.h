@@ -177,6 +177,34 @@ attn_status_t attn_fwd_paged(const void *q, const void *k_pages, const void *v_p
                              int causal, float scale, int round_mode, void *stream);
 
 /*
+ * attn_fwd_host -- attn_fwd_rounded from and to HOST memory.
+ *
+ * q, k, v: host bf16 in `layout`, shapes as attn_fwd (read).
+ * out: host bf16, q's shape (written); lse: host fp32 [B][Hq][Sq] or NULL.
+ * Host buffers should be page-locked (cudaHostAlloc / pinned): the copies
+ * are asynchronous only then.
+ * workspace: DEVICE buffer of at least attn_fwd_host_workspace_bytes(...)
+ *      bytes, 256-byte aligned, owned by the caller; it stages q, k, v, out
+ *      and lse on the device (contents undefined afterwards).
+ * The copies in, the forward kernel and the copies out run in batch chunks
+ * on three library-owned helper streams (created once per device), so the
+ * copies of one chunk overlap the compute of another; the call is ordered
+ * after earlier work on `stream`, and later work on `stream` waits for it
+ * (event dependencies both ways).  The result is the same as copying in,
+ * calling attn_fwd_rounded on the whole batch and copying out, except that
+ * each chunk of batches is its own launch (so a tail split, if a workspace is
+ * registered, may differ).  Errors: those of attn_fwd (checked before any
+ * copy), ATTN_ERR_WORKSPACE for a missing, misaligned or small workspace.
+ */
+attn_status_t attn_fwd_host(const void *q, const void *k, const void *v, void *out, float *lse,
+                            int B, int Hq, int Hkv, int Sq, int Sk, int d,
+                            int layout, int causal, float scale, int round_mode,
+                            void *workspace, size_t workspace_bytes, void *stream);
+
+/* Device workspace attn_fwd_host needs for this shape (0 if invalid). */
+size_t attn_fwd_host_workspace_bytes(int B, int Hq, int Hkv, int Sq, int Sk, int d);
+
+/*
  * attn_fwd_workspace_bytes -- device workspace that lets attn_fwd split the
  * key ranges of its last wave of work units (the Flash-Decoding style tail
  * split of the MoonMath page: the partial results are merged by log-sum-exp)

@@ -181,3 +181,18 @@ def test_decode_append_rejects_bad_arguments(lib):
     bad = list(args)
     bad[17] = None                                                              # workspace
     assert lib.attn_decode_paged_append(*bad) == 5
+
+
+def test_fwd_host_rejects_bad_arguments_before_any_copy(lib):
+    args = [16, 16, 16, 16, None, 2, 4, 2, 64, 64, 128, 0, 1, 0.1, 0, 256, 1 << 30, None]
+    assert lib.attn_fwd_host(None, *args[1:]) == 1
+    bad = list(args); bad[10] = 64
+    assert lib.attn_fwd_host(*bad) == 2
+    bad = list(args); bad[15] = None
+    assert lib.attn_fwd_host(*bad) == 5
+    bad = list(args); bad[16] = 1024                       # too small
+    assert lib.attn_fwd_host(*bad) == 5
+    bad = list(args); bad[11] = 3                          # layout
+    assert lib.attn_fwd_host(*bad) == 1
+    assert lib.attn_fwd_host_workspace_bytes(2, 4, 2, 64, 64, 128) > 0
+    assert lib.attn_fwd_host_workspace_bytes(2, 3, 2, 64, 64, 128) == 0
