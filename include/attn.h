@@ -28,7 +28,8 @@
  *
  * Conventions for every entry point:
  *   - Pointers named q, k, v, out, lse, k_pages, v_pages, block_table, seqlens,
- *     workspace, o_parts, lse_parts are DEVICE pointers owned by the caller;
+ *     workspace, o_parts, lse_parts are DEVICE pointers owned by the caller
+ *     (except attn_fwd_host, whose q, k, v, out and lse are host pointers);
  *     the library never frees them and keeps none past the call, except the
  *     workspace registered with attn_set_workspace.  The library allocates no
  *     device memory on any call.
@@ -36,6 +37,8 @@
  *     enqueued asynchronously; only attn_get_device_status synchronises.
  *   - bf16 tensors are dense and contiguous; every device pointer must be
  *     16-byte aligned.
+ *   - attn_fwd_host creates three streams and a few events per device on its
+ *     first call and keeps them; no other entry point creates CUDA objects.
  *   - Arguments are validated before anything is launched; a rejected call
  *     returns ATTN_ERR_INVALID_ARG or ATTN_ERR_UNSUPPORTED and enqueues nothing.
  *   - A kernel that gives up on a bounded wait (see attn_set_wait_budget_ns)
