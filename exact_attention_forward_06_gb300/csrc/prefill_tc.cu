@@ -327,7 +327,7 @@ __device__ void producer_paged(const PrefillParams &p, const Unit &w, const Smem
 // The issue path is kept to a few integer operations per MMA: each operand
 // descriptor is built once per tile and every k-step adds a compile-time
 // offset (the start-address field is the low 14 bits, and no step carries out
-// of it), so the single issuing thread keeps up with the tensor core.
+// of it), so an issuing thread keeps up with the tensor core.
 __device__ __forceinline__ void issue_s(uint32_t tmem_s, uint64_t q_desc, uint64_t k_desc) {
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) {
