@@ -121,12 +121,12 @@ bool make_map_pool(CUtensorMap *m, const void *ptr, int num_pages, int Hkv, int 
 
 // 3-D map over a page pool [P][16][Hkv][d] for the tensor-core prefill:
 // dims {d, Hkv, 16P}, box = 64 head-dim elements (128 B, 128-byte swizzle) x
-// one page of one KV head (16 rows).
-bool make_map_pool_sw128(CUtensorMap *m, const void *ptr, int num_pages, int Hkv, int d) {
+// `rows` pool rows of one KV head (16: one page; 128: a run of 8 pages).
+bool make_map_pool_sw128(CUtensorMap *m, const void *ptr, int num_pages, int Hkv, int d, int rows = 16) {
     const cuuint64_t e = 2;
     cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)Hkv, (cuuint64_t)num_pages * 16};
     cuuint64_t strides[2] = {(cuuint64_t)d * e, (cuuint64_t)Hkv * d * e};
-    cuuint32_t box[3] = {64, 1, 16};
+    cuuint32_t box[3] = {64, 1, (cuuint32_t)rows};
     const cuuint32_t es[3] = {1, 1, 1};
     CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box, es,
                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -228,7 +228,7 @@ attn_status_t attn_fwd_rounded(const void *q, const void *k, const void *v, void
             ctas = p.n_full_units + su * parts;
         }
     }
-    if (attn::launch_prefill(mq, mk, mv, mo, p, ctas, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    if (attn::launch_prefill(mq, mk, mv, mo, mk, mv, p, ctas, static_cast<cudaStream_t>(stream)) != cudaSuccess)
         return ATTN_ERR_CUDA;
     if (attn::launch_prefill_merge(out, p, static_cast<cudaStream_t>(stream)) != cudaSuccess) return ATTN_ERR_CUDA;
     return ATTN_OK;
@@ -271,7 +271,7 @@ attn_status_t attn_fwd_varlen(const void *q, const void *k, const void *v, void 
     if (!make_map_4d(&mq, q, false, 1, total_q, Hq, d, 128) || !make_map_4d(&mk, k, false, 1, total_k, Hkv, d, 128) ||
         !make_map_4d(&mv, v, false, 1, total_k, Hkv, d, 128) || !make_map_4d(&mo, out, false, 1, total_q, Hq, d, 128))
         return ATTN_ERR_CUDA;
-    if (attn::launch_prefill(mq, mk, mv, mo, p, (int)units, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    if (attn::launch_prefill(mq, mk, mv, mo, mk, mv, p, (int)units, static_cast<cudaStream_t>(stream)) != cudaSuccess)
         return ATTN_ERR_CUDA;
     return ATTN_OK;
 }
@@ -315,7 +315,11 @@ attn_status_t attn_fwd_paged(const void *q, const void *k_pages, const void *v_p
     if (!make_map_4d(&mq, q, false, 1, total_q, Hq, d, 128) || !make_map_pool_sw128(&mk, k_pages, num_pages, Hkv, d) ||
         !make_map_pool_sw128(&mv, v_pages, num_pages, Hkv, d) || !make_map_4d(&mo, out, false, 1, total_q, Hq, d, 128))
         return ATTN_ERR_CUDA;
-    if (attn::launch_prefill(mq, mk, mv, mo, p, (int)units, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    CUtensorMap mk8, mv8;
+    if (!make_map_pool_sw128(&mk8, k_pages, num_pages, Hkv, d, 128) ||
+        !make_map_pool_sw128(&mv8, v_pages, num_pages, Hkv, d, 128))
+        return ATTN_ERR_CUDA;
+    if (attn::launch_prefill(mq, mk, mv, mo, mk8, mv8, p, (int)units, static_cast<cudaStream_t>(stream)) != cudaSuccess)
         return ATTN_ERR_CUDA;
     return ATTN_OK;
 }

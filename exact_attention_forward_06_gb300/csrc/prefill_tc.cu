@@ -273,8 +273,12 @@ __device__ void producer(const PrefillParams &p, const Unit &w, const SmemLayout
 // Lane 0 arms each barrier before any lane issues into it.  Pages past the
 // sequence's last one, and bad entries (reported), get a row past the pool:
 // the copy then fills zeros.
+// When the tile's 8 pages are consecutive in the pool (an engine that hands a
+// sequence pages in order), lane 0 loads the tile with two 128-row boxes of
+// the run maps mk8/mv8 instead.
 __device__ void producer_paged(const PrefillParams &p, const Unit &w, const SmemLayout &sm, const WaitCtx &wc,
-                               int lane, const CUtensorMap *mq, const CUtensorMap *mk, const CUtensorMap *mv) {
+                               int lane, const CUtensorMap *mq, const CUtensorMap *mk, const CUtensorMap *mv,
+                               const CUtensorMap *mk8, const CUtensorMap *mv8) {
     if (p.inject == 1 || w.n_kv == 0) return;
     const uint64_t pol_q = ptx::policy_evict_first();
     const uint64_t pol_kv = ptx::policy_evict_last();
@@ -288,6 +292,7 @@ __device__ void producer_paged(const PrefillParams &p, const Unit &w, const Smem
     const int *row = p.block_table + (int64_t)w.b * p.max_blocks;
     int issued = 0;
     int page_row = p.num_pages * 16;  // this lane's page of the current tile (lanes < 8)
+    bool run = false;                 // the current tile's pages are one run in the pool
     for (int n = 0; n < total; ++n) {
         const int slot = n % NSLOT;
         const int round = n / NSLOT;
@@ -304,7 +309,19 @@ __device__ void producer_paged(const PrefillParams &p, const Unit &w, const Smem
             if (ok) ptx::mbar_arrive_expect_tx(sm.kv_full(slot), TILE_BYTES);
         }
         if (!__shfl_sync(0xffffffffu, ok, 0)) break;
-        if (lane < BN / 16) {
+        if ((n & 1) == 0) {
+            // (after the slot wait, which the table loads overlap)
+            const int first = __shfl_sync(0xffffffffu, page_row, 0);
+            const bool in_run = lane >= BN / 16 || (page_row == first + 16 * lane && first < p.num_pages * 16);
+            run = __all_sync(0xffffffffu, in_run);
+        }
+        if (run) {
+            if (lane == 0) {
+                const CUtensorMap *map = (n & 1) ? mv8 : mk8;
+                ptx::tma_load_3d_hint(sm.slot(slot), map, sm.kv_full(slot), 0, w.g, page_row, pol_kv);
+                ptx::tma_load_3d_hint(sm.slot(slot) + HALF_BYTES, map, sm.kv_full(slot), 64, w.g, page_row, pol_kv);
+            }
+        } else if (lane < BN / 16) {
             // Page `lane` fills rows 16 lane .. 16 lane + 15 of the tile (2 KiB
             // per half, 1024-byte aligned, so the 128-byte swizzle matches the
             // one a single 128-row box gives).
@@ -677,6 +694,7 @@ __device__ void softmax_wg(const PrefillParams &p, const Unit &w, const SmemLayo
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                    const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_o,
+                   const __grid_constant__ CUtensorMap map_k8, const __grid_constant__ CUtensorMap map_v8,
                    const PrefillParams p) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = ptx::smem_addr(smem_raw);
@@ -728,7 +746,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         ptx::setmaxnreg_dec<REGS_CONTROL>();
         if (warp == 0) {
             if (p.block_table != nullptr)
-                producer_paged(p, w, sm, wc, lane, &map_q, &map_k, &map_v);
+                producer_paged(p, w, sm, wc, lane, &map_q, &map_k, &map_v, &map_k8, &map_v8);
             else if (lane == 0)
                 producer(p, w, sm, wc, &map_q, &map_k, &map_v);
         } else if (warp == 1 || warp == 2) {
@@ -766,7 +784,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 int prefill_smem_bytes() { return (int)(g1::SMEM_TILES + g1::SMEM_MISC + g1::SMEM_ALIGN); }
 
 cudaError_t launch_prefill(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
-                           const CUtensorMap &mo, const PrefillParams &p, int num_ctas, cudaStream_t stream) {
+                           const CUtensorMap &mo, const CUtensorMap &mk8, const CUtensorMap &mv8,
+                           const PrefillParams &p, int num_ctas, cudaStream_t stream) {
     const int smem = prefill_smem_bytes();
     static thread_local int configured_device = -1;
     int dev = 0;
@@ -777,7 +796,7 @@ cudaError_t launch_prefill(const CUtensorMap &mq, const CUtensorMap &mk, const C
         if (e != cudaSuccess) return e;
         configured_device = dev;
     }
-    g1::prefill_kernel<<<num_ctas, g1::NUM_THREADS, smem, stream>>>(mq, mk, mv, mo, p);
+    g1::prefill_kernel<<<num_ctas, g1::NUM_THREADS, smem, stream>>>(mq, mk, mv, mo, mk8, mv8, p);
     return cudaGetLastError();
 }
 

@@ -49,8 +49,11 @@ struct PrefillParams {
 
 int prefill_smem_bytes();
 int prefill_num_units(const PrefillParams &p);
+// mk8/mv8: paged K/V only, maps over the pools with 128-row boxes (a run of 8
+// consecutive pages); pass mk/mv otherwise.
 cudaError_t launch_prefill(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
-                           const CUtensorMap &mo, const PrefillParams &p, int num_ctas, cudaStream_t stream);
+                           const CUtensorMap &mo, const CUtensorMap &mk8, const CUtensorMap &mv8,
+                           const PrefillParams &p, int num_ctas, cudaStream_t stream);
 // Merge of the tail-split partials into out (q's layout) and lse.
 cudaError_t launch_prefill_merge(void *out, const PrefillParams &p, cudaStream_t stream);
 // Tail-split plan for a shape on a device with num_sms SMs: split_units and

@@ -141,3 +141,26 @@ def test_full_workload_sampled_rows(A):
                                              Hkv=w.Hkv, Sq=Lq, Sk=Lk, causal=True, scale=w.scale)
         check_out(out[torch.from_numpy(q0 + rows[:, 2]), torch.from_numpy(rows[:, 1])], ref_o, f"paged seq {b}")
         check_lse(lse[torch.from_numpy(rows[:, 1]), torch.from_numpy(q0 + rows[:, 2])], ref_l, f"paged seq {b}")
+
+
+def test_runs_of_consecutive_pages_mixed_with_scattered_ones(A):
+    # A tile whose 8 table entries are consecutive pool pages is loaded as one
+    # run; here some tiles are runs, some have one page out of order, and one
+    # run ends at the last page of the pool.
+    w = inputs.PagedPrefillWorkload("runs", 3, 8, 2, chunks=(100, 300, 129), contexts=(412, 1000, 127), seed=106,
+                                    max_blocks=96)
+    q, kp, vp, table, lens, cu_q = inputs.make_paged_prefill(w)
+    n_pages = [(int(L) + 15) // 16 for L in lens]
+    order = torch.arange(sum(n_pages), dtype=torch.int32)
+    t2 = torch.full_like(table, -1)
+    off = 0
+    for b, n in enumerate(n_pages):
+        t2[b, :n] = order[off:off + n]
+        off += n
+    t2[1, 10], t2[1, 11] = t2[1, 11].clone(), t2[1, 10].clone()     # one tile of sequence 1 is not a run
+    # keep the data of every (sequence, token): move pages to the new ids
+    kp2, vp2 = kp.clone(), vp.clone()
+    for b, n in enumerate(n_pages):
+        kp2[t2[b, :n].long()] = kp[table[b, :n].long()]
+        vp2[t2[b, :n].long()] = vp[table[b, :n].long()]
+    _run_and_compare(A, w, (q, kp2, vp2, t2, lens, cu_q), "paged runs")
