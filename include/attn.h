@@ -224,8 +224,9 @@ size_t attn_fwd_workspace_bytes(int B, int Hq, int Hkv, int Sq, int Sk, int d, i
  * cleared and never frees it.  attn_fwd splits only when a registered buffer
  * is at least attn_fwd_workspace_bytes(...) large; otherwise it runs every
  * unit whole, with the same result to within rounding.  The buffer is used by
- * every attn_fwd on the device: calls that overlap on the GPU must not share
- * one (give each stream its own, or order the streams).
+ * every attn_fwd, attn_fwd_rounded and attn_fwd_host on the device (a single
+ * registration per device): calls that may overlap on the GPU must not both
+ * split, so order their streams, or clear the registration while they run.
  */
 attn_status_t attn_set_workspace(void *ptr, size_t bytes);
 
