@@ -171,6 +171,8 @@ attn_status_t fill_prefill_params(attn::PrefillParams *p, const DeviceInfo *di, 
     p->inject = 0;
     p->round_mode = ATTN_ROUND_RTNE;
     p->n_full_units = attn::prefill_num_units(*p);
+    // L2 prefetch of the next wave's Q for short non-causal units (few K/V tiles).
+    p->prefetch_ahead = (!causal && Sk <= 1024) ? di->sm_count : 0;
     p->split_units = 0;
     p->split_parts = 1;
     p->ws_o = nullptr;
@@ -259,6 +261,7 @@ attn_status_t attn_fwd_varlen(const void *q, const void *k, const void *v, void 
     fill_prefill_params(&p, di, lse, B, Hq, Hkv, max_seqlen_q, max_seqlen_k, ATTN_LAYOUT_BSHD, causal, scale);
     p.round_mode = round_mode;
     p.cu_q = cu_seqlens_q;
+    p.prefetch_ahead = 0;  // (dense coordinates only)
     p.cu_k = cu_seqlens_k;
     p.total_q = total_q;
     p.total_k = total_k;
@@ -301,6 +304,7 @@ attn_status_t attn_fwd_paged(const void *q, const void *k_pages, const void *v_p
                         scale);
     p.round_mode = round_mode;
     p.cu_q = cu_seqlens_q;
+    p.prefetch_ahead = 0;  // (dense coordinates only)
     p.total_q = total_q;
     p.out = out;
     p.block_table = block_table;

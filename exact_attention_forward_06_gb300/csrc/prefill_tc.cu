@@ -250,6 +250,18 @@ __device__ void producer(const PrefillParams &p, const Unit &w, const SmemLayout
     ptx::mbar_arrive_expect_tx(sm.q_full(), 2 * TILE_BYTES);
     load_tile(mq, sm.q_tile(0), sm.q_full(), p.bhsd, w.h[0], w.q0 + w.s0[0], w.tb, pol_q);
     load_tile(mq, sm.q_tile(1), sm.q_full(), p.bhsd, w.h[1], w.q0 + w.s0[1], w.tb, pol_q);
+    if (p.prefetch_ahead > 0 && (int)blockIdx.x + p.prefetch_ahead < p.n_full_units) {
+        // Short units (few K/V tiles) spend much of their time loading Q:
+        // start the Q of the unit about one wave ahead into L2, so the CTA
+        // that gets it finds it there.
+        const Unit nx = unit_coords(p, (int)blockIdx.x + p.prefetch_ahead);
+        for (int t = 0; t < 2; ++t) {
+            const Coord4 lo = coord4(p.bhsd, 0, t ? nx.h[1] : nx.h[0], t ? nx.s0[1] : nx.s0[0], nx.b);
+            const Coord4 hi = coord4(p.bhsd, 64, t ? nx.h[1] : nx.h[0], t ? nx.s0[1] : nx.s0[0], nx.b);
+            ptx::tma_prefetch_4d(mq, lo.c0, lo.c1, lo.c2, lo.c3);
+            ptx::tma_prefetch_4d(mq, hi.c0, hi.c1, hi.c2, hi.c3);
+        }
+    }
     const int total = 2 * w.n_kv;
     int issued = 0;
     for (int n = 0; n < total; ++n) {

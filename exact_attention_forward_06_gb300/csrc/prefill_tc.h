@@ -24,6 +24,7 @@ struct PrefillParams {
     // split_units units is cut into split_parts key ranges, one CTA each, whose
     // fp32 partials go to ws_o [split_units*256][split_parts][128] and
     // ws_lse [split_units*256][split_parts] and are merged afterwards.
+    int prefetch_ahead;  // > 0: L2-prefetch the Q tiles of the unit this many CTAs ahead
     int n_full_units;
     int split_units;
     int split_parts;
