@@ -23,8 +23,6 @@ __device__ __forceinline__ uint64_t globaltimer() {
     return t;
 }
 
-__device__ __forceinline__ uint32_t elect_lane0(uint32_t lane) { return lane == 0; }
-
 // ---------------------------------------------------------------- mbarrier
 
 __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
@@ -95,15 +93,6 @@ __device__ __forceinline__ void tma_load_3d_hint(void *dst, const CUtensorMap *m
         : "memory");
 }
 
-__device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, uint64_t *bar, int c0, int c1,
-                                            int c2) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_addr(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_addr(bar)), "r"(c0), "r"(c1), "r"(c2)
-        : "memory");
-}
-
 // 4-D tiled load global -> shared with an L2 cache-policy hint.
 __device__ __forceinline__ void tma_load_4d(void *dst, const CUtensorMap *map, uint64_t *bar, int c0, int c1,
                                             int c2, int c3, uint64_t policy) {
@@ -122,15 +111,6 @@ __device__ __forceinline__ void tma_store_4d_hint(const CUtensorMap *map, const 
         "cp.async.bulk.tensor.4d.global.shared::cta.tile.bulk_group.L2::cache_hint [%0, {%2, %3, %4, %5}], [%1], %6;" ::"l"(
             reinterpret_cast<uint64_t>(map)),
         "r"(smem_addr(src)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "l"(policy)
-        : "memory");
-}
-
-__device__ __forceinline__ void tma_store_4d(const CUtensorMap *map, const void *src, int c0, int c1, int c2,
-                                             int c3) {
-    asm volatile(
-        "cp.async.bulk.tensor.4d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4, %5}], [%1];" ::"l"(
-            reinterpret_cast<uint64_t>(map)),
-        "r"(smem_addr(src)), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
         : "memory");
 }
 
