@@ -28,6 +28,7 @@
 // shared memory and the split writes its normalised partial output and
 // log-sum-exp.  The merge kernel then combines the splits in a fixed order.
 #include <cstdint>
+#include <type_traits>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -208,11 +209,12 @@ __global__ void __launch_bounds__(NTHREADS, 3)
 #pragma unroll
             for (int e = 0; e < 8; ++e) qf[h][e] = __fmul2_rn(qf[h][e], sc2);
         }
-        float m[HG], lsum[HG];
+        float m[HG], lsum[HG], msub[HG];  // msub: m, or 0 while m is -inf
         float2 acc[HG][8];
 #pragma unroll
         for (int h = 0; h < HG; ++h) {
             m[h] = -INFINITY;
+            msub[h] = 0.f;
             lsum[h] = 0.f;
 #pragma unroll
             for (int e = 0; e < 8; ++e) acc[h][e] = make_float2(0.f, 0.f);
@@ -224,68 +226,77 @@ __global__ void __launch_bounds__(NTHREADS, 3)
             const uint8_t *vs = ks + PAGE_BYTES;
             const bool bad = stage_bad[slot] != 0;
             const int tok0 = (page0 + i) * PAGE;
-            float sc[4][HG];
-#pragma unroll
-            for (int ps = 0; ps < 4; ++ps) {
-                const int t = ps * 4 + tg;
-                const uint4 *kp = reinterpret_cast<const uint4 *>(ks + t * (D * 2));
-                float2 kf[8];
-                bf16x8_to_float2(kp[ds], kf);
-                bf16x8_to_float2(kp[8 + ds], kf + 4);
-#pragma unroll
-                for (int h = 0; h < HG; ++h) {
-                    float2 d2 = __fmul2_rn(qf[h][0], kf[0]);
-#pragma unroll
-                    for (int e = 1; e < 8; ++e) d2 = __ffma2_rn(qf[h][e], kf[e], d2);
-                    float dot = d2.x + d2.y;
-                    dot += __shfl_xor_sync(0xffffffffu, dot, 1);
-                    dot += __shfl_xor_sync(0xffffffffu, dot, 2);
-                    dot += __shfl_xor_sync(0xffffffffu, dot, 4);
-                    sc[ps][h] = (!bad && tok0 + t < L) ? dot : -INFINITY;
-                }
-            }
-            float pr[4][HG];
-#pragma unroll
-            for (int h = 0; h < HG; ++h) {
-                float pm = fmaxf(fmaxf(sc[0][h], sc[1][h]), fmaxf(sc[2][h], sc[3][h]));
-                pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 8));
-                pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 16));
-                if (pm > m[h] + RESCALE_LOG2) {  // warp-uniform
-                    const float alpha = ptx::ex2(m[h] - pm);
-                    lsum[h] *= alpha;
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) acc[h][e] = __fmul2_rn(acc[h][e], make_float2(alpha, alpha));
-                    m[h] = pm;
-                }
-                const float msub = (m[h] == -INFINITY) ? 0.f : m[h];
+            // A page whose 16 slots all hold keys of the sequence needs no
+            // masking: it takes a copy of the page step without the selects.
+            auto page_step = [&](auto full_tag) {
+                constexpr bool FULL = decltype(full_tag)::value;
+                float sc[4][HG];
 #pragma unroll
                 for (int ps = 0; ps < 4; ++ps) {
-                    pr[ps][h] = (sc[ps][h] == -INFINITY) ? 0.f : ptx::ex2(sc[ps][h] - msub);
-                    lsum[h] += pr[ps][h];
-                }
-            }
-            // Slots past the sequence end (and pages that could not be read)
-            // hold arbitrary bits: their P is 0, but 0 * NaN is NaN, so on
-            // such a page the V of invalid tokens is replaced by 0 as well.
-            const bool page_full = !bad && tok0 + PAGE <= L;
+                    const int t = ps * 4 + tg;
+                    const uint4 *kp = reinterpret_cast<const uint4 *>(ks + t * (D * 2));
+                    float2 kf[8];
+                    bf16x8_to_float2(kp[ds], kf);
+                    bf16x8_to_float2(kp[8 + ds], kf + 4);
 #pragma unroll
-            for (int ps = 0; ps < 4; ++ps) {
-                const int t = ps * 4 + tg;
-                const uint4 *vp = reinterpret_cast<const uint4 *>(vs + t * (D * 2));
-                float2 vf[8];
-                bf16x8_to_float2(vp[ds], vf);
-                bf16x8_to_float2(vp[8 + ds], vf + 4);
-                if (!page_full && (bad || tok0 + t >= L)) {
+                    for (int h = 0; h < HG; ++h) {
+                        float2 d2 = __fmul2_rn(qf[h][0], kf[0]);
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) vf[e] = make_float2(0.f, 0.f);
+                        for (int e = 1; e < 8; ++e) d2 = __ffma2_rn(qf[h][e], kf[e], d2);
+                        float dot = d2.x + d2.y;
+                        dot += __shfl_xor_sync(0xffffffffu, dot, 1);
+                        dot += __shfl_xor_sync(0xffffffffu, dot, 2);
+                        dot += __shfl_xor_sync(0xffffffffu, dot, 4);
+                        sc[ps][h] = (FULL || (!bad && tok0 + t < L)) ? dot : -INFINITY;
+                    }
                 }
+                float pr[4][HG];
 #pragma unroll
                 for (int h = 0; h < HG; ++h) {
-                    const float2 p2 = make_float2(pr[ps][h], pr[ps][h]);
+                    float pm = ptx::max3(sc[0][h], sc[1][h], fmaxf(sc[2][h], sc[3][h]));
+                    pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 8));
+                    pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 16));
+                    if (pm > m[h] + RESCALE_LOG2) {  // warp-uniform
+                        const float alpha = ptx::ex2(m[h] - pm);
+                        lsum[h] *= alpha;
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) acc[h][e] = __ffma2_rn(p2, vf[e], acc[h][e]);
+                        for (int e = 0; e < 8; ++e) acc[h][e] = __fmul2_rn(acc[h][e], make_float2(alpha, alpha));
+                        m[h] = pm;
+                        msub[h] = pm;
+                    }
+#pragma unroll
+                    for (int ps = 0; ps < 4; ++ps) {
+                        // a masked score (-inf) gives ex2(-inf) = 0 with no select
+                        pr[ps][h] = ptx::ex2(sc[ps][h] - msub[h]);
+                        lsum[h] += pr[ps][h];
+                    }
                 }
-            }
+                // Slots past the sequence end (and pages that could not be
+                // read) hold arbitrary bits: their P is 0, but 0 * NaN is NaN,
+                // so on such a page the V of invalid tokens is replaced by 0.
+#pragma unroll
+                for (int ps = 0; ps < 4; ++ps) {
+                    const int t = ps * 4 + tg;
+                    const uint4 *vp = reinterpret_cast<const uint4 *>(vs + t * (D * 2));
+                    float2 vf[8];
+                    bf16x8_to_float2(vp[ds], vf);
+                    bf16x8_to_float2(vp[8 + ds], vf + 4);
+                    if (!FULL && (bad || tok0 + t >= L)) {
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) vf[e] = make_float2(0.f, 0.f);
+                    }
+#pragma unroll
+                    for (int h = 0; h < HG; ++h) {
+                        const float2 p2 = make_float2(pr[ps][h], pr[ps][h]);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) acc[h][e] = __ffma2_rn(p2, vf[e], acc[h][e]);
+                    }
+                }
+            };
+            if (!bad && tok0 + PAGE <= L)
+                page_step(std::true_type{});
+            else
+                page_step(std::false_type{});
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(empty + slot);
         }
