@@ -122,13 +122,20 @@ bool make_map_pool(CUtensorMap *m, const void *ptr, int num_pages, int Hkv, int 
 // 3-D map over a page pool [P][16][Hkv][d] for the tensor-core prefill:
 // dims {d, Hkv, 16P}, box = 64 head-dim elements (128 B, 128-byte swizzle) x
 // `rows` pool rows of one KV head (16: one page; 128: a run of 8 pages).
-bool make_map_pool_sw128(CUtensorMap *m, const void *ptr, int num_pages, int Hkv, int d, int rows = 16) {
-    const cuuint64_t e = 2;
-    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)Hkv, (cuuint64_t)num_pages * 16};
-    cuuint64_t strides[2] = {(cuuint64_t)d * e, (cuuint64_t)Hkv * d * e};
-    cuuint32_t box[3] = {64, 1, (cuuint32_t)rows};
-    const cuuint32_t es[3] = {1, 1, 1};
-    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box, es,
+// Page-pool map for the prefill: one box holds whole 16-row pages of one KV
+// head, both 64-column halves, ordered in shared memory as
+// [8-row group][half][8 rows][64 columns] (1 KiB per 8-row half, 128-byte
+// swizzle), so a 128-row tile is 8 boxes of 4 KiB (or one box of 16 row
+// groups for 8 consecutive pages).  Dims, innermost first: 64 columns, 8 rows
+// (stride Hkv*d*2), 2 halves (stride 128 B), row groups of 8 (stride
+// 8*Hkv*d*2), KV head (stride d*2).
+bool make_map_pool_groups(CUtensorMap *m, const void *ptr, int num_pages, int Hkv, int d, int groups) {
+    const cuuint64_t e = 2, row = (cuuint64_t)Hkv * d * e;
+    cuuint64_t dims[5] = {64, 8, 2, (cuuint64_t)num_pages * 2, (cuuint64_t)Hkv};
+    cuuint64_t strides[4] = {row, 64 * e, 8 * row, (cuuint64_t)d * e};
+    cuuint32_t box[5] = {64, 8, 2, (cuuint32_t)groups, 1};
+    const cuuint32_t es[5] = {1, 1, 1, 1, 1};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(ptr), dims, strides, box, es,
                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
@@ -316,12 +323,12 @@ attn_status_t attn_fwd_paged(const void *q, const void *k_pages, const void *v_p
     if (units > 0x7fffffff) return ATTN_ERR_INVALID_ARG;
     p.n_full_units = (int)units;
     CUtensorMap mq, mk, mv, mo;
-    if (!make_map_4d(&mq, q, false, 1, total_q, Hq, d, 128) || !make_map_pool_sw128(&mk, k_pages, num_pages, Hkv, d) ||
-        !make_map_pool_sw128(&mv, v_pages, num_pages, Hkv, d) || !make_map_4d(&mo, out, false, 1, total_q, Hq, d, 128))
+    if (!make_map_4d(&mq, q, false, 1, total_q, Hq, d, 128) || !make_map_pool_groups(&mk, k_pages, num_pages, Hkv, d, 2) ||
+        !make_map_pool_groups(&mv, v_pages, num_pages, Hkv, d, 2) || !make_map_4d(&mo, out, false, 1, total_q, Hq, d, 128))
         return ATTN_ERR_CUDA;
     CUtensorMap mk8, mv8;
-    if (!make_map_pool_sw128(&mk8, k_pages, num_pages, Hkv, d, 128) ||
-        !make_map_pool_sw128(&mv8, v_pages, num_pages, Hkv, d, 128))
+    if (!make_map_pool_groups(&mk8, k_pages, num_pages, Hkv, d, 16) ||
+        !make_map_pool_groups(&mv8, v_pages, num_pages, Hkv, d, 16))
         return ATTN_ERR_CUDA;
     if (attn::launch_prefill(mq, mk, mv, mo, mk8, mv8, p, (int)units, static_cast<cudaStream_t>(stream)) != cudaSuccess)
         return ATTN_ERR_CUDA;

@@ -59,6 +59,12 @@ constexpr int D = 128;           // head dim
 constexpr int NSLOT = 5;         // K/V ring slots
 constexpr uint32_t TILE_BYTES = BM * D * 2;  // 32 KiB (128 rows x 256 B)
 constexpr uint32_t HALF_BYTES = TILE_BYTES / 2;  // one 64-column half (128 B rows, 128-B swizzle)
+// Paged K/V tiles are laid out by 8-row group: [16 groups][2 halves][8 rows]
+// [128 B], so one page (two groups, both halves) is one contiguous 4 KiB box.
+// Row r, half h of such a tile is at (r / 8) * 2048 + h * 1024 + (r % 8) * 128.
+constexpr uint32_t PAGE_BOX_BYTES = 4096;
+constexpr uint32_t PG_GROUP_BYTES = 2048;  // one 8-row group, both halves
+constexpr uint32_t PG_HALF_BYTES = 1024;   // one 8-row group, one half
 constexpr int NUM_THREADS = 384;  // three warpgroups
 constexpr uint32_t REGS_CONTROL = 96;   // warpgroup 0: producer, MMA issuer
 constexpr uint32_t REGS_SOFTMAX = 200;  // warpgroups 1-2: softmax
@@ -327,20 +333,15 @@ __device__ void producer_paged(const PrefillParams &p, const Unit &w, const Smem
             const bool in_run = lane >= BN / 16 || (page_row == first + 16 * lane && first < p.num_pages * 16);
             run = __all_sync(0xffffffffu, in_run);
         }
+        // The pool maps are in 8-row groups (see the paged tile layout): a
+        // page is one 4 KiB box at group page_row / 8, a run one box of 16.
         if (run) {
-            if (lane == 0) {
-                const CUtensorMap *map = (n & 1) ? mv8 : mk8;
-                ptx::tma_load_3d_hint(sm.slot(slot), map, sm.kv_full(slot), 0, w.g, page_row, pol_kv);
-                ptx::tma_load_3d_hint(sm.slot(slot) + HALF_BYTES, map, sm.kv_full(slot), 64, w.g, page_row, pol_kv);
-            }
+            if (lane == 0)
+                ptx::tma_load_5d_hint(sm.slot(slot), (n & 1) ? mv8 : mk8, sm.kv_full(slot), 0, 0, 0, page_row / 8,
+                                      w.g, pol_kv);
         } else if (lane < BN / 16) {
-            // Page `lane` fills rows 16 lane .. 16 lane + 15 of the tile (2 KiB
-            // per half, 1024-byte aligned, so the 128-byte swizzle matches the
-            // one a single 128-row box gives).
-            const CUtensorMap *map = (n & 1) ? mv : mk;
-            uint8_t *dst = sm.slot(slot) + lane * 2048;
-            ptx::tma_load_3d_hint(dst, map, sm.kv_full(slot), 0, w.g, page_row, pol_kv);
-            ptx::tma_load_3d_hint(dst + HALF_BYTES, map, sm.kv_full(slot), 64, w.g, page_row, pol_kv);
+            ptx::tma_load_5d_hint(sm.slot(slot) + lane * PAGE_BOX_BYTES, (n & 1) ? mv : mk, sm.kv_full(slot), 0, 0, 0,
+                                  page_row / 8, w.g, pol_kv);
         }
         issued = n + 1;
     }
@@ -357,19 +358,25 @@ __device__ void producer_paged(const PrefillParams &p, const Unit &w, const Smem
 // descriptor is built once per tile and every k-step adds a compile-time
 // offset (the start-address field is the low 14 bits, and no step carries out
 // of it), so an issuing thread keeps up with the tensor core.
+// PAGED: K and V tiles in the 8-row-group layout of the page-pool loads.
+template <bool PAGED>
 __device__ __forceinline__ void issue_s(uint32_t tmem_s, uint64_t q_desc, uint64_t k_desc) {
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) {
-        const uint64_t off = (uint64_t)(((kk >> 2) * HALF_BYTES + (kk & 3) * 32) >> 4);
-        ptx::umma_ss(tmem_s, q_desc + off, k_desc + off, IDESC_S, kk > 0);
+        const uint64_t qoff = (uint64_t)(((kk >> 2) * HALF_BYTES + (kk & 3) * 32) >> 4);
+        const uint64_t koff =
+            PAGED ? (uint64_t)(((kk >> 2) * PG_HALF_BYTES + (kk & 3) * 32) >> 4) : qoff;
+        ptx::umma_ss(tmem_s, q_desc + qoff, k_desc + koff, IDESC_S, kk > 0);
     }
 }
 
+template <bool PAGED>
 __device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t tmem_p, uint64_t v_desc, uint32_t accumulate) {
 #pragma unroll
     for (int kk = 0; kk < BN / 16; ++kk) {
-        // 16 keys per step: 8 packed bf16x2 columns of P, 16 rows (2 x 1024-B atoms) of V.
-        ptx::umma_ts(tmem_o, tmem_p + kk * 8, v_desc + (uint64_t)((kk * 2048) >> 4), IDESC_PV,
+        // 16 keys per step: 8 packed bf16x2 columns of P, 16 rows (2 x 8-row atoms) of V.
+        const uint32_t step = PAGED ? 2 * PG_GROUP_BYTES : 2048;
+        ptx::umma_ts(tmem_o, tmem_p + kk * 8, v_desc + (uint64_t)((kk * step) >> 4), IDESC_PV,
                      kk > 0 ? 1u : accumulate);
     }
 }
@@ -390,7 +397,7 @@ __device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t tmem_p, uint6
 //   PV_t(j) needs P_t(j) (p_full[t]) and V_j.
 // A ring slot takes one release per stream (a commit after the stream's
 // product that reads it).
-template <int T>
+template <int T, bool PAGED>
 __device__ void mma_stream(const Unit &w, const SmemLayout &sm, const WaitCtx &wc, uint32_t tmem_base) {
     if (w.n_kv == 0) return;  // nothing to multiply (and no Q is loaded)
     if (!wait_spin(sm.q_full(), 0, wc, kSiteMmaQ)) return;
@@ -407,7 +414,11 @@ __device__ void mma_stream(const Unit &w, const SmemLayout &sm, const WaitCtx &w
         if (prev >= 0 && !wait_spin(sm.s_free(1 - T), (uint32_t)(prev & 1), wc, kSiteMmaPoll)) return false;
         if (!wait_spin(sm.kv_full(slot_of(item)), par_of(item), wc, kSiteMmaPoll)) return false;
         ptx::tc_fence_after();
-        issue_s(tmem_base + TM_S, q_desc, ptx::desc_kmajor_sw128(slot0 + slot_of(item) * TILE_BYTES));
+        const uint32_t k_addr = slot0 + slot_of(item) * TILE_BYTES;
+        // K-major, 128-byte swizzle; 8-row atoms 1 KiB apart, or 2 KiB in the paged layout
+        const uint64_t k_desc = PAGED ? ptx::smem_desc(k_addr, 16, PG_GROUP_BYTES, ptx::kLayoutSwizzle128B)
+                                      : ptx::desc_kmajor_sw128(k_addr);
+        issue_s<PAGED>(tmem_base + TM_S, q_desc, k_desc);
         ptx::umma_commit(sm.s_full(T));
         ptx::umma_commit(sm.kv_empty(slot_of(item)));  // this stream is done with K_j
         return true;
@@ -417,8 +428,12 @@ __device__ void mma_stream(const Unit &w, const SmemLayout &sm, const WaitCtx &w
         if (!wait_spin(sm.p_full(T), (uint32_t)(j & 1), wc, kSiteMmaPoll)) return false;
         if (!wait_spin(sm.kv_full(slot_of(item)), par_of(item), wc, kSiteMmaPoll)) return false;
         ptx::tc_fence_after();
-        issue_pv(tmem_base + tm_o(T), tmem_base + tm_p(T),
-                 ptx::desc_mnmajor_sw128(slot0 + slot_of(item) * TILE_BYTES, HALF_BYTES), j > 0 ? 1u : 0u);
+        const uint32_t v_addr = slot0 + slot_of(item) * TILE_BYTES;
+        // MN-major, 128-byte swizzle: the two 64-column halves HALF_BYTES apart
+        // and 8-key atoms 1 KiB apart, or 1 KiB and 2 KiB in the paged layout
+        const uint64_t v_desc = PAGED ? ptx::smem_desc(v_addr, PG_HALF_BYTES, PG_GROUP_BYTES, ptx::kLayoutSwizzle128B)
+                                      : ptx::desc_mnmajor_sw128(v_addr, HALF_BYTES);
+        issue_pv<PAGED>(tmem_base + tm_o(T), tmem_base + tm_p(T), v_desc, j > 0 ? 1u : 0u);
         ptx::umma_commit(sm.o_full(T));
         ptx::umma_commit(sm.kv_empty(slot_of(item)));  // this stream is done with V_j
         return true;
@@ -602,10 +617,13 @@ __device__ void softmax_wg(const PrefillParams &p, const Unit &w, const SmemLayo
             }
             if (kbase + r >= w.Sk) {
                 const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+                // row r, both halves (dense or paged tile layout)
+                uint8_t *h0 = p.block_table != nullptr ? vt + (r >> 3) * PG_GROUP_BYTES + (r & 7) * 128 : vt + r * 128;
+                uint8_t *h1 = h0 + (p.block_table != nullptr ? PG_HALF_BYTES : HALF_BYTES);
 #pragma unroll
                 for (int c = 0; c < 8; ++c) {
-                    reinterpret_cast<uint4 *>(vt + r * 128)[c] = z;
-                    reinterpret_cast<uint4 *>(vt + HALF_BYTES + r * 128)[c] = z;
+                    reinterpret_cast<uint4 *>(h0)[c] = z;
+                    reinterpret_cast<uint4 *>(h1)[c] = z;
                 }
             }
             ptx::fence_proxy_async_smem();
@@ -763,10 +781,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 producer(p, w, sm, wc, &map_q, &map_k, &map_v);
         } else if (warp == 1 || warp == 2) {
             if (lane == 0) {
+                const bool paged = p.block_table != nullptr;
                 if (warp == 1)
-                    mma_stream<0>(w, sm, wc, tmem_base);
+                    paged ? mma_stream<0, true>(w, sm, wc, tmem_base) : mma_stream<0, false>(w, sm, wc, tmem_base);
                 else
-                    mma_stream<1>(w, sm, wc, tmem_base);
+                    paged ? mma_stream<1, true>(w, sm, wc, tmem_base) : mma_stream<1, false>(w, sm, wc, tmem_base);
                 // Whatever happened, wait until every product issued (by
                 // either stream) has completed before tensor memory is released.
                 ptx::umma_commit(sm.fin());

@@ -93,6 +93,17 @@ __device__ __forceinline__ void tma_load_3d_hint(void *dst, const CUtensorMap *m
         : "memory");
 }
 
+// 5-D tiled load global -> shared with an L2 cache-policy hint.
+__device__ __forceinline__ void tma_load_5d_hint(void *dst, const CUtensorMap *map, uint64_t *bar, int c0, int c1,
+                                                 int c2, int c3, int c4, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%3, %4, %5, %6, %7}], [%2], %8;" ::"r"(smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_addr(bar)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4),
+        "l"(policy)
+        : "memory");
+}
+
 // 4-D tiled load global -> shared with an L2 cache-policy hint.
 __device__ __forceinline__ void tma_load_4d(void *dst, const CUtensorMap *map, uint64_t *bar, int c0, int c1,
                                             int c2, int c3, uint64_t policy) {
