@@ -23,6 +23,7 @@ import hashlib
 import json
 import math
 import os
+import re
 import subprocess
 import sys
 import threading
@@ -55,8 +56,13 @@ def load_peaks():
 
 
 def source_hash(path):
+    """Hash of a kernel source's code: comments removed and whitespace collapsed,
+    so that an edit to comments alone does not mark its ncu counters stale."""
     with open(path, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+        text = f.read().decode()
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return hashlib.sha256(" ".join(text.split()).encode()).hexdigest()[:16]
 
 
 def traffic_for(kernel_key, src_path, units_per_launch):

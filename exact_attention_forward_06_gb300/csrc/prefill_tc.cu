@@ -301,15 +301,15 @@ __device__ void producer(const PrefillParams &p, const Unit &w, const SmemLayout
 }
 
 // Paged K/V: the whole warp 0 produces.  A K/V tile is 8 pages; lane i < 8
-// reads table entry i of the tile and issues the two 16-row boxes (one per
-// 64-column half) of page i, so the table loads and the 32 copies of a tile
+// reads table entry i of the tile and issues the one 4 KiB box (16 rows, both
+// 64-column halves) of page i, so the table loads and the 16 copies of a tile
 // pair go out in parallel instead of one after another from a single lane.
 // Lane 0 arms each barrier before any lane issues into it.  Pages past the
 // sequence's last one, and bad entries (reported), get a row past the pool:
 // the copy then fills zeros.
 // When the tile's 8 pages are consecutive in the pool (an engine that hands a
-// sequence pages in order), lane 0 loads the tile with two 128-row boxes of
-// the run maps mk8/mv8 instead.
+// sequence pages in order), lane 0 loads the tile with one 128-row box of the
+// run maps mk8/mv8 instead.
 __device__ void producer_paged(const PrefillParams &p, const Unit &w, const SmemLayout &sm, const WaitCtx &wc,
                                int lane, const CUtensorMap *mq, const CUtensorMap *mk, const CUtensorMap *mv,
                                const CUtensorMap *mk8, const CUtensorMap *mv8) {

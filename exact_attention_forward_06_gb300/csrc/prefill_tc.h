@@ -40,9 +40,9 @@ struct PrefillParams {
     void *out;
     // Paged K/V (block_table == nullptr: K and V are tensors): sequence b has
     // seqlens_k[b] keys, key t in slot t % 16 of page block_table[b][t / 16]
-    // of the pools [num_pages][16][Hkv][d]; the maps for K and V are then 3-D
-    // maps over the pools with one 16-row page per box.  Queries are packed
-    // as above (cu_q); cu_k is unused.
+    // of the pools [num_pages][16][Hkv][d]; the maps for K and V are then 5-D
+    // maps over the pools (see make_map_pool_groups) with one whole page of
+    // one KV head per box.  Queries are packed as above (cu_q); cu_k is unused.
     const int *block_table;
     const int *seqlens_k;
     int max_blocks, num_pages;
@@ -50,7 +50,7 @@ struct PrefillParams {
 
 int prefill_smem_bytes();
 int prefill_num_units(const PrefillParams &p);
-// mk8/mv8: paged K/V only, maps over the pools with 128-row boxes (a run of 8
+// mk8/mv8: paged K/V only, the same pool maps with 128-row boxes (a run of 8
 // consecutive pages); pass mk/mv otherwise.
 cudaError_t launch_prefill(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
                            const CUtensorMap &mo, const CUtensorMap &mk8, const CUtensorMap &mv8,
