@@ -178,6 +178,7 @@ attn_status_t fill_prefill_params(attn::PrefillParams *p, const DeviceInfo *di, 
     p->inject = 0;
     p->round_mode = ATTN_ROUND_RTNE;
     p->n_full_units = attn::prefill_num_units(*p);
+    p->kv_major = 0;
     // L2 prefetch of the next wave's Q for short non-causal units (few K/V tiles).
     p->prefetch_ahead = (!causal && Sk <= 1024) ? di->sm_count : 0;
     p->split_units = 0;
@@ -270,6 +271,8 @@ attn_status_t attn_fwd_varlen(const void *q, const void *k, const void *v, void 
     p.cu_q = cu_seqlens_q;
     p.prefetch_ahead = 0;  // (dense coordinates only)
     p.cu_k = cu_seqlens_k;
+    // Keys much longer than queries (chunks against a context): K/V-first order.
+    p.kv_major = max_seqlen_k >= 2 * max_seqlen_q ? 1 : 0;
     p.total_q = total_q;
     p.total_k = total_k;
     p.out = out;
@@ -315,6 +318,7 @@ attn_status_t attn_fwd_paged(const void *q, const void *k_pages, const void *v_p
     p.total_q = total_q;
     p.out = out;
     p.block_table = block_table;
+    p.kv_major = 1;  // chunks against a cache: K/V-first order
     p.seqlens_k = seqlens_k;
     p.max_blocks = max_blocks_per_seq;
     p.num_pages = num_pages;

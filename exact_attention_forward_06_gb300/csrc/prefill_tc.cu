@@ -147,13 +147,12 @@ __host__ __device__ __forceinline__ void unit_kv_range(const PrefillParams &p, U
 __host__ __device__ __forceinline__ Unit unit_coords(const PrefillParams &p, int u) {
     Unit w;
     int m_step;
-    // Dense and packed batches go row block first: all heads of the longest
-    // row blocks, then the next, which balances the causal work.  Against a
-    // paged cache, whose pages together are larger than L2, the units go
-    // sequence and KV head first (longest row blocks first within), so that
-    // the units reading the same pages run at the same time: +3% there, while
-    // the same order cost the packed-batch path 3% of balance.
-    const bool kv_major = p.block_table != nullptr;
+    // Row block first (all heads of the longest row blocks, then the next)
+    // balances the causal work.  Sequence and KV head first (longest row
+    // blocks first within) runs the units that read the same K/V at the same
+    // time, which pays when the keys of all sequences exceed L2 and every row
+    // block reads a long context (chunks against a cache); the host chooses.
+    const bool kv_major = p.kv_major != 0;
     if (p.pair_heads) {
         const int pairs = p.G / 2;
         int r;

@@ -26,6 +26,7 @@ struct PrefillParams {
     // ws_lse [split_units*256][split_parts] and are merged afterwards.
     int prefetch_ahead;  // > 0: L2-prefetch the Q tiles of the unit this many CTAs ahead
     int n_full_units;
+    int kv_major;        // 1: units ordered by sequence and KV head (see unit_coords)
     int split_units;
     int split_parts;
     float *ws_o;
