@@ -76,6 +76,23 @@ def test_cross_lengths_match_oracle(A, causal):
     assert A.device_status()[0] == 0
 
 
+def test_unit_order_does_not_change_the_result(A):
+    # Keys at least twice as long as the queries switch the launch to the
+    # sequence-and-KV-head unit order; a larger stated key bound selects it
+    # for the same data, which must give the same bits.
+    lq = (300, 64, 200, 129)
+    lk = (500, 300, 77, 383)
+    w = inputs.VarlenWorkload("order", len(lq), 8, 2, causal=True, seed=96, lens_q=lq, lens_k=lk)
+    q, k, v, cu_q, cu_k = (t.cuda() for t in inputs.make_varlen(w))
+    o_row, l_row = A.fwd_varlen(q, k, v, cu_q, cu_k, max_seqlen_q=300, max_seqlen_k=500, causal=True,
+                                scale=w.scale)
+    o_kv, l_kv = A.fwd_varlen(q, k, v, cu_q, cu_k, max_seqlen_q=300, max_seqlen_k=sum(lk), causal=True,
+                              scale=w.scale)
+    torch.cuda.synchronize()
+    assert A.device_status()[0] == 0
+    assert torch.equal(o_row, o_kv) and torch.equal(l_row, l_kv)
+
+
 def test_equal_lengths_equal_the_dense_batch_bitwise(A):
     B, L, Hq, Hkv = 3, 300, 8, 2
     w = inputs.PrefillWorkload("dense", B, Hq, Hkv, L, L, causal=True, seed=93)
