@@ -5,8 +5,8 @@ forward kernel on each chunk and copies the results back; each batch is
 computed exactly as attn_fwd would compute it, so the result must equal the
 device call bit for bit (no tail-split workspace is registered here) and the
 oracle within the tolerance.  Shapes cover one chunk per batch, several
-batches per chunk with a short last chunk (B = 10), both layouts and a
-missing lse.
+batches per chunk with a short last chunk (B = 10), longer causal rows
+(including Sk > Sq and an odd group size), both layouts and a missing lse.
 """
 import pytest
 import torch
@@ -27,10 +27,12 @@ def A():
     return attn
 
 
-@pytest.mark.parametrize("layout,B,Hq,Hkv,S,causal", [("bshd", 3, 8, 2, 300, True), ("bhsd", 2, 4, 4, 200, False),
-                                                        ("bshd", 10, 2, 1, 130, True)])
-def test_host_call_equals_device_call_and_oracle(A, layout, B, Hq, Hkv, S, causal):
-    w = inputs.PrefillWorkload("host", B, Hq, Hkv, S, S, layout=layout, causal=causal, seed=121)
+@pytest.mark.parametrize("layout,B,Hq,Hkv,S,Sk,causal", [
+    ("bshd", 3, 8, 2, 300, 300, True), ("bhsd", 2, 4, 4, 200, 200, False), ("bshd", 10, 2, 1, 130, 130, True),
+    # longer causal rows: paired and unpaired heads, Sk > Sq
+    ("bshd", 2, 8, 2, 1000, 1000, True), ("bshd", 1, 3, 1, 600, 700, True), ("bshd", 5, 4, 2, 520, 520, True)])
+def test_host_call_equals_device_call_and_oracle(A, layout, B, Hq, Hkv, S, Sk, causal):
+    w = inputs.PrefillWorkload("host", B, Hq, Hkv, S, Sk, layout=layout, causal=causal, seed=121)
     q, k, v = (t.pin_memory() for t in inputs.make_prefill(w))
     out, lse = A.fwd_host(q, k, v, causal=causal, scale=w.scale, layout=layout)
     torch.cuda.synchronize()
@@ -38,7 +40,7 @@ def test_host_call_equals_device_call_and_oracle(A, layout, B, Hq, Hkv, S, causa
     o_dev, l_dev = A.fwd(q.cuda(), k.cuda(), v.cuda(), causal=causal, scale=w.scale, layout=layout)
     torch.cuda.synchronize()
     assert torch.equal(out, o_dev.cpu()) and torch.equal(lse, l_dev.cpu())
-    ref_o, ref_l = oracle.attention(q, k, v, B=B, Hq=Hq, Hkv=Hkv, Sq=S, Sk=S, layout=layout, causal=causal,
+    ref_o, ref_l = oracle.attention(q, k, v, B=B, Hq=Hq, Hkv=Hkv, Sq=S, Sk=Sk, layout=layout, causal=causal,
                                     scale=w.scale)
     check_out(out, ref_o, f"host {layout} B={B}")
     check_lse(lse, ref_l, f"host {layout} B={B}")
