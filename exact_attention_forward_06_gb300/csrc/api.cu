@@ -181,6 +181,7 @@ attn_status_t fill_prefill_params(attn::PrefillParams *p, const DeviceInfo *di, 
     p->kv_major = 0;
     // L2 prefetch of the next wave's Q for short non-causal units (few K/V tiles).
     p->prefetch_ahead = (!causal && Sk <= 1024) ? di->sm_count : 0;
+    p->early_start = (!causal && Sk <= 1024) ? 1 : 0;
     p->split_units = 0;
     p->split_parts = 1;
     p->ws_o = nullptr;
@@ -270,6 +271,7 @@ attn_status_t attn_fwd_varlen(const void *q, const void *k, const void *v, void 
     p.round_mode = round_mode;
     p.cu_q = cu_seqlens_q;
     p.prefetch_ahead = 0;  // (dense coordinates only)
+    p.early_start = 0;
     p.cu_k = cu_seqlens_k;
     // Keys much longer than queries (chunks against a context): K/V-first order.
     p.kv_major = max_seqlen_k >= 2 * max_seqlen_q ? 1 : 0;
@@ -315,6 +317,7 @@ attn_status_t attn_fwd_paged(const void *q, const void *k_pages, const void *v_p
     p.round_mode = round_mode;
     p.cu_q = cu_seqlens_q;
     p.prefetch_ahead = 0;  // (dense coordinates only)
+    p.early_start = 0;
     p.total_q = total_q;
     p.out = out;
     p.block_table = block_table;

@@ -75,7 +75,7 @@ constexpr uint32_t SMEM_Q0 = 0;
 constexpr uint32_t SMEM_Q1 = TILE_BYTES;
 constexpr uint32_t SMEM_SLOTS = 2 * TILE_BYTES;
 constexpr uint32_t SMEM_TILES = SMEM_SLOTS + NSLOT * TILE_BYTES;
-constexpr int NBARS = 1 + 2 * NSLOT + 2 + 1 + 2 + 2 + 1 + 1;
+constexpr int NBARS = 1 + 2 * NSLOT + 2 + 1 + 2 + 2 + 1 + 1 + 1;
 constexpr uint32_t SMEM_MISC = 256;
 constexpr uint32_t SMEM_ALIGN = 1024;
 constexpr float RESCALE_LOG2 = 8.0f;  // move the running max only past a 2^8 growth
@@ -98,7 +98,10 @@ __device__ __forceinline__ uint32_t tm_o(int t) { return TM_O0 + 128 * t; }
 struct SmemLayout {
     uint8_t *base;
     uint64_t *bars;
+    // q_full: both Q tiles have landed; with an early start Q_1 has its own
+    // barrier q_full1 and q_full covers Q_0 alone.
     __device__ uint64_t *q_full() const { return bars; }
+    __device__ uint64_t *q_full1() const { return bars + NBARS - 1; }
     __device__ uint64_t *kv_full(int s) const { return bars + 1 + s; }
     __device__ uint64_t *kv_empty(int s) const { return bars + 1 + NSLOT + s; }
     __device__ uint64_t *s_full(int t) const { return bars + 1 + 2 * NSLOT + t; }
@@ -259,8 +262,35 @@ __device__ __forceinline__ void load_tile(const CUtensorMap *map, uint8_t *dst, 
     ptx::tma_load_4d(dst + HALF_BYTES, map, bar, hi.c0, hi.c1, hi.c2, hi.c3, pol);
 }
 
+// The copies a unit can issue before anything is consumed, in the order its
+// first products need them: Q_0, K_0, Q_1, V_0, then further ring items up to
+// the ring's size (no slot has to be released yet).  With an early start the
+// barrier-initialising thread issues them before the CTA-wide barrier, while
+// tensor memory is being allocated.  Returns the number of ring items issued.
+__device__ int producer_start(const PrefillParams &p, const Unit &w, const SmemLayout &sm, const CUtensorMap *mq,
+                              const CUtensorMap *mk, const CUtensorMap *mv) {
+    const uint64_t pol_q = ptx::policy_evict_first();
+    const uint64_t pol_kv = ptx::policy_evict_last();
+    const int total = 2 * w.n_kv;
+    const int first = total < NSLOT ? total : NSLOT;
+    for (int n = 0; n < first; ++n) {
+        if (n < 2) {
+            uint64_t *qb = n ? sm.q_full1() : sm.q_full();
+            ptx::mbar_arrive_expect_tx(qb, TILE_BYTES);
+            load_tile(mq, sm.q_tile(n), qb, p.bhsd, n ? w.h[1] : w.h[0], w.q0 + (n ? w.s0[1] : w.s0[0]), w.tb,
+                      pol_q);
+        }
+        ptx::mbar_arrive_expect_tx(sm.kv_full(n), TILE_BYTES);
+        load_tile((n & 1) ? mv : mk, sm.slot(n), sm.kv_full(n), p.bhsd, w.g, w.k0 + (w.j_lo + (n >> 1)) * BN, w.tb,
+                  pol_kv);
+    }
+    return first;
+}
+
+// first: ring items producer_start already issued (EARLY), else 0.
+template <bool EARLY>
 __device__ void producer(const PrefillParams &p, const Unit &w, const SmemLayout &sm, const WaitCtx &wc,
-                         const CUtensorMap *mq, const CUtensorMap *mk, const CUtensorMap *mv) {
+                         const CUtensorMap *mq, const CUtensorMap *mk, const CUtensorMap *mv, int first) {
     if (p.inject == 1) return;  // fault injection: issue nothing
     // A unit whose rows see no key loads nothing: its output tiles are zeros,
     // written into the Q tile buffers, which therefore must not receive a
@@ -268,9 +298,11 @@ __device__ void producer(const PrefillParams &p, const Unit &w, const SmemLayout
     if (w.n_kv == 0) return;
     const uint64_t pol_q = ptx::policy_evict_first();
     const uint64_t pol_kv = ptx::policy_evict_last();
-    ptx::mbar_arrive_expect_tx(sm.q_full(), 2 * TILE_BYTES);
-    load_tile(mq, sm.q_tile(0), sm.q_full(), p.bhsd, w.h[0], w.q0 + w.s0[0], w.tb, pol_q);
-    load_tile(mq, sm.q_tile(1), sm.q_full(), p.bhsd, w.h[1], w.q0 + w.s0[1], w.tb, pol_q);
+    if (!EARLY) {
+        ptx::mbar_arrive_expect_tx(sm.q_full(), 2 * TILE_BYTES);
+        load_tile(mq, sm.q_tile(0), sm.q_full(), p.bhsd, w.h[0], w.q0 + w.s0[0], w.tb, pol_q);
+        load_tile(mq, sm.q_tile(1), sm.q_full(), p.bhsd, w.h[1], w.q0 + w.s0[1], w.tb, pol_q);
+    }
     if (p.prefetch_ahead > 0 && (int)blockIdx.x + p.prefetch_ahead < p.n_full_units) {
         // Short units (few K/V tiles) spend much of their time loading Q:
         // start the Q of the unit about one wave ahead into L2, so the CTA
@@ -284,8 +316,8 @@ __device__ void producer(const PrefillParams &p, const Unit &w, const SmemLayout
         }
     }
     const int total = 2 * w.n_kv;
-    int issued = 0;
-    for (int n = 0; n < total; ++n) {
+    int issued = EARLY ? first : 0;
+    for (int n = issued; n < total; ++n) {
         const int slot = n % NSLOT;
         const int round = n / NSLOT;
         if (round > 0 && !wait_bounded(sm.kv_empty(slot), (round - 1) & 1, wc, kSiteProducerEmpty)) break;
@@ -296,6 +328,7 @@ __device__ void producer(const PrefillParams &p, const Unit &w, const SmemLayout
     }
     // On the way out make sure no copy is still writing into shared memory.
     drain_wait(sm.q_full(), 0, wc);
+    if (EARLY) drain_wait(sm.q_full1(), 0, wc);
     for (int n = max(0, issued - NSLOT); n < issued; ++n) drain_wait(sm.kv_full(n % NSLOT), (n / NSLOT) & 1, wc);
 }
 
@@ -412,10 +445,10 @@ __device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t tmem_p, uint6
 //   PV_t(j) needs P_t(j) (p_full[t]) and V_j.
 // A ring slot takes one release per stream (a commit after the stream's
 // product that reads it).
-template <int T, bool PAGED>
+template <int T, bool PAGED, bool EARLY>
 __device__ void mma_stream(const Unit &w, const SmemLayout &sm, const WaitCtx &wc, uint32_t tmem_base) {
     if (w.n_kv == 0) return;  // nothing to multiply (and no Q is loaded)
-    if (!wait_spin(sm.q_full(), 0, wc, kSiteMmaQ)) return;
+    if (!wait_spin(EARLY && T == 1 ? sm.q_full1() : sm.q_full(), 0, wc, kSiteMmaQ)) return;
     ptx::tc_fence_after();
     const uint64_t q_desc = ptx::desc_kmajor_sw128(ptx::smem_addr(sm.q_tile(T)));
     const uint32_t slot0 = ptx::smem_addr(sm.slot(0));
@@ -736,6 +769,7 @@ __device__ void softmax_wg(const PrefillParams &p, const Unit &w, const SmemLayo
 
 // ------------------------------------------------------------------ kernel
 
+template <bool EARLY>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                    const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_o,
@@ -754,8 +788,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // grid is sized by the longest sequence) has nothing to do.
     if (w.s0[0] >= w.Sq) return;
 
+    int first = 0;  // ring items issued before the CTA-wide barrier (thread 0, EARLY)
     if (threadIdx.x == 0) {
         ptx::mbar_init(sm.q_full(), 1);
+        ptx::mbar_init(sm.q_full1(), 1);
         for (int s = 0; s < NSLOT; ++s) {
             ptx::mbar_init(sm.kv_full(s), 1);
             ptx::mbar_init(sm.kv_empty(s), 2);  // one release per issuing stream
@@ -776,6 +812,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         ptx::prefetch_tensormap(&map_k);
         ptx::prefetch_tensormap(&map_v);
         ptx::prefetch_tensormap(&map_o);
+        if (EARLY && p.block_table == nullptr && p.inject != 1 && w.n_kv > 0)
+            first = producer_start(p, w, sm, &map_q, &map_k, &map_v);
     }
     if (warp == 1) {
         ptx::tmem_alloc(sm.tmem_slot(), 512);
@@ -793,14 +831,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if (p.block_table != nullptr)
                 producer_paged(p, w, sm, wc, lane, &map_q, &map_k, &map_v, &map_k8, &map_v8);
             else if (lane == 0)
-                producer(p, w, sm, wc, &map_q, &map_k, &map_v);
+                producer<EARLY>(p, w, sm, wc, &map_q, &map_k, &map_v, first);
         } else if (warp == 1 || warp == 2) {
             if (lane == 0) {
                 const bool paged = p.block_table != nullptr;
                 if (warp == 1)
-                    paged ? mma_stream<0, true>(w, sm, wc, tmem_base) : mma_stream<0, false>(w, sm, wc, tmem_base);
+                    paged ? mma_stream<0, true, false>(w, sm, wc, tmem_base)
+                          : mma_stream<0, false, EARLY>(w, sm, wc, tmem_base);
                 else
-                    paged ? mma_stream<1, true>(w, sm, wc, tmem_base) : mma_stream<1, false>(w, sm, wc, tmem_base);
+                    paged ? mma_stream<1, true, false>(w, sm, wc, tmem_base)
+                          : mma_stream<1, false, EARLY>(w, sm, wc, tmem_base);
                 // Whatever happened, wait until every product issued (by
                 // either stream) has completed before tensor memory is released.
                 ptx::umma_commit(sm.fin());
@@ -838,11 +878,18 @@ cudaError_t launch_prefill(const CUtensorMap &mq, const CUtensorMap &mk, const C
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (configured_device != dev) {
-        e = cudaFuncSetAttribute(g1::prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        e = cudaFuncSetAttribute(g1::prefill_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(g1::prefill_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
         configured_device = dev;
     }
-    g1::prefill_kernel<<<num_ctas, g1::NUM_THREADS, smem, stream>>>(mq, mk, mv, mo, mk8, mv8, p);
+    // Short non-causal units (few K/V tiles) start their first copies before
+    // the CTA-wide barrier; every other launch runs the plain instantiation.
+    if (p.early_start && p.block_table == nullptr)
+        g1::prefill_kernel<true><<<num_ctas, g1::NUM_THREADS, smem, stream>>>(mq, mk, mv, mo, mk8, mv8, p);
+    else
+        g1::prefill_kernel<false><<<num_ctas, g1::NUM_THREADS, smem, stream>>>(mq, mk, mv, mo, mk8, mv8, p);
     return cudaGetLastError();
 }
 

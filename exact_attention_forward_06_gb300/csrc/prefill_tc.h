@@ -25,6 +25,7 @@ struct PrefillParams {
     // fp32 partials go to ws_o [split_units*256][split_parts][128] and
     // ws_lse [split_units*256][split_parts] and are merged afterwards.
     int prefetch_ahead;  // > 0: L2-prefetch the Q tiles of the unit this many CTAs ahead
+    int early_start;     // 1: a unit's first copies go out before the CTA-wide barrier
     int n_full_units;
     int kv_major;        // 1: units ordered by sequence and KV head (see unit_coords)
     int split_units;
