@@ -2,7 +2,8 @@
 
 The shapes are built from the device's SM count so that the work units leave
 a partial last wave: B = num_SMs + 8 batches of one unit each (or two with a
-head pair), non-causal, 16 K/V tiles.  With a workspace registered, the last
+head pair), non-causal, 16 K/V tiles, or 8 (short units, whose first copies
+the kernel issues before its CTA-wide barrier).  With a workspace registered, the last
 units run as key-range parts whose fp32 partials are merged; every row of the
 split units and a sample of the others is compared with the oracle, and the
 split result is checked against the unsplit one and for determinism.
@@ -27,10 +28,11 @@ def A():
     return attn
 
 
+@pytest.mark.parametrize("Sk", [2048, 1024])
 @pytest.mark.parametrize("layout,Hq,Hkv", [("bshd", 1, 1), ("bhsd", 2, 1)])
-def test_tail_split_matches_oracle_and_unsplit(A, layout, Hq, Hkv):
+def test_tail_split_matches_oracle_and_unsplit(A, layout, Hq, Hkv, Sk):
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    B, Sq, Sk = sms + 8, 256, 2048
+    B, Sq = sms + 8, 256
     w = inputs.PrefillWorkload("tail", B, Hq, Hkv, Sq, Sk, layout=layout, seed=71)
     need = A.fwd_workspace_bytes(B, Hq, Hkv, Sq, Sk, causal=False)
     assert need > 0, "this shape is meant to get a tail split"
