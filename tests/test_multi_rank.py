@@ -60,3 +60,21 @@ def test_bench_rejects_short_warmup(warmup):
     import bench
     with pytest.raises(SystemExit):
         bench.main(["--warmup", str(warmup)])
+
+
+def test_traffic_entry_follows_kernel_code_not_comments(tmp_path):
+    # The committed ncu traffic is used only while its kernel's code is the one
+    # measured: a comment edit keeps the entry, a code edit drops it.
+    import bench
+    src = tmp_path / "k.cu"
+    src.write_text("// kernel\n__global__ void k(int *p) { p[0] = 1; }  /* store */\n")
+    h = bench.source_hash(str(src))
+    src.write_text("// the kernel, reworded\n__global__ void k(int *p) {\n    p[0] = 1;\n}\n")
+    assert bench.source_hash(str(src)) == h
+    src.write_text("__global__ void k(int *p) { p[0] = 2; }\n")
+    assert bench.source_hash(str(src)) != h
+    with open(bench.TRAFFIC_PATH) as f:
+        import json
+        entry = json.load(f)["prefill_kernel"]
+    assert bench.traffic_for("prefill_kernel", str(src), 10) is None
+    assert entry["bytes_per_unit"] > 0
