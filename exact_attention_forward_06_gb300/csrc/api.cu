@@ -178,7 +178,10 @@ attn_status_t fill_prefill_params(attn::PrefillParams *p, const DeviceInfo *di, 
     p->inject = 0;
     p->round_mode = ATTN_ROUND_RTNE;
     p->n_full_units = attn::prefill_num_units(*p);
-    p->kv_major = 0;
+    // Non-causal units all have the same length, so ordering them by batch and
+    // KV head costs no balance; it keeps the units that read the same K/V
+    // together, which pays once the K/V of all heads exceed L2.
+    p->kv_major = (!causal && (double)B * Hkv * Sk * 128 * 4 > 64.0 * (1 << 20)) ? 1 : 0;
     // L2 prefetch of the next wave's Q for short non-causal units (few K/V tiles).
     p->prefetch_ahead = (!causal && Sk <= 1024) ? di->sm_count : 0;
     p->early_start = (!causal && Sk <= 1024) ? 1 : 0;

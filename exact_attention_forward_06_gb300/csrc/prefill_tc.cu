@@ -153,8 +153,9 @@ __host__ __device__ __forceinline__ Unit unit_coords(const PrefillParams &p, int
     // Row block first (all heads of the longest row blocks, then the next)
     // balances the causal work.  Sequence and KV head first (longest row
     // blocks first within) runs the units that read the same K/V at the same
-    // time, which pays when the keys of all sequences exceed L2 and every row
-    // block reads a long context (chunks against a cache); the host chooses.
+    // time, which pays when the keys of all heads exceed L2 and every row
+    // block reads a long context (non-causal launches, whose units are all
+    // alike, and chunks against a cache); the host chooses.
     const bool kv_major = p.kv_major != 0;
     if (p.pair_heads) {
         const int pairs = p.G / 2;
