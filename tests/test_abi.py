@@ -196,3 +196,46 @@ def test_fwd_host_rejects_bad_arguments_before_any_copy(lib):
     assert lib.attn_fwd_host(*bad) == 1
     assert lib.attn_fwd_host_workspace_bytes(2, 4, 2, 64, 64, 128) > 0
     assert lib.attn_fwd_host_workspace_bytes(2, 3, 2, 64, 64, 128) == 0
+
+
+def _header_prototypes():
+    """{name: [kind, ...]} from include/*.h, kinds 'ptr', 'int', 'float', 'u64'."""
+    protos = {}
+    for h in HEADERS:
+        text = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
+        for ret, name, params in re.findall(r"([\w\s\*]+?)\b(attn_[a-z0-9_]+)\s*\(([^)]*)\)\s*;", text):
+            kinds = []
+            for prm in [x.strip() for x in params.split(",")]:
+                if prm in ("", "void"):
+                    continue
+                if "*" in prm:
+                    kinds.append("ptr")
+                elif prm.startswith("float"):
+                    kinds.append("float")
+                elif prm.startswith("size_t"):
+                    kinds.append("u64")  # LP64: size_t is a 64-bit unsigned, as ctypes' c_size_t
+                elif prm.startswith("uint64_t"):
+                    kinds.append("u64")
+                else:
+                    # plain ints and the header's enums (passed as int)
+                    assert prm.split()[0] in ("int", "int32_t", "attn_status_t", "attn_layout_t", "attn_round_t"), \
+                        f"{name}: unexpected parameter {prm!r}"
+                    kinds.append("int")
+            protos[name] = kinds
+    return protos
+
+
+def test_binding_argtypes_match_the_header(lib):
+    # The ctypes declarations of the binding must follow include/attn.h
+    # parameter for parameter (a mismatch would pass garbage silently).
+    kind_of = {ctypes.c_void_p: "ptr", ctypes.c_int: "int", ctypes.c_float: "float", ctypes.c_size_t: "u64",
+               ctypes.c_uint64: "u64"}
+    protos = _header_prototypes()
+    assert set(protos) == set(declared_functions())
+    for name, kinds in protos.items():
+        argtypes = getattr(lib, name).argtypes
+        got = [] if argtypes is None else [
+            "ptr" if (t in (ctypes.c_void_p, ctypes.c_char_p) or hasattr(t, "contents") or
+                      getattr(t, "_type_", None) is not None and t.__name__.startswith("LP_")) else kind_of.get(t, repr(t))
+            for t in argtypes]
+        assert got == kinds, f"{name}: binding {got} vs header {kinds}"
