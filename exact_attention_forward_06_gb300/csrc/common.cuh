@@ -33,6 +33,7 @@ enum WaitSite : unsigned {
     kSitePagedTable = 13,
     kSiteSoftmaxV = 14,
     kSiteAppendSlot = 15,
+    kSiteDecodeSeqlen = 16,
 };
 
 // First error wins; the site is informative only.

@@ -107,13 +107,18 @@ __global__ void __launch_bounds__(NTHREADS, 3)
     const int lane = threadIdx.x & 31;
 
     const int L_raw = p.seqlens[b];
-    const int L = max(0, min(L_raw, p.max_blocks * PAGE));
+    // A length outside [0, 16 * max_blocks] is reported, and the sequence is
+    // skipped: its rows get O = 0 and lse = -inf, and nothing is appended.
+    const bool bad_len = L_raw < 0 || L_raw > p.max_blocks * PAGE;
+    if (bad_len && threadIdx.x == 0 && split == 0 && blockIdx.x == 0)
+        report_status(p.status, kStatusDeviceBounds, kSiteDecodeSeqlen);
+    const int L = bad_len ? 0 : L_raw;
     const int npages = (L + PAGE - 1) / PAGE;
     const int page0 = split * p.pages_per_split;
     const int np = max(0, min(p.pages_per_split, npages - page0));
     const int64_t row0 = (int64_t)b * p.Hq + h0;  // first (b, h) row of this CTA
     // With a fused append, split 0 also attends to the new token (position L).
-    const bool new_token = p.k_new != nullptr && split == 0;
+    const bool new_token = p.k_new != nullptr && split == 0 && !bad_len;
 
     if (np == 0 && !new_token) {  // nothing to attend to in this split
         for (int i = threadIdx.x; i < GH * D; i += NTHREADS)

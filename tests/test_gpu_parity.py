@@ -277,6 +277,26 @@ def test_paged_decode_bad_block_table_is_reported(A):
     assert torch.isfinite(out).all()
 
 
+@pytest.mark.parametrize("bad_len", [-1, 8 * 16 + 1, -(2 ** 31)])
+def test_paged_decode_bad_length_is_reported(A, bad_len):
+    # A length outside [0, 16 * max_blocks] is neither clamped nor read past:
+    # it is reported and that sequence's rows come back as zeros and -inf.
+    w = inputs.DecodeWorkload("badlen", B=3, Hq=8, Hkv=2, max_blocks=8, seed=19)
+    q, kp, vp, table, lens = inputs.make_decode(w, seqlens=[40, 128, 7])
+    bad = lens.clone()
+    bad[1] = bad_len
+    assert A.device_status()[0] == 0
+    out, lse = A.decode_paged(q.cuda(), kp.cuda(), vp.cuda(), table.cuda(), bad.cuda(), scale=w.scale)
+    code, site = A.device_status()
+    assert code == 6 and site == 16  # ATTN_ERR_DEVICE_BOUNDS at the length check
+    assert torch.equal(out[1].cpu(), torch.zeros_like(out[1].cpu()))
+    assert torch.isneginf(lse[1]).all()
+    keep = [0, 2]
+    ref_o, ref_l = oracle.decode_paged(q[keep], kp, vp, table[keep], lens[keep], scale=w.scale)
+    check_out(out[keep], ref_o, "bad length, good rows")
+    check_lse(lse[keep], ref_l, "bad length, good rows")
+
+
 def test_lse_merge_matches_oracle(A):
     g = torch.Generator().manual_seed(11)
     rows, nsplit, d = 37, 5, 128
