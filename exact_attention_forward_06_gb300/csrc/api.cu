@@ -13,6 +13,7 @@
 #include <cudaTypedefs.h>
 
 #include "attn.h"
+#include "api_internal.h"
 #include "prefill_tc.h"
 
 // Device status word: [0] = first error code recorded, [1] = wait/check site.
@@ -394,11 +395,16 @@ size_t attn_decode_workspace_bytes(int B, int Hq, int d, int max_blocks_per_seq)
     return o_bytes + l_bytes;
 }
 
-static attn_status_t decode_impl(const void *q, const void *k_new, const void *v_new, const void *k_pages,
-                                 const void *v_pages, const int32_t *block_table, const int32_t *seqlens, void *out,
-                                 float *lse, int B, int Hq, int Hkv, int d, int page_size, int num_pages,
-                                 int max_blocks_per_seq, float scale, void *workspace, size_t workspace_bytes,
-                                 void *stream) {
+}  // extern "C"
+
+namespace attn {
+
+// The argument checks of a decode step other than its workspace (pointers,
+// alignment, shapes, scale), shared by the entry points that take a
+// workspace and the one that does not.
+attn_status_t check_decode_args(const void *q, const void *k_pages, const void *v_pages, const int32_t *block_table,
+                                const int32_t *seqlens, const void *out, const float *lse, int B, int Hq, int Hkv,
+                                int d, int page_size, int num_pages, int max_blocks_per_seq, float scale) {
     if (!q || !k_pages || !v_pages || !block_table || !seqlens || !out) return ATTN_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(k_pages) || !aligned16(v_pages) || !aligned16(out)) return ATTN_ERR_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(block_table) & 3u) || (reinterpret_cast<uintptr_t>(seqlens) & 3u))
@@ -409,10 +415,24 @@ static attn_status_t decode_impl(const void *q, const void *k_new, const void *v
     if (!std::isfinite(scale) || scale < 0.f) return ATTN_ERR_INVALID_ARG;
     if (d != 128 || page_size != 16) return ATTN_ERR_UNSUPPORTED;
     if ((int64_t)num_pages * 16 > ((int64_t)1 << 31) - 1) return ATTN_ERR_INVALID_ARG;
+    return ATTN_OK;
+}
+
+}  // namespace attn
+
+extern "C" {
+
+static attn_status_t decode_impl(const void *q, const void *k_new, const void *v_new, const void *k_pages,
+                                 const void *v_pages, const int32_t *block_table, const int32_t *seqlens, void *out,
+                                 float *lse, int B, int Hq, int Hkv, int d, int page_size, int num_pages,
+                                 int max_blocks_per_seq, float scale, void *workspace, size_t workspace_bytes,
+                                 void *stream) {
+    attn_status_t st = attn::check_decode_args(q, k_pages, v_pages, block_table, seqlens, out, lse, B, Hq, Hkv, d,
+                                               page_size, num_pages, max_blocks_per_seq, scale);
+    if (st != ATTN_OK) return st;
     const size_t need = attn_decode_workspace_bytes(B, Hq, d, max_blocks_per_seq);
     if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < need)
         return ATTN_ERR_WORKSPACE;
-    attn_status_t st;
     DeviceInfo *di = nullptr;
     if ((st = device_info(&di)) != ATTN_OK) return st;
     CUtensorMap mk, mv;

@@ -260,6 +260,10 @@ size_t attn_decode_workspace_bytes(int B, int Hq, int d, int max_blocks_per_seq)
  *              physical page of keys 16p .. 16p+15 of sequence b.  Entries at
  *              or past ceil(seqlens[b]/16) are never read (may hold -1).
  * seqlens:     int32 [B] on the device, each in [0, 16 * max_blocks_per_seq].
+ *              A length outside that range is not clamped: it is recorded as
+ *              ATTN_ERR_DEVICE_BOUNDS in the device status word and that
+ *              sequence is skipped (its rows get zeros and lse = -inf); the
+ *              other sequences are unaffected.
  * out:         bf16 [B][Hq][d] (written); a sequence of length 0 gets zeros.
  * lse:         fp32 [B][Hq] (written, -inf for length 0), or NULL.
  * page_size must be 16; d must be 128; Hq % Hkv == 0.
@@ -294,7 +298,9 @@ attn_status_t attn_decode_paged(const void *q, const void *k_pages, const void *
  * included; out, lse, the other arguments, the workspace and the errors are
  * those of attn_decode_paged.  A slot outside the table or the pool is
  * recorded as ATTN_ERR_DEVICE_BOUNDS and that token is not written (it is
- * still attended to).  k_new, v_new must not overlap the pools.
+ * still attended to).  A length outside [0, 16 * max_blocks_per_seq] skips
+ * the sequence as in attn_decode_paged: nothing is appended for it.
+ * k_new, v_new must not overlap the pools.
  */
 attn_status_t attn_decode_paged_append(const void *q, const void *k_new, const void *v_new,
                                        void *k_pages, void *v_pages,
@@ -325,11 +331,16 @@ attn_status_t attn_decode_paged_append(const void *q, const void *k_new, const v
  * partials in a library-owned device array of ATTN_DECODE_NOALLOC_SCRATCH_BYTES
  * instead.  It calls no cudaMalloc, cudaFree or other allocating routine.
  *
- * The caller still passes every input and output buffer.  A shape whose
+ * The caller still passes every input and output buffer.  Arguments are
+ * checked as in attn_decode_paged first (ATTN_ERR_INVALID_ARG,
+ * ATTN_ERR_UNSUPPORTED); a call that passes them but whose
  * attn_decode_workspace_bytes(B, Hq, d, max_blocks_per_seq) exceeds the array
- * is rejected with ATTN_ERR_WORKSPACE before anything is launched.  The first
- * call on a device looks up the array's device address (cudaGetSymbolAddress)
- * on that device; make that first call before any stream capture.  All calls
+ * is then rejected with ATTN_ERR_WORKSPACE, before anything is launched.  The
+ * first call in each CUDA context looks up the array's device address
+ * (cudaGetSymbolAddress) with that context current and remembers it under the
+ * context's unique id; make that first call before any stream capture.  A
+ * context created later (after cudaDeviceReset, for instance) gets a lookup of
+ * its own, so no address outlives its context.  All calls
  * share the one array, which keeps the last call's contents (nothing in it
  * needs to start at zero): calls that overlap on the GPU, e.g. on two streams
  * with no ordering between them, race on it and must not be issued.

@@ -102,6 +102,29 @@ def test_decode_rejects_bad_arguments_before_any_launch(lib, kw, code):
     assert _decode(lib, **kw) == code
 
 
+def _decode_noalloc(lib, **kw):
+    a = dict(q=16, kp=16, vp=16, bt=16, sl=16, out=16, lse=None, B=2, Hq=4, Hkv=2, d=128, page=16, npages=10,
+             maxb=4, scale=0.1)
+    a.update(kw)
+    return lib.attn_decode_paged_noalloc(a["q"], a["kp"], a["vp"], a["bt"], a["sl"], a["out"], a["lse"], a["B"],
+                                         a["Hq"], a["Hkv"], a["d"], a["page"], a["npages"], a["maxb"], a["scale"],
+                                         None)
+
+
+# 64 sequences x 64 heads x 8192 pages: far more partials than the 16 MiB array holds
+_HUGE = dict(B=64, Hq=64, Hkv=8, maxb=8192)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=None), 1), (dict(bt=18), 1), (dict(Hq=5), 1), (dict(scale=float("nan")), 1), (dict(d=256), 2),
+    # the argument checks come before the array's size limit
+    (dict(q=None, **_HUGE), 1), (dict(out=24, **_HUGE), 1), (dict(page=32, **_HUGE), 2),
+    (dict(_HUGE), 5),
+])
+def test_decode_noalloc_checks_arguments_before_its_size_limit(lib, kw, code):
+    assert _decode_noalloc(lib, **kw) == code
+
+
 def test_merge_rejects_bad_arguments(lib):
     assert lib.attn_lse_merge(None, 16, 16, None, 4, 2, 128, 0, None) == 1
     assert lib.attn_lse_merge(16, 16, 16, None, 0, 2, 128, 0, None) == 1

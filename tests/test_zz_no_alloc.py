@@ -5,8 +5,10 @@ outputs with no workspace hook, or an engine that has reserved all of HBM and
 forbids further cudaMalloc) get the split partials kept in a library-owned
 device array instead of a workspace they would have to allocate.  This checks,
 through the C ABI, that two calls in a row of the allocation-free entry point
-match the workspace-taking attn_decode_paged within the parity tolerance, and
-that a shape too large for the array is refused.
+give bit for bit the output of the workspace-taking attn_decode_paged (the
+same split plan, kernels and merge order), that each also matches the fp64
+oracle within the parity tolerance, and that a shape too large for the array
+is refused.
 
 Kept in its own file, named to be collected last, so that a failure here never
 stops a run before the other tests have run.
@@ -14,6 +16,7 @@ stops a run before the other tests have run.
 import pytest
 import torch
 
+import oracle
 from exact_attention_forward_06_gb300 import inputs
 from parity_util import check_lse, check_out
 
@@ -43,14 +46,20 @@ def test_noalloc_decode_matches_workspace_decode_twice(A):
     ]
     for w, lens in cases:
         assert A.decode_workspace_bytes(w.B, w.Hq, w.d, w.max_blocks) <= 16 * 1024 * 1024
-        q, kp, vp, table, seqlens = _device_inputs(w, lens)
+        host = inputs.make_decode(w, seqlens=lens)
+        q, kp, vp, table, seqlens = (t.cuda() for t in host)
         ref_out, ref_lse = A.decode_paged(q, kp, vp, table, seqlens, scale=w.scale)
-        out = torch.empty_like(q)
-        lse = torch.empty((w.B, w.Hq), device=q.device, dtype=torch.float32)
+        out = torch.full_like(q, float("nan"))
+        lse = torch.full((w.B, w.Hq), float("nan"), device=q.device, dtype=torch.float32)
         A.decode_paged_noalloc(q, kp, vp, table, seqlens, scale=w.scale, out=out, lse=lse)
         torch.cuda.synchronize()
-        check_out(out, ref_out.double().cpu().numpy(), f"noalloc {w.name}")
-        check_lse(lse, ref_lse.double().cpu().numpy(), f"noalloc {w.name}")
+        # Same plan, kernels and merge order as the workspace call: bit for bit.
+        assert torch.equal(out, ref_out), f"noalloc {w.name}: output differs from attn_decode_paged"
+        assert torch.equal(lse, ref_lse), f"noalloc {w.name}: lse differs from attn_decode_paged"
+        # And against the fp64 oracle directly.
+        o_ref, l_ref = oracle.decode_paged(*host, scale=w.scale)
+        check_out(out, o_ref, f"noalloc {w.name} vs oracle")
+        check_lse(lse, l_ref, f"noalloc {w.name} vs oracle")
         assert A.device_status()[0] == 0
 
 
