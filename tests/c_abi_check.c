@@ -1,12 +1,14 @@
 /*
  * c_abi_check.c -- the library used from plain C through include/attn.h only
  * (no Python, no torch): device buffers from the CUDA runtime, one causal GQA
- * prefill through attn_fwd compared with the SIMT cross-check attn_fwd_simple,
- * and one paged decode step through attn_decode_paged compared with a
- * double-precision reference computed here on the host.  Exits 0 when both
- * agree within |a - b| <= 4e-3 + 8e-3 |b|.
+ * prefill through attn_fwd and one paged decode step through
+ * attn_decode_paged, each compared with a double-precision reference
+ * computed here on the host from the definition (softmax of the scaled scores
+ * over the visible keys, bottom-right causal alignment, kv head h / (Hq/Hkv)).
+ * Exits 0 when every output element agrees within |a - b| <= 4e-3 + 8e-3 |b|
+ * and every prefill log-sum-exp within 1e-3.
  *
- * Built and run by tests/test_gpu_c_abi.py:
+ * Built and run by tests/test_c_abi_program.py:
  *   gcc -std=c11 -O2 c_abi_check.c -I include -I $CUDA/include -L <pkg> -lattn -L $CUDA/lib64 -lcudart -lm
  */
 #include <math.h>
@@ -69,31 +71,52 @@ int main(void) {
     const int B = 2, Hq = 8, Hkv = 2, S = 300, D = 128;
     const size_t nq = (size_t)B * S * Hq * D, nk = (size_t)B * S * Hkv * D;
     uint16_t *hq = fill(nq), *hk = fill(nk), *hv = fill(nk);
-    void *q, *k, *v, *o1, *o2;
-    float *l1, *l2;
+    void *q, *k, *v, *o1;
+    float *l1;
     CHECK_CUDA(cudaMalloc(&q, nq * 2));
     CHECK_CUDA(cudaMalloc(&k, nk * 2));
     CHECK_CUDA(cudaMalloc(&v, nk * 2));
     CHECK_CUDA(cudaMalloc(&o1, nq * 2));
-    CHECK_CUDA(cudaMalloc(&o2, nq * 2));
     CHECK_CUDA(cudaMalloc((void **)&l1, (size_t)B * Hq * S * 4));
-    CHECK_CUDA(cudaMalloc((void **)&l2, (size_t)B * Hq * S * 4));
     CHECK_CUDA(cudaMemcpy(q, hq, nq * 2, cudaMemcpyHostToDevice));
     CHECK_CUDA(cudaMemcpy(k, hk, nk * 2, cudaMemcpyHostToDevice));
     CHECK_CUDA(cudaMemcpy(v, hv, nk * 2, cudaMemcpyHostToDevice));
     const float scale = 0.08838834764831845f;
     CHECK_ATTN(attn_fwd(q, k, v, o1, l1, B, Hq, Hkv, S, S, D, ATTN_LAYOUT_BSHD, 1, scale, NULL));
-    CHECK_ATTN(attn_fwd_simple(q, k, v, o2, l2, B, Hq, Hkv, S, S, D, ATTN_LAYOUT_BSHD, 1, scale, NULL));
     int site = 0;
     CHECK_ATTN(attn_get_device_status(NULL, &site));
-    uint16_t *ho1 = (uint16_t *)malloc(nq * 2), *ho2 = (uint16_t *)malloc(nq * 2);
+    uint16_t *ho1 = (uint16_t *)malloc(nq * 2);
+    float *hl1 = (float *)malloc((size_t)B * Hq * S * 4);
     CHECK_CUDA(cudaMemcpy(ho1, o1, nq * 2, cudaMemcpyDeviceToHost));
-    CHECK_CUDA(cudaMemcpy(ho2, o2, nq * 2, cudaMemcpyDeviceToHost));
-    size_t bad = 0;
-    for (size_t i = 0; i < nq; ++i)
-        if (!within(from_bf16(ho1[i]), from_bf16(ho2[i]))) ++bad;
-    printf("prefill: %zu of %zu elements differ from the SIMT cross-check\n", bad, nq);
-    if (bad) return 1;
+    CHECK_CUDA(cudaMemcpy(hl1, l1, (size_t)B * Hq * S * 4, cudaMemcpyDeviceToHost));
+    size_t bad = 0, bad_lse = 0;
+    double *sc = (double *)malloc(sizeof(double) * 512);
+    for (int b = 0; b < B; ++b)
+        for (int i = 0; i < S; ++i)
+            for (int h = 0; h < Hq; ++h) {
+                /* row (b, i, h) of a BSHD tensor; causal, Sq == Sk: keys 0 .. i */
+                const int g = h / (Hq / Hkv);
+                const size_t qrow = (((size_t)b * S + i) * Hq + h) * D;
+                double m = -INFINITY, l = 0.0, o[128] = {0};
+                for (int j = 0; j <= i; ++j) {
+                    const size_t krow = (((size_t)b * S + j) * Hkv + g) * D;
+                    double s = 0.0;
+                    for (int c = 0; c < D; ++c) s += from_bf16(hq[qrow + c]) * from_bf16(hk[krow + c]);
+                    sc[j] = s * scale;
+                    if (sc[j] > m) m = sc[j];
+                }
+                for (int j = 0; j <= i; ++j) {
+                    const size_t vrow = (((size_t)b * S + j) * Hkv + g) * D;
+                    const double w = exp(sc[j] - m);
+                    l += w;
+                    for (int c = 0; c < D; ++c) o[c] += w * from_bf16(hv[vrow + c]);
+                }
+                for (int c = 0; c < D; ++c)
+                    if (!within(from_bf16(ho1[qrow + c]), o[c] / l)) ++bad;
+                if (fabs((double)hl1[((size_t)b * Hq + h) * S + i] - (m + log(l))) > 1e-3) ++bad_lse;
+            }
+    printf("prefill: %zu of %zu elements differ from the host reference (lse: %zu rows)\n", bad, nq, bad_lse);
+    if (bad || bad_lse) return 1;
 
     /* ---- paged decode: 3 sequences, Hq=8, Hkv=2, 16-token pages in reverse order */
     const int DB = 3, PS = 16, MAXB = 8;
@@ -128,7 +151,6 @@ int main(void) {
     uint16_t *hdo = (uint16_t *)malloc(ndq * 2);
     CHECK_CUDA(cudaMemcpy(hdo, dout, ndq * 2, cudaMemcpyDeviceToHost));
     bad = 0;
-    double *sc = (double *)malloc(sizeof(double) * 128);
     for (int b = 0; b < DB; ++b)
         for (int h = 0; h < Hq; ++h) {
             const int g = h / (Hq / Hkv);

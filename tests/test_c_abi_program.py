@@ -1,8 +1,8 @@
 """The library used from plain C: tests/c_abi_check.c includes only
 include/attn.h and the CUDA runtime header, links libattn.so, and checks a
-prefill against the SIMT cross-check and a paged decode step against a
-host reference of its own.  On CPU the program must compile and link; on a
-GPU it must run and exit 0."""
+causal GQA prefill and a paged decode step, each against a double-precision
+host reference of its own written from the definition.  On CPU the program
+must compile and link; on a GPU it must run and exit 0."""
 import os
 import shutil
 import subprocess
