@@ -35,13 +35,27 @@
  * style tail split of the MoonMath HIP kernel page), and paged-KV decode with
  * an int32 block table (the ROCm port page, "Vendor-Agnostic 多查询推理优化").
  */
-#include <math.h>
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
+#include <tgmath.h>
 #ifdef _OPENMP
 #include <omp.h>
 #endif
+
+/*
+ * The number type of the whole-row definition (attend_row, behind
+ * oracle_attention and oracle_attention_rows).  Double unless built with
+ * -DORACLE_REAL=float: the test suite builds that single-precision copy only
+ * to check that the fp64 results sit far inside the parity tolerance of any
+ * rounding of the same steps (an oracle whose numbers depended on the last
+ * bits of its arithmetic could not judge a bf16 kernel).  <tgmath.h> makes
+ * exp and log follow the argument's type.
+ */
+#ifndef ORACLE_REAL
+#define ORACLE_REAL double
+#endif
+typedef ORACLE_REAL oreal;
 
 #define ORACLE_OK 0
 #define ORACLE_BAD_ARG -1
@@ -97,41 +111,43 @@ static int check_problem(const problem_t *p) {
 
 /*
  * One query row over the keys [klo, khi) that it may see, straight from the
- * definition.  scores: scratch of at least Sk doubles.  Writes d outputs and
- * the row's log-sum-exp.
+ * definition.  scores: scratch of at least Sk values; acc: scratch of d
+ * values.  Writes d outputs and the row's log-sum-exp.  (bf16 inputs are
+ * exact in either number type.)
  */
 static void attend_row(const problem_t *p, int64_t b, int64_t h, int64_t i,
-                       int64_t klo, int64_t khi, double *scores,
+                       int64_t klo, int64_t khi, oreal *scores, oreal *acc,
                        double *o, double *lse) {
     const int64_t g = h / (p->Hq / p->Hkv);
     const int64_t d = p->d;
     int64_t last = last_visible_key(p->causal, i, p->Sq, p->Sk);
     if (khi > last + 1) khi = last + 1;
     if (klo < 0) klo = 0;
-    for (int64_t c = 0; c < d; ++c) o[c] = 0.0;
+    for (int64_t c = 0; c < d; ++c) acc[c] = 0.0;
     if (khi <= klo) {
+        for (int64_t c = 0; c < d; ++c) o[c] = 0.0;
         *lse = -INFINITY;
         return;
     }
-    double M = -INFINITY;
+    oreal M = -INFINITY;
     for (int64_t j = klo; j < khi; ++j) {
-        double dot = 0.0;
+        oreal dot = 0.0;
         for (int64_t c = 0; c < d; ++c) {
-            double qv = bf16_to_double(p->q[offset_of(p->layout, b, i, h, c, p->Sq, p->Hq, d)]);
-            double kv = bf16_to_double(p->k[offset_of(p->layout, b, j, g, c, p->Sk, p->Hkv, d)]);
+            oreal qv = (oreal)bf16_to_double(p->q[offset_of(p->layout, b, i, h, c, p->Sq, p->Hq, d)]);
+            oreal kv = (oreal)bf16_to_double(p->k[offset_of(p->layout, b, j, g, c, p->Sk, p->Hkv, d)]);
             dot += qv * kv;
         }
-        scores[j] = p->scale * dot;
+        scores[j] = (oreal)p->scale * dot;
         if (scores[j] > M) M = scores[j];
     }
-    double L = 0.0;
+    oreal L = 0.0;
     for (int64_t j = klo; j < khi; ++j) {
-        double w = exp(scores[j] - M);
+        oreal w = exp(scores[j] - M);
         L += w;
         for (int64_t c = 0; c < d; ++c)
-            o[c] += w * bf16_to_double(p->v[offset_of(p->layout, b, j, g, c, p->Sk, p->Hkv, d)]);
+            acc[c] += w * (oreal)bf16_to_double(p->v[offset_of(p->layout, b, j, g, c, p->Sk, p->Hkv, d)]);
     }
-    for (int64_t c = 0; c < d; ++c) o[c] /= L;
+    for (int64_t c = 0; c < d; ++c) o[c] = acc[c] / L;
     *lse = M + log(L);
 }
 
@@ -149,9 +165,10 @@ int oracle_attention(const uint16_t *q, const uint16_t *k, const uint16_t *v,
     int failed = 0;
 #pragma omp parallel
     {
-        double *scores = (double *)malloc(sizeof(double) * (size_t)Sk);
+        oreal *scores = (oreal *)malloc(sizeof(oreal) * (size_t)Sk);
+        oreal *acc = (oreal *)malloc(sizeof(oreal) * (size_t)d);
         double *orow = (double *)malloc(sizeof(double) * (size_t)d);
-        if (!scores || !orow) {
+        if (!scores || !acc || !orow) {
 #pragma omp atomic write
             failed = 1;
         } else {
@@ -159,12 +176,13 @@ int oracle_attention(const uint16_t *q, const uint16_t *k, const uint16_t *v,
             for (int64_t r = 0; r < nrows; ++r) {
                 int64_t b = r / (Hq * Sq), h = (r / Sq) % Hq, i = r % Sq;
                 double l;
-                attend_row(&p, b, h, i, 0, Sk, scores, orow, &l);
+                attend_row(&p, b, h, i, 0, Sk, scores, acc, orow, &l);
                 for (int64_t c = 0; c < d; ++c) out[offset_of(layout, b, i, h, c, Sq, Hq, d)] = orow[c];
                 if (lse) lse[(b * Hq + h) * Sq + i] = l;
             }
         }
         free(scores);
+        free(acc);
         free(orow);
     }
     return failed ? ORACLE_NO_MEMORY : ORACLE_OK;
@@ -191,18 +209,20 @@ int oracle_attention_rows(const uint16_t *q, const uint16_t *k, const uint16_t *
     int failed = 0;
 #pragma omp parallel
     {
-        double *scores = (double *)malloc(sizeof(double) * (size_t)Sk);
-        if (!scores) {
+        oreal *scores = (oreal *)malloc(sizeof(oreal) * (size_t)Sk);
+        oreal *acc = (oreal *)malloc(sizeof(oreal) * (size_t)d);
+        if (!scores || !acc) {
 #pragma omp atomic write
             failed = 1;
         } else {
 #pragma omp for schedule(dynamic, 1)
             for (int64_t r = 0; r < n; ++r) {
                 const int64_t *t = rows + 3 * r;
-                attend_row(&p, t[0], t[1], t[2], klo, khi, scores, out + r * d, lse + r);
+                attend_row(&p, t[0], t[1], t[2], klo, khi, scores, acc, out + r * d, lse + r);
             }
         }
         free(scores);
+        free(acc);
     }
     return failed ? ORACLE_NO_MEMORY : ORACLE_OK;
 }

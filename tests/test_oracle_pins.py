@@ -303,6 +303,33 @@ def test_probability_rows_sum_to_one():
                 assert (p[i + 1:] == 0).all()
 
 
+def _sdpa_weights(q, k, causal, scale):
+    """Attention weights P from torch's scaled_dot_product_attention in fp64:
+    with the identity matrix as V (one value column per key) its output row
+    is the row of P itself.  q [Sq, d], k [Sk, d]; bottom-right causal mask."""
+    q, k = q.to(torch.float64), k.to(torch.float64)
+    Sq, Sk = q.shape[0], k.shape[0]
+    eye = torch.eye(Sk, dtype=torch.float64)
+    mask = None
+    if causal:
+        mask = torch.arange(Sk)[None, :] <= torch.arange(Sq)[:, None] + (Sk - Sq)
+    return torch.nn.functional.scaled_dot_product_attention(q[None, None], k[None, None], eye[None, None],
+                                                            attn_mask=mask, scale=scale)[0, 0].numpy()
+
+
+@pytest.mark.parametrize("Sq,Sk,causal,scale", [(29, 29, False, 0.5), (29, 29, True, 0.5), (7, 40, True, 0.13),
+                                                  (12, 9, False, 1.7)])
+def test_probability_row_matches_sdpa_weights(Sq, Sk, causal, scale):
+    d, Hq, Hkv = 16, 4, 2
+    q, k = rand_bf16((1, Sq, Hq, d), 41, std=3.0), rand_bf16((1, Sk, Hkv, d), 42, std=3.0)
+    for h in (0, 1, 3):     # h = 1 tells h / G from h % Hkv apart
+        ref = _sdpa_weights(q[0, :, h], k[0, :, h // 2], causal, scale)
+        for i in (0, Sq // 2, Sq - 1):
+            p = oracle.attention_probs_row(q, k, 0, h, i, B=1, Hq=Hq, Hkv=Hkv, Sq=Sq, Sk=Sk, d=d,
+                                           causal=causal, scale=scale)
+            np.testing.assert_allclose(p, ref[i], rtol=1e-10, atol=1e-14, err_msg=f"h={h} i={i}")
+
+
 def test_fully_masked_rows_are_zero_with_minus_inf_lse():
     Sq, Sk, d = 10, 4, 8          # causal with Sq > Sk: rows i < Sq - Sk see no key
     q, k, v = rand_bf16((1, Sq, 1, d), 19), rand_bf16((1, Sk, 1, d), 20), rand_bf16((1, Sk, 1, d), 21)
@@ -514,14 +541,16 @@ MUTATIONS = {
     # top-left causal alignment instead of bottom-right
     "causal_top_left": ("int64_t lim = i + Sk - Sq;", "int64_t lim = i;"),
     # sign error in the exponent
-    "exp_sign": ("double w = exp(scores[j] - M);", "double w = exp(M - scores[j]);"),
+    "exp_sign": ("oreal w = exp(scores[j] - M);", "oreal w = exp(M - scores[j]);"),
     # dropped normalisation
-    "no_normalise": ("for (int64_t c = 0; c < d; ++c) o[c] /= L;", ";"),
+    "no_normalise": ("for (int64_t c = 0; c < d; ++c) o[c] = acc[c] / L;",
+                     "for (int64_t c = 0; c < d; ++c) o[c] = acc[c];"),
     # lse off by the log term
     "lse_sign": ("*lse = M + log(L);", "*lse = M - log(L);"),
     # transposed operand: key index used for the value row
-    "value_from_query_row": ("o[c] += w * bf16_to_double(p->v[offset_of(p->layout, b, j, g, c, p->Sk, p->Hkv, d)]);",
-                             "o[c] += w * bf16_to_double(p->v[offset_of(p->layout, b, i < p->Sk ? i : 0, g, c, p->Sk, p->Hkv, d)]);"),
+    "value_from_query_row": (
+        "acc[c] += w * (oreal)bf16_to_double(p->v[offset_of(p->layout, b, j, g, c, p->Sk, p->Hkv, d)]);",
+        "acc[c] += w * (oreal)bf16_to_double(p->v[offset_of(p->layout, b, i < p->Sk ? i : 0, g, c, p->Sk, p->Hkv, d)]);"),
 }
 
 
@@ -595,3 +624,71 @@ def test_planted_mistake_is_caught(name, tmp_path):
     assert failures, f"no pin caught the planted mistake {name}"
     # and the real oracle passes the same suite
     assert not _pin_suite()
+
+
+PROBS_MUTATIONS = {
+    # scale dropped from the probability row's scores
+    "probs_no_scale": ("probs[j] = scale * dot;", "probs[j] = dot;"),
+    # wrong head map in the probability row
+    "probs_head_map": ("const int64_t g = h / (Hq / Hkv);\n    int64_t last", "const int64_t g = h % Hkv;\n    int64_t last"),
+    # unnormalised probabilities
+    "probs_no_normalise": ("probs[j] = exp(probs[j] - M) / L;", "probs[j] = exp(probs[j] - M);"),
+}
+
+
+def _probs_pin_suite():
+    failures = []
+    for fn in (lambda: test_probability_row_matches_sdpa_weights(29, 29, True, 0.5),
+               lambda: test_probability_row_matches_sdpa_weights(7, 40, True, 0.13)):
+        try:
+            fn()
+        except AssertionError:
+            failures.append(fn)
+    return failures
+
+
+@pytest.mark.skipif(shutil.which("gcc") is None, reason="needs gcc")
+@pytest.mark.parametrize("name", sorted(PROBS_MUTATIONS))
+def test_planted_probability_row_mistake_is_caught(name, tmp_path):
+    src = open(os.path.join(os.path.dirname(oracle.__file__), "attn_oracle.c")).read()
+    old, new = PROBS_MUTATIONS[name]
+    assert old in src, f"mutation anchor for {name} not found"
+    bad = tmp_path / "bad.c"
+    bad.write_text(src.replace(old, new, 1))
+    so = tmp_path / "libbad.so"
+    subprocess.run(["gcc", "-O1", "-fopenmp", "-shared", "-fPIC", "-o", str(so), str(bad), "-lm"], check=True)
+    with oracle.use_library(str(so)):
+        failures = _probs_pin_suite()
+    assert failures, f"no pin caught the planted mistake {name}"
+    assert not _probs_pin_suite()
+
+
+# ---------------------------------------------------------------- the oracle's own numerics
+
+@pytest.mark.skipif(shutil.which("gcc") is None, reason="needs gcc")
+def test_fp32_build_agrees_with_fp64_far_inside_the_tolerance(tmp_path):
+    """The same oracle source built with ORACLE_REAL=float: on workload-like
+    inputs (unit normal, and peaked rows from keys scaled by 8) its results
+    differ from the fp64 build by at most 5% of the parity tolerance
+    (4e-3 + 8e-3 |O|, 1e-3 on lse); the fp64 build's own rounding error is
+    about 2^29 times smaller still, so it cannot decide a parity verdict."""
+    so = tmp_path / "liboracle32.so"
+    subprocess.run(["gcc", "-O2", "-fopenmp", "-shared", "-fPIC", "-std=c11", "-DORACLE_REAL=float", "-o", str(so),
+                    os.path.join(os.path.dirname(oracle.__file__), "attn_oracle.c"), "-lm"], check=True)
+    cases = [inputs.PrefillWorkload("f32a", 1, 4, 2, 700, 700, causal=True, seed=51),
+             inputs.PrefillWorkload("f32b", 1, 2, 2, 300, 1500, causal=False, seed=52)]
+    for w in cases:
+        q, k, v = inputs.make_prefill(w)
+        if w.name == "f32b":       # a few keys scaled by 8: peaked softmax rows
+            k = k.float()
+            k[:, ::97] *= 8
+            k = k.to(torch.bfloat16)
+        kw = dict(B=w.B, Hq=w.Hq, Hkv=w.Hkv, Sq=w.Sq, Sk=w.Sk, d=w.d, layout=w.layout, causal=w.causal, scale=w.scale)
+        o64, l64 = oracle.attention(q, k, v, **kw)
+        with oracle.use_library(str(so)):
+            o32, l32 = oracle.attention(q, k, v, **kw)
+        assert not np.array_equal(o32, o64), "the float build should round differently"
+        excess = np.abs(o32 - o64) / (4e-3 + 8e-3 * np.abs(o64))
+        # at most 5% of either tolerance
+        assert excess.max() < 0.05, f"{w.name}: fp32 build uses {excess.max():.3g} of the tolerance"
+        assert np.abs(l32 - l64).max() < 5e-5, f"{w.name}: lse differs by {np.abs(l32 - l64).max():.3g}"
