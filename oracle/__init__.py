@@ -8,11 +8,15 @@ never imports the product: they share no code.
 The arithmetic lives in ``attn_oracle.c`` (plain C, double precision,
 OpenMP over rows); this module compiles it with gcc on first use and wraps it
 with numpy.  Inputs are bf16 bit patterns (``numpy.uint16``), widened to
-double exactly inside the C code.
+double exactly inside the C code.  One function is written here instead:
+``attention_matmul``, the same definition with its two contractions as fp64
+matrix products (plain torch CPU ops), for checking whole full-size outputs;
+it shares no code with the C functions and is pinned against them.
 """
 from __future__ import annotations
 
 import ctypes
+import math
 import os
 import subprocess
 import threading
@@ -146,7 +150,79 @@ def attention(q, k, v, *, B, Hq, Hkv, Sq, Sk, d=128, layout="bshd", causal=False
     return out, lse
 
 
-def attention_varlen(q, k, v, cu_q, cu_k, *, Hq, Hkv, d=128, causal=False, scale, seqs=None):
+def _f64_tensor(a):
+    """bf16 data (a torch bf16 tensor or uint16 bit patterns) as a float64 CPU tensor (exact)."""
+    import torch
+    if isinstance(a, torch.Tensor):
+        return a.detach().cpu().to(torch.float64)
+    bits = np.ascontiguousarray(a)
+    if bits.dtype != np.uint16:
+        raise TypeError(f"expected bf16 bit patterns (uint16), got {bits.dtype}")
+    return torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(torch.float64)
+
+
+def attention_matmul(q, k, v, *, B, Hq, Hkv, Sq, Sk, d=128, layout="bshd", causal=False, scale, row_block=1024):
+    """The definition attention() computes, with its two contractions done as
+    fp64 matrix products on the CPU (torch, all cores): for each batch b, head h
+    (kv head g = h // (Hq / Hkv)) and block of query rows,
+
+        S   = scale * Q K_g^T, with S[i, j] = -inf where key j is not visible to
+              row i (causal: j > i + Sk - Sq, bottom-right alignment),
+        M   = max_j S[i, j],      P = exp(S - M),      L = sum_j P[i, j],
+        O   = (P V_g) / L,        lse = M + ln L,
+
+    and a row that sees no key gives O = 0, lse = -inf.  The matrix product is
+    a library step of the definition; a block of rows is only a batch of
+    independent rows, and its product runs over the keys [0, kn) that some
+    row of the block may see (the rest would only be masked); nothing is
+    tiled over keys or reordered.  It exists for
+    parity checks of whole full-size outputs, where the row-by-row C code would
+    take minutes.  Returns (out in q's layout, lse [B, Hq, Sq]) as float64 numpy.
+    """
+    import torch
+    q64, k64, v64 = _f64_tensor(q), _f64_tensor(k), _f64_tensor(v)
+    bshd = LAYOUTS[layout] == 0
+    G = Hq // Hkv
+    out = torch.empty((B, Sq, Hq, d) if bshd else (B, Hq, Sq, d), dtype=torch.float64)
+    lse = torch.empty((B, Hq, Sq), dtype=torch.float64)
+    keys = torch.arange(Sk)[None, :]
+    for b in range(B):
+        for g in range(Hkv):
+            kg = (k64[b, :, g] if bshd else k64[b, g]).contiguous()   # [Sk, d]
+            vg = (v64[b, :, g] if bshd else v64[b, g]).contiguous()
+            for h in range(g * G, (g + 1) * G):
+                qh = (q64[b, :, h] if bshd else q64[b, h]).contiguous()  # [Sq, d]
+                for r0 in range(0, Sq, row_block):
+                    r1 = min(Sq, r0 + row_block)
+                    # keys [0, kn) are the ones any row of the block may see
+                    kn = min(Sk, r1 + Sk - Sq) if causal else Sk
+                    if kn <= 0:
+                        if bshd:
+                            out[b, r0:r1, h] = 0.0
+                        else:
+                            out[b, h, r0:r1] = 0.0
+                        lse[b, h, r0:r1] = -math.inf
+                        continue
+                    s = (qh[r0:r1] @ kg[:kn].T) * scale
+                    if causal:
+                        rows = torch.arange(r0, r1)[:, None]
+                        s.masked_fill_(keys[:, :kn] > rows + (Sk - Sq), -math.inf)
+                    m = s.amax(dim=1, keepdim=True)
+                    none = torch.isneginf(m)                       # rows that see no key
+                    m_sub = torch.where(none, torch.zeros_like(m), m)
+                    p = s.sub_(m_sub).exp_()                       # masked keys: exp(-inf) = 0
+                    l_sum = p.sum(dim=1, keepdim=True)
+                    o = (p @ vg[:kn]) / l_sum
+                    o[none[:, 0]] = 0.0
+                    if bshd:
+                        out[b, r0:r1, h] = o
+                    else:
+                        out[b, h, r0:r1] = o
+                    lse[b, h, r0:r1] = (m_sub + torch.log(l_sum))[:, 0]
+    return out.numpy(), lse.numpy()
+
+
+def attention_varlen(q, k, v, cu_q, cu_k, *, Hq, Hkv, d=128, causal=False, scale, seqs=None, dense=None):
     """A packed variable-length batch, one sequence at a time.
 
     q [total_q, Hq, d], k and v [total_k, Hkv, d] (bf16); sequence b owns rows
@@ -158,8 +234,10 @@ def attention_varlen(q, k, v, cu_q, cu_k, *, Hq, Hkv, d=128, causal=False, scale
 
     Returns (out [total_q, Hq, d] float64, lse [Hq, total_q] float64); rows
     that belong to no sequence (or to a sequence not in `seqs`, when given)
-    are NaN.
+    are NaN.  `dense` picks the dense implementation used per sequence:
+    attention (default) or attention_matmul.
     """
+    dense = attention if dense is None else dense
     cu_q = [int(x) for x in cu_q]
     cu_k = [int(x) for x in cu_k]
     total_q = q.shape[0]
@@ -173,8 +251,8 @@ def attention_varlen(q, k, v, cu_q, cu_k, *, Hq, Hkv, d=128, causal=False, scale
             out[q0:q1] = 0.0
             lse[:, q0:q1] = -np.inf
             continue
-        o_b, l_b = attention(q[q0:q1][None], k[k0:k1][None], v[k0:k1][None], B=1, Hq=Hq, Hkv=Hkv,
-                             Sq=q1 - q0, Sk=k1 - k0, d=d, causal=causal, scale=scale)
+        o_b, l_b = dense(q[q0:q1][None], k[k0:k1][None], v[k0:k1][None], B=1, Hq=Hq, Hkv=Hkv,
+                         Sq=q1 - q0, Sk=k1 - k0, d=d, causal=causal, scale=scale)
         out[q0:q1] = o_b[0]
         lse[:, q0:q1] = l_b[0]
     return out, lse
@@ -192,7 +270,7 @@ def gather_pages(pages, block_table_row, L, page_size=16):
 
 
 def attention_paged(q, k_pages, v_pages, block_table, seqlens_k, cu_q, *, Hq, Hkv, d=128, causal=False, scale,
-                    page_size=16, seqs=None):
+                    page_size=16, seqs=None, dense=None):
     """Prefill of packed query chunks against a paged KV cache.
 
     Sequence b has seqlens_k[b] cached keys, key t at slot t % 16 of page
@@ -200,7 +278,9 @@ def attention_paged(q, k_pages, v_pages, block_table, seqlens_k, cu_q, *, Hq, Hk
     of q [total_q, Hq, d]; causal alignment is bottom-right (the chunk is the
     cache's last tokens).  Each sequence is gathered into contiguous K, V and
     run through the plain attention above.  Returns (out [total_q, Hq, d],
-    lse [Hq, total_q]) in float64, NaN for rows of no sequence."""
+    lse [Hq, total_q]) in float64, NaN for rows of no sequence.  `dense` as in
+    attention_varlen."""
+    dense = attention if dense is None else dense
     cu_q = [int(x) for x in cu_q]
     lens = [int(x) for x in seqlens_k]
     bt = np.asarray(block_table)
@@ -217,8 +297,8 @@ def attention_paged(q, k_pages, v_pages, block_table, seqlens_k, cu_q, *, Hq, Hk
             continue
         k_b = gather_pages(k_pages, bt[b], Lk, page_size)
         v_b = gather_pages(v_pages, bt[b], Lk, page_size)
-        o_b, l_b = attention(q[q0:q1][None], k_b[None], v_b[None], B=1, Hq=Hq, Hkv=Hkv, Sq=q1 - q0, Sk=Lk, d=d,
-                             causal=causal, scale=scale)
+        o_b, l_b = dense(q[q0:q1][None], k_b[None], v_b[None], B=1, Hq=Hq, Hkv=Hkv, Sq=q1 - q0, Sk=Lk, d=d,
+                         causal=causal, scale=scale)
         out[q0:q1] = o_b[0]
         lse[:, q0:q1] = l_b[0]
     return out, lse

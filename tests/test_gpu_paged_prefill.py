@@ -120,27 +120,18 @@ def test_bad_table_entry_is_reported_without_a_fault(A):
     _run_and_compare(A, w, (q, kp, vp, table, lens, cu_q), "after bad table")
 
 
-def test_full_workload_sampled_rows(A):
+def test_full_workload_every_output(A):
     w = inputs.PAGED_PREFILL
     q, kp, vp, table, lens, cu_q = inputs.make_paged_prefill(w)
     out, lse = A.fwd_paged(q.cuda(), kp.cuda(), vp.cuda(), table.cuda(), lens.cuda(), cu_q.cuda(), causal=True,
                            scale=w.scale)
     torch.cuda.synchronize()
     assert A.device_status()[0] == 0
-    out, lse = out.cpu(), lse.cpu()
-    assert torch.isfinite(out.float()).all()
-    lq, lk = w.lengths()
-    rng = np.random.default_rng(105)
-    for b in sorted({0, int(np.argmax(lk)), int(np.argmin(lq)), w.B - 1}):
-        q0, Lq, Lk = int(cu_q[b]), lq[b], lk[b]
-        k_b = oracle.gather_pages(kp, table[b], Lk)
-        v_b = oracle.gather_pages(vp, table[b], Lk)
-        rows_i = sorted(({0, 1, 127, 128, Lq // 2, Lq - 1} & set(range(Lq))) | set(rng.integers(0, Lq, 6).tolist()))
-        rows = np.array([(0, h, i) for h in (0, 9, 31) for i in rows_i], dtype=np.int64)
-        ref_o, ref_l = oracle.attention_rows(q[q0:q0 + Lq][None], k_b[None], v_b[None], rows, B=1, Hq=w.Hq,
-                                             Hkv=w.Hkv, Sq=Lq, Sk=Lk, causal=True, scale=w.scale)
-        check_out(out[torch.from_numpy(q0 + rows[:, 2]), torch.from_numpy(rows[:, 1])], ref_o, f"paged seq {b}")
-        check_lse(lse[torch.from_numpy(rows[:, 1]), torch.from_numpy(q0 + rows[:, 2])], ref_l, f"paged seq {b}")
+    ref_o, ref_l = oracle.attention_paged(q, kp, vp, table, lens, cu_q, Hq=w.Hq, Hkv=w.Hkv, causal=True,
+                                          scale=w.scale, dense=oracle.attention_matmul)
+    assert not np.isnan(ref_l).any()
+    check_out(out.cpu(), ref_o, w.name)
+    check_lse(lse.cpu(), ref_l, w.name)
 
 
 def test_runs_of_consecutive_pages_mixed_with_scattered_ones(A):

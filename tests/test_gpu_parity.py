@@ -1,8 +1,8 @@
 """GPU parity: the CUDA path (through the C ABI) against the fp64 CPU oracle.
 
 Every comparison is element-wise at |O - O_ref| <= 4e-3 + 8e-3 |O_ref| and
-|lse - lse_ref| <= 1e-3.  Small shapes are compared in full; the full-size
-workloads are compared on sampled rows the oracle computes one by one.
+|lse - lse_ref| <= 1e-3.  Small shapes and the full-size workloads are both
+compared in full: every output element and every lse.
 """
 import math
 
@@ -175,24 +175,45 @@ def test_output_guard_regions_untouched(A):
     check_lse(lse, ref_l, "guard")
 
 
-# ---------------------------------------------------------------- full-size workloads, sampled rows
+# ---------------------------------------------------------------- full-size workloads, every output
 
-FULL = [inputs.GQA_CAUSAL, inputs.MQA_CAUSAL, inputs.RAGGED_SELF, inputs.RAGGED_CROSS, inputs.TINY_BHSD]
+FULL = [inputs.TINY_BHSD, inputs.GQA_CAUSAL, inputs.MQA_CAUSAL, inputs.RAGGED_SELF, inputs.RAGGED_CROSS]
+
+
+def _run_as_benched(A, w, q, k, v):
+    """One call in the launch configuration the benchmark times: the tail-split
+    workspace registered whenever the shape gets a split on this device."""
+    dq, dk, dv = (t.cuda() for t in (q, k, v))
+    n = A.fwd_workspace_bytes(w.B, w.Hq, w.Hkv, w.Sq, w.Sk, w.d, w.causal)
+    ws = torch.empty(n, device="cuda", dtype=torch.uint8) if n else None
+    A.set_workspace(ws)
+    try:
+        out, lse = A.fwd(dq, dk, dv, causal=w.causal, scale=w.scale, layout=w.layout)
+        torch.cuda.synchronize()
+    finally:
+        A.set_workspace(None)
+    return out, lse, n
 
 
 @pytest.mark.parametrize("w", FULL, ids=[w.name for w in FULL])
-def test_full_size_sampled_rows(A, w):
+def test_full_size_every_output(A, w):
+    """Every element of O and every lse of the full-size workloads against the
+    fp64 oracle (its matmul form, all host cores), plus a cross-check of that
+    form against the row-by-row oracle on sampled rows at the same size."""
     q, k, v = inputs.make_prefill(w)
-    out, lse = _run(A, w, q, k, v)
+    out, lse, ws_bytes = _run_as_benched(A, w, q, k, v)
+    assert A.device_status()[0] == 0
+    kw = dict(B=w.B, Hq=w.Hq, Hkv=w.Hkv, Sq=w.Sq, Sk=w.Sk, d=w.d, layout=w.layout, causal=w.causal, scale=w.scale)
+    ref_o, ref_l = oracle.attention_matmul(q, k, v, **kw)
+    out_c, lse_c = out.cpu(), lse.cpu()
+    for b in range(w.B):   # one batch at a time keeps the host copies small
+        check_out(out_c[b], ref_o[b], f"{w.name} batch {b} (tail split: {bool(ws_bytes)})")
+        check_lse(lse_c[b], ref_l[b], f"{w.name} batch {b}")
     rows = sample_rows(w.B, w.Hq, w.Sq, w.Hq // w.Hkv, seed=w.seed)
-    ref_o, ref_l = oracle.attention_rows(q, k, v, rows, B=w.B, Hq=w.Hq, Hkv=w.Hkv, Sq=w.Sq, Sk=w.Sk, d=w.d,
-                                         layout=w.layout, causal=w.causal, scale=w.scale)
-    o_rows, l_rows = gather_rows(out, lse, rows, w.layout)
-    check_out(o_rows, ref_o, w.name)
-    check_lse(l_rows, ref_l, w.name)
-    # properties over the whole output
-    assert torch.isfinite(out).all()
-    assert torch.isfinite(lse).all()
+    row_o, row_l = oracle.attention_rows(q, k, v, rows, **kw)
+    mm_o, mm_l = gather_rows(torch.from_numpy(ref_o), torch.from_numpy(ref_l), rows, w.layout)
+    np.testing.assert_allclose(mm_o.numpy(), row_o, rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(mm_l.numpy(), row_l, rtol=0, atol=1e-10)
 
 
 def test_gqa_workload_deterministic(A):

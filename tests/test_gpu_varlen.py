@@ -134,24 +134,14 @@ def test_bad_offsets_are_reported_without_a_fault(A):
     assert A.device_status()[0] == 0
 
 
-def test_full_workload_sampled_rows(A):
+def test_full_workload_every_output(A):
     w = inputs.VARLEN_CAUSAL
     q, k, v, cu_q, cu_k = inputs.make_varlen(w)
     out, lse = A.fwd_varlen(q.cuda(), k.cuda(), v.cuda(), cu_q.cuda(), cu_k.cuda(), causal=True, scale=w.scale)
     torch.cuda.synchronize()
     assert A.device_status()[0] == 0
-    out, lse = out.cpu(), lse.cpu()
-    assert torch.isfinite(out.float()).all()
-    lq, _ = w.lengths()
-    rng = np.random.default_rng(96)
-    for b in sorted({0, int(np.argmax(lq)), int(np.argmin(lq)), w.B - 1}):
-        q0, L = int(cu_q[b]), lq[b]
-        rows_i = sorted({0, 1, 127, 128, L // 2, L - 129, L - 2, L - 1} & set(range(L)) |
-                        set(rng.integers(0, L, 6).tolist()))
-        rows = np.array([(0, h, i) for h in (0, 5, 31) for i in rows_i], dtype=np.int64)
-        ref_o, ref_l = oracle.attention_rows(q[q0:q0 + L][None], k[q0:q0 + L][None], v[q0:q0 + L][None], rows,
-                                             B=1, Hq=w.Hq, Hkv=w.Hkv, Sq=L, Sk=L, causal=True, scale=w.scale)
-        got_o = out[torch.from_numpy(q0 + rows[:, 2]), torch.from_numpy(rows[:, 1])]
-        got_l = lse[torch.from_numpy(rows[:, 1]), torch.from_numpy(q0 + rows[:, 2])]
-        check_out(got_o, ref_o, f"varlen workload seq {b}")
-        check_lse(got_l, ref_l, f"varlen workload seq {b}")
+    ref_o, ref_l = oracle.attention_varlen(q, k, v, cu_q, cu_k, Hq=w.Hq, Hkv=w.Hkv, causal=True, scale=w.scale,
+                                           dense=oracle.attention_matmul)
+    assert not np.isnan(ref_l).any()   # the workload's sequences cover every row
+    check_out(out.cpu(), ref_o, w.name)
+    check_lse(lse.cpu(), ref_l, w.name)

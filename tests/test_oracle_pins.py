@@ -100,6 +100,82 @@ def test_matches_torch_sdpa_fp64(B, Hq, Hkv, Sq, Sk, causal, layout):
     np.testing.assert_allclose(out, ref, rtol=1e-10, atol=1e-12)
 
 
+# ---------------------------------------------------------------- the matmul form of the definition
+
+MATMUL_SHAPES = [
+    # B, Hq, Hkv, Sq, Sk, layout, causal
+    (2, 8, 2, 70, 70, "bshd", True),      # GQA, causal
+    (1, 6, 3, 40, 90, "bhsd", True),      # Sk > Sq: bottom-right alignment
+    (1, 2, 2, 50, 20, "bshd", True),      # Sq > Sk: rows that see no key
+    (2, 4, 1, 33, 129, "bhsd", False),    # MQA, cross
+    (1, 3, 1, 1, 64, "bshd", False),      # one query
+    (1, 2, 2, 17, 1, "bshd", False),      # one key
+]
+
+
+def _matmul_vs_c(impl, B, Hq, Hkv, Sq, Sk, layout, causal, row_block=16):
+    w = inputs.PrefillWorkload("mm", B, Hq, Hkv, Sq, Sk, d=32, layout=layout, causal=causal, seed=61 + Sq)
+    q, k, v = inputs.make_prefill(w)
+    kw = dict(B=B, Hq=Hq, Hkv=Hkv, Sq=Sq, Sk=Sk, d=32, layout=layout, causal=causal, scale=0.21)
+    o1, l1 = impl(q, k, v, row_block=row_block, **kw)
+    o2, l2 = oracle.attention(q, k, v, **kw)
+    np.testing.assert_allclose(o1, o2, rtol=1e-11, atol=1e-13)
+    assert (np.isneginf(l1) == np.isneginf(l2)).all()
+    fin = np.isfinite(l2)
+    np.testing.assert_allclose(l1[fin], l2[fin], rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("shape", MATMUL_SHAPES, ids=[str(s) for s in MATMUL_SHAPES])
+def test_matmul_form_equals_row_by_row_oracle(shape):
+    """The matmul form against the row-by-row C oracle (itself pinned by the
+    closed forms and SDPA above), with row blocks small enough that every
+    shape spans several."""
+    _matmul_vs_c(oracle.attention_matmul, *shape)
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,Sq,Sk,causal,layout", [(2, 4, 2, 33, 33, True, "bshd"),
+                                                          (1, 6, 3, 24, 31, True, "bhsd")])
+def test_matmul_form_matches_torch_sdpa_fp64(B, Hq, Hkv, Sq, Sk, causal, layout):
+    w = inputs.PrefillWorkload("t", B, Hq, Hkv, Sq, Sk, d=32, layout=layout, causal=causal, seed=11)
+    q, k, v = inputs.make_prefill(w)
+    out, _ = oracle.attention_matmul(q, k, v, B=B, Hq=Hq, Hkv=Hkv, Sq=Sq, Sk=Sk, d=32, layout=layout,
+                                     causal=causal, scale=1.0 / math.sqrt(32), row_block=8)
+    np.testing.assert_allclose(out, _sdpa_reference(q, k, v, causal, 1.0 / math.sqrt(32), layout),
+                               rtol=1e-10, atol=1e-12)
+
+
+MATMUL_MUTATIONS = {
+    "head_map_modulo": ("for h in range(g * G, (g + 1) * G):", "for h in range(g, Hq, Hkv):"),
+    "causal_top_left": ("s.masked_fill_(keys[:, :kn] > rows + (Sk - Sq), -math.inf)",
+                        "s.masked_fill_(keys[:, :kn] > rows, -math.inf)"),
+    "key_range_short": ("kn = min(Sk, r1 + Sk - Sq) if causal else Sk", "kn = min(Sk, r1 - 1 + Sk - Sq) if causal else Sk"),
+    "scale_dropped": ("s = (qh[r0:r1] @ kg[:kn].T) * scale", "s = qh[r0:r1] @ kg[:kn].T"),
+    "no_normalise": ("o = (p @ vg[:kn]) / l_sum", "o = p @ vg[:kn]"),
+    "lse_sign": ("(m_sub + torch.log(l_sum))", "(m_sub - torch.log(l_sum))"),
+    "value_of_query_head": ("vg = (v64[b, :, g] if bshd else v64[b, g]).contiguous()",
+                            "vg = (v64[b, :, 0] if bshd else v64[b, 0]).contiguous()"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MATMUL_MUTATIONS))
+def test_planted_matmul_form_mistake_is_caught(name):
+    import inspect
+    import textwrap
+    src = textwrap.dedent(inspect.getsource(oracle.attention_matmul))
+    old, new = MATMUL_MUTATIONS[name]
+    assert old in src, f"mutation anchor for {name} not found"
+    ns = dict(vars(oracle))
+    exec(compile(src.replace(old, new, 1), "<mutated attention_matmul>", "exec"), ns)
+    bad = ns["attention_matmul"]
+    caught = 0
+    for shape in MATMUL_SHAPES:
+        try:
+            _matmul_vs_c(bad, *shape)
+        except AssertionError:
+            caught += 1
+    assert caught, f"no pin caught the planted mistake {name}"
+
+
 # ---------------------------------------------------------------- packed variable-length batches
 
 @pytest.mark.parametrize("causal", [False, True])
