@@ -4,12 +4,24 @@ One step = one pass of the whole hot path: the fused prefill forward on the
 GQA causal workload (B=4, Hq=32, Hkv=8, Sq=Sk=4096, d=128, bf16, BSHD) followed
 by one paged-KV decode step (32 sequences, Hq=32, Hkv=8, lengths U[1024, 8192],
 16-token pages).  `value` is the prefill TFLOPS (4*B*Hq*Sq*Sk*d / 2 flops per
-launch, causal) over the timed steps; the decode GB/s (algorithmic K+V bytes
+launch, causal) over the K timed steps; the decode GB/s (algorithmic K+V bytes
 per launch / time) is reported beside it.  Inputs are seeded synthetic data of
 those shapes, resident in HBM when the timed region starts, and larger than
 L2 (no flush needed).
 
+Beside the headline the same line carries:
+  sustained  the same step back to back for at least a second, with its own
+             clock record, against the sustained tensor peak;
+  workloads  every other prefill workload (tiny BHSD, MQA causal, ragged self
+             and cross attention, the packed varlen batch, chunked prefill on
+             a paged cache), each launched alone after an L2 flush, with its
+             TFLOP/s, roofline fraction and the DRAM traffic of its own ncu
+             capture;
+  e2e        the headline prefill from pinned host memory through attn_fwd_host;
+  decode_append, cpu_baseline.
+
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
+                    [--no-workloads] [--no-cpu-baseline]
 
 Under torchrun (N > 1) every rank runs its own replica of the step (weak
 scaling, no collective on the data path); timing is bracketed by a barrier and
@@ -65,20 +77,24 @@ def source_hash(path):
     return hashlib.sha256(" ".join(text.split()).encode()).hexdigest()[:16]
 
 
-def traffic_for(kernel_key, src_path, units_per_launch):
-    """DRAM bytes per launch from the committed ncu summary, or None if stale/absent.
+def traffic_for(workload, src_path):
+    """DRAM bytes per launch of `workload` from its committed ncu summary, or
+    None if absent or stale.
 
-    The summary stores bytes per unit of work measured on one capture; the
-    kernel source hash recorded with it must match the current source.
+    Each entry of profiles/dram_traffic.json is keyed by workload and holds
+    dram__bytes_read.sum + dram__bytes_write.sum of one captured launch of that
+    workload, with a hash of the kernel source it was taken on; when the source
+    has changed since, the figure no longer describes the kernel and None is
+    reported until it is captured again.
     """
     try:
         with open(TRAFFIC_PATH) as f:
-            t = json.load(f)[kernel_key]
+            t = json.load(f)[workload]
     except (OSError, ValueError, KeyError):
         return None
     if t.get("source_sha256_16") != source_hash(src_path):
         return None
-    return t["bytes_per_unit"] * units_per_launch
+    return t["bytes_per_launch"]
 
 
 def reduce_max_over_ranks(x: float) -> float:
@@ -177,9 +193,6 @@ class DenseCase:
         self.flop_note = "4*B*Hq*Sq*Sk*d" + ("/2" if w.causal else "")
         self.api = "exact_attention_forward_06_gb300.fwd (C ABI attn_fwd)"
 
-    def units(self):
-        return prefill_units(self.w)
-
     def workspace_bytes(self, A):
         w = self.w
         return A.fwd_workspace_bytes(w.B, w.Hq, w.Hkv, w.Sq, w.Sk, w.d, w.causal)
@@ -210,9 +223,6 @@ class VarlenCase:
                        "layout": "thd (packed)", "causal": w.causal}
         self.flop_note = "sum over sequences of 4*Hq*Lq*Lk*d" + ("/2" if w.causal else "")
         self.api = "exact_attention_forward_06_gb300.fwd_varlen (C ABI attn_fwd_varlen)"
-
-    def units(self):
-        return None   # units differ in size: no per-unit traffic figure
 
     def workspace_bytes(self, A):
         return 0
@@ -328,10 +338,19 @@ def run_ours(args, rank, world, local_rank):
     prefill_ms = reduce_max_over_ranks(prefill_ms)
     decode_ms = reduce_max_over_ranks(decode_ms)
 
+    # The same step back to back for at least a second: the clocks and the
+    # tensor peak that hold for a kernel timed inside a long run.
+    sustained = run_sustained(prefill, decode, case.flops, total_ms / K, dev, stream, peaks, peak_src,
+                              args.sustained_seconds)
+    A.set_workspace(None)
+
     # End to end through the public API: pinned host inputs -> device -> result back to pinned host.
     e2e = run_e2e(A, case, dev, stream, args)
     # The fused append + decode step on the same decode workload (timed on its own, outside the step).
     dec_append = run_decode_append(A, wd, lens_h, dev, stream, args)
+    del dev_in, out, lse
+    # Every other prefill workload, each on its own.
+    workloads = None if args.no_workloads else run_workloads(A, args, dev, stream, peaks, peak_src, skip=case.name)
 
     if rank != 0:
         return None
@@ -340,9 +359,8 @@ def run_ours(args, rank, world, local_rank):
     per_launch_tflops = flops / (prefill_ms * 1e-3) / 1e12
     kv_bytes = inputs.decode_kv_bytes(lens_h.tolist(), wd.Hkv, wd.d)
     dec_gbs_launch = kv_bytes / (decode_ms * 1e-3) / 1e9
-    n_units = case.units()
-    traffic = traffic_for("prefill_kernel", PREFILL_KERNEL_SRC, n_units) if n_units else None
-    dec_traffic = traffic_for("decode_split_kernel", DECODE_KERNEL_SRC, sum(int(x) for x in lens_h.tolist()))
+    traffic = traffic_for(case.name, PREFILL_KERNEL_SRC)
+    dec_traffic = traffic_for(wd.name, DECODE_KERNEL_SRC)
     clk = clocks.summary()
     line = {
         "metric": "attn fwd TFLOPS (bf16, d=128) and % of GB300 bf16 peak; paged decode HBM GB/s",
@@ -367,7 +385,8 @@ def run_ours(args, rank, world, local_rank):
         "roofline": {"bound": "tensor", "achieved": round(per_launch_tflops, 2),
                      "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                      "frac": round(per_launch_tflops / peaks["bf16_tflops"], 4),
-                     "traffic": traffic, "peak_source": f"{peak_src} bf16_tflops (burst)",
+                     "traffic": traffic, "peak_source": f"{peak_src} bf16_tflops (burst: {K} steps, "
+                                                        f"{total_ms:.1f} ms timed)",
                      "kernel": "attn::g1::prefill_kernel",
                      "algorithmic": f"{flops:.4g} flop per launch ({case.flop_note})"},
         "decode": {"value": round(dec_gbs_launch * world, 1), "unit": "GB/s", "ms_per_launch": round(decode_ms, 4),
@@ -376,6 +395,8 @@ def run_ours(args, rank, world, local_rank):
                                 "traffic": dec_traffic, "peak_source": f"{peak_src} hbm_gbs",
                                 "kernel": "attn::dec::split_kernel + merge_kernel",
                                 "algorithmic": f"{kv_bytes} B K+V per launch (4096 B per token)"}},
+        "sustained": sustained,
+        "workloads": workloads,
         "decode_append": dec_append,
         "e2e": e2e,
         "gpu_launches": (4 if fws_bytes else 3) * K,
@@ -386,13 +407,102 @@ def run_ours(args, rank, world, local_rank):
     return line
 
 
-def prefill_units(w):
-    """Work units (two 128-row Q tiles) one prefill launch processes."""
-    G = w.Hq // w.Hkv
-    n_m = (w.Sq + 127) // 128
-    if G % 2 == 0:
-        return w.B * w.Hkv * (G // 2) * n_m
-    return w.B * w.Hq * ((n_m + 1) // 2)
+def run_sustained(prefill, decode, flops, step_ms, dev, stream, peaks, peak_src, seconds):
+    """The benchmark step repeated back to back for about `seconds`, timed as a
+    whole and per prefill launch, with the clocks sampled meanwhile."""
+    n = max(1, int(math.ceil(seconds * 1e3 / max(step_ms, 1e-3))))
+    pre = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(dev.index if dev.index is not None else 0) as clocks:
+        s.record(stream)
+        for a, b in pre:
+            a.record(stream)
+            prefill()
+            b.record(stream)
+            decode()
+        e.record(stream)
+        torch.cuda.synchronize(dev)
+    barrier()
+    total_ms = reduce_max_over_ranks(s.elapsed_time(e))
+    prefill_ms = reduce_max_over_ranks(sum(a.elapsed_time(b) for a, b in pre) / n)
+    tf = flops / (prefill_ms * 1e-3) / 1e12
+    peak = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
+    return {"steps": n, "seconds": round(total_ms / 1e3, 3), "ms_per_step": round(total_ms / n, 4),
+            "value": round(_world() * tf, 2), "unit": "TFLOP/s", "prefill_ms_per_launch": round(prefill_ms, 4),
+            "roofline": {"bound": "tensor", "achieved": round(tf, 2), "peak": peak, "unit": "TFLOP/s",
+                         "frac": round(tf / peak, 4),
+                         "peak_source": f"{peak_src} bf16_tflops_sustained (seconds-long run)"},
+            "clocks": clocks.summary()}
+
+
+# Prefill workloads reported beside the headline, in this order.
+OTHER_WORKLOADS = [inputs.TINY_BHSD.name, inputs.MQA_CAUSAL.name, inputs.RAGGED_SELF.name, inputs.RAGGED_CROSS.name,
+                   inputs.VARLEN_CAUSAL.name, inputs.PAGED_PREFILL.name]
+L2_FLUSH_BYTES = 256 << 20   # twice the L2
+
+
+def run_workloads(A, args, dev, stream, peaks, peak_src, skip=None):
+    """Each prefill workload launched alone: an L2 flush (a 256 MB write,
+    outside the timed events) before every launch, CUDA events around the
+    launch itself, at least `args.steps` launches and about half a second of
+    them; value, roofline fraction against the burst peak, and the DRAM
+    traffic of the workload's own ncu capture."""
+    flush = torch.empty(L2_FLUSH_BYTES, device=dev, dtype=torch.uint8)
+    result = {}
+    for name in OTHER_WORKLOADS:
+        if name == skip:
+            continue
+        case = make_case(name)
+        dev_in = [t.to(dev) for t in case.host]
+        out = torch.empty_like(dev_in[0])
+        lse = torch.empty(case.lse_shape, device=dev, dtype=torch.float32)
+        fws_bytes = case.workspace_bytes(A)
+        fws = torch.empty(fws_bytes, device=dev, dtype=torch.uint8) if fws_bytes else None
+        A.set_workspace(fws)
+
+        def one():
+            flush.fill_(1)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            case.call(A, dev_in, out, lse, stream)
+            b.record(stream)
+            return a, b
+
+        for _ in range(args.warmup):
+            one()
+        torch.cuda.synchronize(dev)
+        a, b = one()
+        torch.cuda.synchronize(dev)
+        est = max(a.elapsed_time(b), 1e-3)
+        n = max(args.steps, min(400, int(math.ceil(500.0 / (est + 0.06)))))
+        barrier()
+        with ClockSampler(dev.index if dev.index is not None else 0) as clocks:
+            evs = [one() for _ in range(n)]
+            torch.cuda.synchronize(dev)
+        barrier()
+        code, site = A.device_status()
+        A.set_workspace(None)
+        if code != 0:
+            raise RuntimeError(f"device status {code} at site {site} in workload {name}")
+        ms = reduce_max_over_ranks(sum(x.elapsed_time(y) for x, y in evs) / n)
+        tf = case.flops / (ms * 1e-3) / 1e12
+        result[name] = {
+            "value": round(_world() * tf, 2), "unit": "TFLOP/s", "ms_per_launch": round(ms, 4), "launches": n,
+            "config": case.config, "api": case.api, "tail_split_workspace_bytes": fws_bytes,
+            "l2": "flushed (256 MB write) before every timed launch",
+            "roofline": {"bound": "tensor", "achieved": round(tf, 2), "peak": peaks["bf16_tflops"],
+                         "unit": "TFLOP/s", "frac": round(tf / peaks["bf16_tflops"], 4),
+                         "traffic": traffic_for(name, PREFILL_KERNEL_SRC),
+                         "peak_source": f"{peak_src} bf16_tflops (burst: one launch at a time)",
+                         "kernel": "attn::g1::prefill_kernel",
+                         "algorithmic": f"{case.flops:.4g} flop per launch ({case.flop_note})"},
+            "clocks": clocks.summary(),
+        }
+        del dev_in, out, lse, fws
+        torch.cuda.empty_cache()
+    return result
 
 
 def run_decode_append(A, wd, lens_h, dev, stream, args):
@@ -669,7 +779,9 @@ def main(argv=None):
                     choices=sorted(inputs.PREFILL_WORKLOADS) + sorted(inputs.VARLEN_WORKLOADS) +
                     sorted(inputs.PAGED_PREFILL_WORKLOADS))
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--sustained-seconds", type=float, default=1.5)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true", help="skip the record of the other prefill workloads")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

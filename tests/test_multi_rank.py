@@ -47,14 +47,6 @@ def test_single_process_is_identity():
     assert bench.reduce_max_over_ranks(3.5) == 3.5
 
 
-def test_prefill_units_match_kernel_plan():
-    import bench
-    from exact_attention_forward_06_gb300 import inputs
-    assert bench.prefill_units(inputs.GQA_CAUSAL) == 4 * 8 * 2 * 32       # paired heads, 32 row blocks
-    assert bench.prefill_units(inputs.RAGGED_SELF) == 2 * 12 * 128        # G = 1: pairs of row blocks
-    assert bench.prefill_units(inputs.MQA_CAUSAL) == 1 * 1 * 16 * 128
-
-
 @pytest.mark.parametrize("warmup", [0, 2])
 def test_bench_rejects_short_warmup(warmup):
     import bench
@@ -75,6 +67,9 @@ def test_traffic_entry_follows_kernel_code_not_comments(tmp_path):
     assert bench.source_hash(str(src)) != h
     with open(bench.TRAFFIC_PATH) as f:
         import json
-        entry = json.load(f)["prefill_kernel"]
-    assert bench.traffic_for("prefill_kernel", str(src), 10) is None
-    assert entry["bytes_per_unit"] > 0
+        table = json.load(f)
+    # entries are keyed by workload, each a whole launch's DRAM bytes
+    name = "gqa_causal_4x32q8kv_4096"
+    assert table[name]["bytes_per_launch"] > 0
+    assert bench.traffic_for(name, str(src)) is None
+    assert bench.traffic_for("no_such_workload", bench.PREFILL_KERNEL_SRC) is None
