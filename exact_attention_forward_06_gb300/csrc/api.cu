@@ -19,6 +19,13 @@
 // Device status word: [0] = first error code recorded, [1] = wait/check site.
 __device__ unsigned int g_attn_status[2];
 
+// Work counters of the prefill launches whose CTAs claim items as they free up:
+// each launch takes the next pair (next item, CTAs done) round robin, and its
+// last CTA sets the pair back to zero.  Launches in flight at the same time on
+// one device therefore need distinct pairs: up to kSchedPairs of them.
+constexpr int kSchedPairs = 256;
+__device__ unsigned int g_prefill_sched[kSchedPairs][2];
+
 namespace {
 
 constexpr int kMaxDevices = 64;
@@ -29,6 +36,7 @@ struct DeviceInfo {
     bool supported = false;
     int sm_count = 0;
     unsigned *status = nullptr;
+    unsigned *sched = nullptr;  // g_prefill_sched on this device
     void *workspace = nullptr;  // caller-owned, for attn_fwd's tail split
     size_t workspace_bytes = 0;
 };
@@ -38,6 +46,12 @@ DeviceInfo g_dev[kMaxDevices];
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::atomic<uint64_t> g_budget{kDefaultBudgetNs};
 std::atomic<int> g_inject{0};
+std::atomic<unsigned> g_sched_next{0};
+
+// The counter pair for the next prefill launch on the device.
+unsigned *next_sched(const DeviceInfo *di) {
+    return di->sched + 2 * (g_sched_next.fetch_add(1, std::memory_order_relaxed) % kSchedPairs);
+}
 
 attn_status_t device_info(DeviceInfo **out) {
     int dev = 0;
@@ -58,6 +72,8 @@ attn_status_t device_info(DeviceInfo **out) {
             if (cudaGetSymbolAddress(&ptr, g_attn_status) != cudaSuccess) return ATTN_ERR_CUDA;
             d.status = static_cast<unsigned *>(ptr);
             if (cudaMemset(d.status, 0, 2 * sizeof(unsigned)) != cudaSuccess) return ATTN_ERR_CUDA;
+            if (cudaGetSymbolAddress(&ptr, g_prefill_sched) != cudaSuccess) return ATTN_ERR_CUDA;
+            d.sched = static_cast<unsigned *>(ptr);
         }
         if (!g_encode) {
             void *fn = nullptr;
@@ -179,13 +195,14 @@ attn_status_t fill_prefill_params(attn::PrefillParams *p, const DeviceInfo *di, 
     p->inject = 0;
     p->round_mode = ATTN_ROUND_RTNE;
     p->n_full_units = attn::prefill_num_units(*p);
+    p->n_items = p->n_full_units;
+    p->sched = next_sched(di);
     // Non-causal units all have the same length, so ordering them by batch and
     // KV head costs no balance; it keeps the units that read the same K/V
     // together, which pays once the K/V of all heads exceed L2.
     p->kv_major = (!causal && (double)B * Hkv * Sk * 128 * 4 > 64.0 * (1 << 20)) ? 1 : 0;
     // L2 prefetch of the next wave's Q for short non-causal units (few K/V tiles).
     p->prefetch_ahead = (!causal && Sk <= 1024) ? di->sm_count : 0;
-    p->early_start = (!causal && Sk <= 1024) ? 1 : 0;
     p->split_units = 0;
     p->split_parts = 1;
     p->ws_o = nullptr;
@@ -243,7 +260,9 @@ attn_status_t attn_fwd_rounded(const void *q, const void *k, const void *v, void
             ctas = p.n_full_units + su * parts;
         }
     }
-    if (attn::launch_prefill(mq, mk, mv, mo, mk, mv, p, ctas, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    p.n_items = ctas;
+    if (attn::launch_prefill(mq, mk, mv, mo, mk, mv, p, attn::prefill_grid(p.n_items, di->sm_count),
+                             static_cast<cudaStream_t>(stream)) != cudaSuccess)
         return ATTN_ERR_CUDA;
     if (attn::launch_prefill_merge(out, p, static_cast<cudaStream_t>(stream)) != cudaSuccess) return ATTN_ERR_CUDA;
     return ATTN_OK;
@@ -275,7 +294,6 @@ attn_status_t attn_fwd_varlen(const void *q, const void *k, const void *v, void 
     p.round_mode = round_mode;
     p.cu_q = cu_seqlens_q;
     p.prefetch_ahead = 0;  // (dense coordinates only)
-    p.early_start = 0;
     p.cu_k = cu_seqlens_k;
     // Keys much longer than queries (chunks against a context): K/V-first order.
     p.kv_major = max_seqlen_k >= 2 * max_seqlen_q ? 1 : 0;
@@ -286,11 +304,13 @@ attn_status_t attn_fwd_varlen(const void *q, const void *k, const void *v, void 
     const int64_t units = p.pair_heads ? (int64_t)B * Hkv * (p.G / 2) * p.n_m : (int64_t)B * Hq * ((p.n_m + 1) / 2);
     if (units > 0x7fffffff) return ATTN_ERR_INVALID_ARG;
     p.n_full_units = (int)units;
+    p.n_items = (int)units;
     CUtensorMap mq, mk, mv, mo;
     if (!make_map_4d(&mq, q, false, 1, total_q, Hq, d, 128) || !make_map_4d(&mk, k, false, 1, total_k, Hkv, d, 128) ||
         !make_map_4d(&mv, v, false, 1, total_k, Hkv, d, 128) || !make_map_4d(&mo, out, false, 1, total_q, Hq, d, 128))
         return ATTN_ERR_CUDA;
-    if (attn::launch_prefill(mq, mk, mv, mo, mk, mv, p, (int)units, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    if (attn::launch_prefill(mq, mk, mv, mo, mk, mv, p, attn::prefill_grid(p.n_items, di->sm_count),
+                             static_cast<cudaStream_t>(stream)) != cudaSuccess)
         return ATTN_ERR_CUDA;
     return ATTN_OK;
 }
@@ -321,7 +341,6 @@ attn_status_t attn_fwd_paged(const void *q, const void *k_pages, const void *v_p
     p.round_mode = round_mode;
     p.cu_q = cu_seqlens_q;
     p.prefetch_ahead = 0;  // (dense coordinates only)
-    p.early_start = 0;
     p.total_q = total_q;
     p.out = out;
     p.block_table = block_table;
@@ -333,6 +352,7 @@ attn_status_t attn_fwd_paged(const void *q, const void *k_pages, const void *v_p
     const int64_t units = p.pair_heads ? (int64_t)B * Hkv * (p.G / 2) * p.n_m : (int64_t)B * Hq * ((p.n_m + 1) / 2);
     if (units > 0x7fffffff) return ATTN_ERR_INVALID_ARG;
     p.n_full_units = (int)units;
+    p.n_items = (int)units;
     CUtensorMap mq, mk, mv, mo;
     if (!make_map_4d(&mq, q, false, 1, total_q, Hq, d, 128) || !make_map_pool_groups(&mk, k_pages, num_pages, Hkv, d, 2) ||
         !make_map_pool_groups(&mv, v_pages, num_pages, Hkv, d, 2) || !make_map_4d(&mo, out, false, 1, total_q, Hq, d, 128))
@@ -341,7 +361,8 @@ attn_status_t attn_fwd_paged(const void *q, const void *k_pages, const void *v_p
     if (!make_map_pool_groups(&mk8, k_pages, num_pages, Hkv, d, 16) ||
         !make_map_pool_groups(&mv8, v_pages, num_pages, Hkv, d, 16))
         return ATTN_ERR_CUDA;
-    if (attn::launch_prefill(mq, mk, mv, mo, mk8, mv8, p, (int)units, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    if (attn::launch_prefill(mq, mk, mv, mo, mk8, mv8, p, attn::prefill_grid(p.n_items, di->sm_count),
+                             static_cast<cudaStream_t>(stream)) != cudaSuccess)
         return ATTN_ERR_CUDA;
     return ATTN_OK;
 }

@@ -34,6 +34,9 @@ enum WaitSite : unsigned {
     kSiteSoftmaxV = 14,
     kSiteAppendSlot = 15,
     kSiteDecodeSeqlen = 16,
+    kSiteProducerQ = 17,
+    kSiteEpilogueSlot = 18,
+    kSiteItem = 19,
 };
 
 // First error wins; the site is informative only.

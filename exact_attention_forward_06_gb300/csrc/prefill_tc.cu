@@ -9,19 +9,26 @@
 // diagonal are never loaded or computed (the upper-triangle skip of the
 // reverse-engineering page, 观点一).
 //
-// One CTA owns two 128-row Q tiles ("units" of 256 rows: two heads of one KV
-// group at the same positions when the group size is even, else two adjacent
-// position blocks of one head), so every K/V tile that is loaded serves 256
-// query rows.  Warp roles (384 threads, three warpgroups):
-//   warp 0      TMA producer: Q tiles once, then K_j / V_j into a 5-slot ring
-//               of 32 KiB slots (full/empty mbarrier pairs);
+// A work unit is two 128-row Q tiles (256 rows: two heads of one KV group at
+// the same positions when the group size is even, else two adjacent position
+// blocks of one head), so every K/V tile that is loaded serves 256 query
+// rows.  The grid has at most one CTA per SM; each CTA takes units from the
+// list (longest first where lengths differ) as it frees up, and every barrier
+// phase runs on across its units, so the next unit's Q, K and V load while
+// the current unit finishes.  Warp roles (384 threads, three
+// warpgroups):
+//   warp 0      TMA producer: per unit the two Q tiles (each once the previous
+//               unit's last S product has read its buffer), then K_j / V_j
+//               into a 5-slot ring of 32 KiB slots (full/empty mbarrier
+//               pairs), then two ring slots that the softmax groups use to
+//               stage the unit's output tiles for their TMA stores;
 //   warp 1      TMEM allocator and tcgen05 MMA issuer for Q tile 0 (one lane);
 //   warp 2      tcgen05 MMA issuer for Q tile 1 (one lane);
 //   warp 3      idle (it completes warpgroup 0, which gives up registers);
 //   warps 4-7   softmax warpgroup for Q tile 0 (one thread per row);
 //   warps 8-11  softmax warpgroup for Q tile 1.
-// setmaxnreg moves registers from warpgroup 0 (96 each) to the softmax
-// warpgroups (200 each), which hold a whole 128-column score row.
+// setmaxnreg moves registers from warpgroup 0 (80 each) to the softmax
+// warpgroups (208 each), which hold a whole 128-column score row.
 // Tensor memory (512 columns): one fp32 score buffer S that the two tiles use
 // in turn, a bf16 probability buffer P_t per tile (64 columns of packed
 // pairs, read by the P V product straight from tensor memory) and an fp32
@@ -38,10 +45,15 @@
 // Softmax: scores are scaled into the log2 domain (scale * log2 e folded into
 // one FFMA) and exponentiated with ex2.approx.  A row's running max is only
 // moved (and O rescaled) when the new tile's max exceeds it by more than
-// 2^8; otherwise the stale max is kept, which is exact because m and l stay
-// consistent and P <= 256 is representable.  The rescale, when needed, is done
-// by the softmax warp itself on its own 32 rows of O in tensor memory, after
-// the previous P V product has completed.
+// 2^8, or when the new maximum would carry more than half of the row's sum so
+// far; otherwise the stale max is kept, which is exact because m and l stay
+// consistent and P <= 256 is representable.  The second condition is for
+// accuracy: P goes to the tensor core rounded to bf16 (8 significant bits), so
+// a key that dominates its row must get P = 1 exactly (its score is the
+// running max), or the rounding of two dominant keys whose V rows cancel
+// shows in O.  On unit-normal scores it fires on about 1 warp-tile in 10^4.
+// The rescale, when needed, is done by the softmax warp itself on its own 32
+// rows of O in tensor memory, after the previous P V product has completed.
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -66,22 +78,30 @@ constexpr uint32_t PAGE_BOX_BYTES = 4096;
 constexpr uint32_t PG_GROUP_BYTES = 2048;  // one 8-row group, both halves
 constexpr uint32_t PG_HALF_BYTES = 1024;   // one 8-row group, one half
 constexpr int NUM_THREADS = 384;  // three warpgroups
-constexpr uint32_t REGS_CONTROL = 96;   // warpgroup 0: producer, MMA issuer
-constexpr uint32_t REGS_SOFTMAX = 200;  // warpgroups 1-2: softmax
+constexpr uint32_t REGS_CONTROL = 80;   // warpgroup 0: producer, MMA issuer
+constexpr uint32_t REGS_SOFTMAX = 208;  // warpgroups 1-2: softmax
 // setmaxnreg hands registers between warpgroups within the launch budget
-// (384 threads x 168): 128 x 96 + 256 x 200 <= 384 x 168.
+// (384 threads x 168): 128 x 80 + 256 x 208 <= 384 x 168.
 static_assert(128 * REGS_CONTROL + 256 * REGS_SOFTMAX <= NUM_THREADS * 168, "register split exceeds the launch budget");
 constexpr uint32_t SMEM_Q0 = 0;
 constexpr uint32_t SMEM_Q1 = TILE_BYTES;
 constexpr uint32_t SMEM_SLOTS = 2 * TILE_BYTES;
 constexpr uint32_t SMEM_TILES = SMEM_SLOTS + NSLOT * TILE_BYTES;
-constexpr int NBARS = 1 + 2 * NSLOT + 2 + 1 + 2 + 2 + 1 + 1 + 1;
-constexpr uint32_t SMEM_MISC = 256;
+// Work items handed from the producer to the other roles through a small
+// ring in shared memory.
+constexpr int ITEM_RING = 4;
+// Roles that read each handed-out unit: the two MMA issuing threads and the
+// eight softmax warps.
+constexpr uint32_t ITEM_READERS = 2 + 8;
+// q_full[2], q_free[2], kv_full[NSLOT], kv_empty[NSLOT], s_full[2], s_free[2],
+// p_full[2], o_full[2], fin, item_full[ITEM_RING], item_empty[ITEM_RING]
+constexpr int NBARS = 2 + 2 + 2 * NSLOT + 2 + 2 + 2 + 2 + 1 + 2 * ITEM_RING;
+constexpr uint32_t SMEM_MISC = 768;
 constexpr uint32_t SMEM_ALIGN = 1024;
-constexpr float RESCALE_LOG2 = 8.0f;  // move the running max only past a 2^8 growth
+constexpr float RESCALE_LOG2 = 8.0f;  // move the running max past a 2^8 growth (and see softmax_wg)
 constexpr float LN2 = 0.6931471805599453f;
 
-static_assert(NBARS * 8 + 16 <= SMEM_MISC, "barrier area too small");
+static_assert(NBARS * 8 + 8 + 64 * ITEM_RING <= SMEM_MISC, "barrier area too small");
 
 constexpr uint32_t IDESC_S = ptx::idesc_bf16_f32(128, 128, 0, 0);   // Q K^T: both K-major
 constexpr uint32_t IDESC_PV = ptx::idesc_bf16_f32(128, 128, 0, 1);  // P V: V is N(d)-major
@@ -98,21 +118,30 @@ __device__ __forceinline__ uint32_t tm_o(int t) { return TM_O0 + 128 * t; }
 struct SmemLayout {
     uint8_t *base;
     uint64_t *bars;
-    // q_full: both Q tiles have landed; with an early start Q_1 has its own
-    // barrier q_full1 and q_full covers Q_0 alone.
-    __device__ uint64_t *q_full() const { return bars; }
-    __device__ uint64_t *q_full1() const { return bars + NBARS - 1; }
-    __device__ uint64_t *kv_full(int s) const { return bars + 1 + s; }
-    __device__ uint64_t *kv_empty(int s) const { return bars + 1 + NSLOT + s; }
-    __device__ uint64_t *s_full(int t) const { return bars + 1 + 2 * NSLOT + t; }
-    // s_free(t): phase j completes when softmax group t has loaded its score tile j.
-    __device__ uint64_t *s_free(int t) const { return t ? bars + 9 + 2 * NSLOT : bars + 3 + 2 * NSLOT; }
-    __device__ uint64_t *p_full(int t) const { return bars + 4 + 2 * NSLOT + t; }
-    __device__ uint64_t *o_full(int t) const { return bars + 6 + 2 * NSLOT + t; }
-    __device__ uint64_t *fin() const { return bars + 8 + 2 * NSLOT; }
+    // q_full(t): Q tile t of the current unit has landed; q_free(t): the
+    // unit's last S product has read it (one phase per unit each).
+    __device__ uint64_t *q_full(int t) const { return bars + t; }
+    __device__ uint64_t *q_free(int t) const { return bars + 2 + t; }
+    __device__ uint64_t *kv_full(int s) const { return bars + 4 + s; }
+    __device__ uint64_t *kv_empty(int s) const { return bars + 4 + NSLOT + s; }
+    __device__ uint64_t *s_full(int t) const { return bars + 4 + 2 * NSLOT + t; }
+    // s_free(t): phase g completes when softmax group t has loaded its score tile g.
+    __device__ uint64_t *s_free(int t) const { return bars + 6 + 2 * NSLOT + t; }
+    __device__ uint64_t *p_full(int t) const { return bars + 8 + 2 * NSLOT + t; }
+    __device__ uint64_t *o_full(int t) const { return bars + 10 + 2 * NSLOT + t; }
+    __device__ uint64_t *fin() const { return bars + 12 + 2 * NSLOT; }
+    // item_full(i): entry i of the item ring holds the next item; item_empty(i):
+    // every reader has taken it.
+    __device__ uint64_t *item_full(int i) const { return bars + 13 + 2 * NSLOT + i; }
+    __device__ uint64_t *item_empty(int i) const { return bars + 13 + 2 * NSLOT + ITEM_RING + i; }
     __device__ uint32_t *tmem_slot() const { return reinterpret_cast<uint32_t *>(bars + NBARS); }
     __device__ volatile int *abort_flag() const { return reinterpret_cast<volatile int *>(bars + NBARS) + 1; }
+    // Entry i of the item ring: a decoded unit (16 ints), 8-byte aligned.
+    __device__ volatile int *item_ring(int i) const {
+        return reinterpret_cast<volatile int *>(bars + NBARS + 1) + 16 * i;
+    }
     __device__ uint8_t *q_tile(int t) const { return base + (t ? SMEM_Q1 : SMEM_Q0); }
+    // Ring slot s: a K or V tile, or a tile's output staging area.
     __device__ uint8_t *slot(int s) const { return base + SMEM_SLOTS + s * TILE_BYTES; }
 };
 
@@ -203,16 +232,22 @@ __host__ __device__ __forceinline__ Unit unit_coords(const PrefillParams &p, int
     return w;
 }
 
-// The unit (and key range) CTA number cta works on.  CTAs past the whole
-// units are the parts of the tail units, part-major within a unit.
-__device__ __forceinline__ Unit decode_unit(const PrefillParams &p, int cta) {
-    if (p.block_table != nullptr) {
+// The unit (and key range) of work item `it`, for each kind of launch.
+// kDense: items past the whole units are the parts of the tail units,
+// part-major within a unit.  kPacked / kPaged: the unit's rows and keys are
+// those of its sequence; offsets that are out of order or out of range, or
+// lengths past the stated maxima, are reported and the unit does nothing.
+enum LaunchKind : int { kDense = 0, kPacked = 1, kPaged = 2 };
+
+template <int KIND>
+__device__ __forceinline__ Unit decode_unit(const PrefillParams &p, int it) {
+    if (KIND == kPaged) {
         // Query chunk of sequence w.b against its paged cache.
-        Unit w = unit_coords(p, cta);
+        Unit w = unit_coords(p, it);
         const int q0 = p.cu_q[w.b], q1 = p.cu_q[w.b + 1];
         const int Lk = p.seqlens_k[w.b];
         const bool bad = q0 < 0 || q1 < q0 || q1 > p.total_q || q1 - q0 > p.Sq || Lk < 0 || Lk > p.max_blocks * 16;
-        if (bad && threadIdx.x == 0) report_status(p.status, kStatusDeviceBounds, kSiteVarlenOffsets);
+        if (bad) report_status(p.status, kStatusDeviceBounds, kSiteVarlenOffsets);
         w.Sq = bad ? 0 : q1 - q0;
         w.Sk = bad ? 0 : Lk;
         w.q0 = bad ? 0 : q0;
@@ -221,16 +256,13 @@ __device__ __forceinline__ Unit decode_unit(const PrefillParams &p, int cta) {
         unit_kv_range(p, w);
         return w;
     }
-    if (p.cu_q != nullptr) {
-        // Packed batch: the unit's rows and keys are those of sequence w.b.
-        // Offsets that are out of order or out of range, or lengths past the
-        // stated maxima, are reported and the unit does nothing.
-        Unit w = unit_coords(p, cta);
+    if (KIND == kPacked) {
+        Unit w = unit_coords(p, it);
         const int q0 = p.cu_q[w.b], q1 = p.cu_q[w.b + 1];
         const int k0 = p.cu_k[w.b], k1 = p.cu_k[w.b + 1];
         const bool bad = q0 < 0 || q1 < q0 || q1 > p.total_q || k0 < 0 || k1 < k0 || k1 > p.total_k ||
                          q1 - q0 > p.Sq || k1 - k0 > p.Sk;
-        if (bad && threadIdx.x == 0) report_status(p.status, kStatusDeviceBounds, kSiteVarlenOffsets);
+        if (bad) report_status(p.status, kStatusDeviceBounds, kSiteVarlenOffsets);
         w.Sq = bad ? 0 : q1 - q0;
         w.Sk = bad ? 0 : k1 - k0;
         w.q0 = bad ? 0 : q0;
@@ -239,8 +271,8 @@ __device__ __forceinline__ Unit decode_unit(const PrefillParams &p, int cta) {
         unit_kv_range(p, w);
         return w;
     }
-    if (cta < p.n_full_units) return unit_coords(p, cta);
-    const int v = cta - p.n_full_units;
+    if (it < p.n_full_units) return unit_coords(p, it);
+    const int v = it - p.n_full_units;
     const int su = v / p.split_parts;
     const int part = v % p.split_parts;
     Unit w = unit_coords(p, p.n_full_units + su);
@@ -253,6 +285,92 @@ __device__ __forceinline__ Unit decode_unit(const PrefillParams &p, int cta) {
     return w;
 }
 
+// ------------------------------------------------------------------ work items
+
+// Work items are handed out dynamically: CTA c starts with item c, and each
+// CTA that finishes one takes the next unclaimed item from a counter shared
+// by the launch (p.sched[0], counting from gridDim.x), so the CTAs work
+// through the list in order, each taking the next item as soon as it is free
+// -- the order the hardware would dispatch one CTA per item in, without a
+// CTA launch per item.  The producer thread claims the items and hands them
+// to the other roles through the item ring; -1 ends the list.  With one CTA
+// per item no counter is used.
+__device__ __forceinline__ int claim_item(const PrefillParams &p) {
+    if ((int)gridDim.x >= p.n_items) return -1;
+    const int it = (int)gridDim.x + (int)atomicAdd(p.sched, 1u);
+    return it < p.n_items ? it : -1;
+}
+
+// The next unit this CTA works on: the first item (this CTA's own first one,
+// or claimed) whose rows do not all lie past their sequence's end (packed
+// batches size their item list by the longest sequence); n_kv = -1 when the
+// list is used up.  Only the producer thread calls this: it decodes each item
+// once and hands the decoded unit to the other roles.
+// Given item `it` whose rows lie past its sequence's end, the first item after
+// it that may have rows, when the item list is ordered by sequence and KV head
+// (kv_major): such items are contiguous within their (sequence, KV group)
+// block -- its first items for a causal launch (longest row blocks first), its
+// last ones otherwise.  Without that order, the next item.
+__device__ __forceinline__ int next_candidate(const PrefillParams &p, int it, int seq_len) {
+    if (!p.kv_major) return it + 1;
+    const int step = p.pair_heads ? p.G / 2 : 1;              // items per row-block step
+    const int steps = p.pair_heads ? p.n_m : (p.n_m + 1) / 2;   // row-block steps per block
+    const int rows_per_step = p.pair_heads ? BM : 2 * BM;
+    const int per = step * steps;
+    const int start = it - it % per;
+    const int valid = (seq_len + rows_per_step - 1) / rows_per_step;  // steps with rows
+    const int target = p.causal ? start + (steps - valid) * step : start + per;
+    return target > it + 1 ? target : it + 1;
+}
+
+template <int KIND>
+__device__ __forceinline__ Unit next_unit(const PrefillParams &p, bool first) {
+    for (int it = first ? ((int)blockIdx.x < p.n_items ? (int)blockIdx.x : -1) : claim_item(p); it >= 0;
+         it = claim_item(p)) {
+        const Unit w = decode_unit<KIND>(p, it);
+        if (w.s0[0] < w.Sq) return w;
+        // Move the shared counter past the rest of this run of empty items
+        // (they would only be claimed and skipped one by one).
+        const int nx = KIND == kDense ? it + 1 : next_candidate(p, it, w.Sq);
+        if (nx > it + 1 && (int)gridDim.x < p.n_items) atomicMax(p.sched, (unsigned)max(0, nx - (int)gridDim.x));
+    }
+    Unit end{};
+    end.n_kv = -1;
+    return end;
+}
+
+// Producer side: put unit w (n_kv = -1: end of the list) into ring entry
+// u % ITEM_RING for the readers.
+__device__ __forceinline__ bool publish_unit(const SmemLayout &sm, const WaitCtx &wc, int u, const Unit &w) {
+    const int e = u % ITEM_RING;
+    if (u >= ITEM_RING && !wait_bounded(sm.item_empty(e), (uint32_t)(((u / ITEM_RING) - 1) & 1), wc, kSiteItem))
+        return false;
+    volatile int *d = sm.item_ring(e);
+    d[0] = w.b; d[1] = w.g; d[2] = w.h[0]; d[3] = w.h[1]; d[4] = w.s0[0]; d[5] = w.s0[1]; d[6] = w.n_kv;
+    d[7] = w.j_lo; d[8] = w.part; d[9] = w.ws_row; d[10] = w.Sq; d[11] = w.Sk; d[12] = w.q0; d[13] = w.k0;
+    d[14] = w.tb;
+    ptx::mbar_arrive(sm.item_full(e));  // release: the writes above are seen by whoever sees the phase
+    return true;
+}
+
+// Reader side (every lane of a reading warp): unit u of this CTA.  Returns
+// false when the CTA is giving up; w.n_kv = -1 marks the end of the list.
+// The caller hands the entry back (item_empty) once every lane has read it.
+__device__ __forceinline__ bool read_unit(const SmemLayout &sm, const WaitCtx &wc, int u, bool spin, Unit &w) {
+    const int e = u % ITEM_RING;
+    const uint32_t par = (uint32_t)((u / ITEM_RING) & 1);
+    if (!(spin ? wait_spin(sm.item_full(e), par, wc, kSiteItem) : wait_bounded(sm.item_full(e), par, wc, kSiteItem)))
+        return false;
+    const volatile int *d = sm.item_ring(e);
+    w.b = d[0]; w.g = d[1]; w.h[0] = d[2]; w.h[1] = d[3]; w.s0[0] = d[4]; w.s0[1] = d[5]; w.n_kv = d[6];
+    w.j_lo = d[7]; w.part = d[8]; w.ws_row = d[9]; w.Sq = d[10]; w.Sk = d[11]; w.q0 = d[12]; w.k0 = d[13];
+    w.tb = d[14];
+    return true;
+}
+
+// Ring items of a unit: its K/V tiles, then one output staging slot per Q tile.
+__device__ __forceinline__ int ring_items(const Unit &w) { return 2 * w.n_kv + 2; }
+
 // ------------------------------------------------------------------ producer
 
 __device__ __forceinline__ void load_tile(const CUtensorMap *map, uint8_t *dst, uint64_t *bar, bool bhsd, int h,
@@ -263,141 +381,195 @@ __device__ __forceinline__ void load_tile(const CUtensorMap *map, uint8_t *dst, 
     ptx::tma_load_4d(dst + HALF_BYTES, map, bar, hi.c0, hi.c1, hi.c2, hi.c3, pol);
 }
 
-// The copies a unit can issue before anything is consumed, in the order its
-// first products need them: Q_0, K_0, Q_1, V_0, then further ring items up to
-// the ring's size (no slot has to be released yet).  With an early start the
-// barrier-initialising thread issues them before the CTA-wide barrier, while
-// tensor memory is being allocated.  Returns the number of ring items issued.
-__device__ int producer_start(const PrefillParams &p, const Unit &w, const SmemLayout &sm, const CUtensorMap *mq,
-                              const CUtensorMap *mk, const CUtensorMap *mv) {
-    const uint64_t pol_q = ptx::policy_evict_first();
-    const uint64_t pol_kv = ptx::policy_evict_last();
-    const int total = 2 * w.n_kv;
-    const int first = total < NSLOT ? total : NSLOT;
-    for (int n = 0; n < first; ++n) {
-        if (n < 2) {
-            uint64_t *qb = n ? sm.q_full1() : sm.q_full();
-            ptx::mbar_arrive_expect_tx(qb, TILE_BYTES);
-            load_tile(mq, sm.q_tile(n), qb, p.bhsd, n ? w.h[1] : w.h[0], w.q0 + (n ? w.s0[1] : w.s0[0]), w.tb,
-                      pol_q);
-        }
-        ptx::mbar_arrive_expect_tx(sm.kv_full(n), TILE_BYTES);
-        load_tile((n & 1) ? mv : mk, sm.slot(n), sm.kv_full(n), p.bhsd, w.g, w.k0 + (w.j_lo + (n >> 1)) * BN, w.tb,
-                  pol_kv);
+// L2 prefetch of the Q tiles of this CTA's next unit (short units spend much
+// of their time loading Q: start it early so it is in L2 when wanted).
+__device__ __forceinline__ void prefetch_q(const PrefillParams &p, const CUtensorMap *mq, const Unit &w) {
+    if (w.n_kv < 0) return;
+    for (int t = 0; t < 2; ++t) {
+        const Coord4 lo = coord4(p.bhsd, 0, t ? w.h[1] : w.h[0], w.q0 + (t ? w.s0[1] : w.s0[0]), w.tb);
+        const Coord4 hi = coord4(p.bhsd, 64, t ? w.h[1] : w.h[0], w.q0 + (t ? w.s0[1] : w.s0[0]), w.tb);
+        ptx::tma_prefetch_4d(mq, lo.c0, lo.c1, lo.c2, lo.c3);
+        ptx::tma_prefetch_4d(mq, hi.c0, hi.c1, hi.c2, hi.c3);
     }
-    return first;
 }
 
-// first: ring items producer_start already issued (EARLY), else 0.
-template <bool EARLY>
-__device__ void producer(const PrefillParams &p, const Unit &w, const SmemLayout &sm, const WaitCtx &wc,
-                         const CUtensorMap *mq, const CUtensorMap *mk, const CUtensorMap *mv, int first) {
+// Dense and packed K/V (one lane).  Per unit: hand it to the other roles,
+// load the two Q tiles, each once the previous unit's last S product has
+// read its buffer (q_free), find the next unit while they load, then the K/V
+// tiles into the ring, then the two output staging slots (a plain arrive on
+// the slot's full barrier once the slot is empty: the softmax group fills it
+// and empties it again after its output store has read it).
+template <int KIND>
+__device__ void producer(const PrefillParams &p, const SmemLayout &sm, const WaitCtx &wc, const CUtensorMap *mq,
+                         const CUtensorMap *mk, const CUtensorMap *mv) {
     if (p.inject == 1) return;  // fault injection: issue nothing
-    // A unit whose rows see no key loads nothing: its output tiles are zeros,
-    // written into the Q tile buffers, which therefore must not receive a
-    // late-landing Q copy.
-    if (w.n_kv == 0) return;
     const uint64_t pol_q = ptx::policy_evict_first();
     const uint64_t pol_kv = ptx::policy_evict_last();
-    if (!EARLY) {
-        ptx::mbar_arrive_expect_tx(sm.q_full(), 2 * TILE_BYTES);
-        load_tile(mq, sm.q_tile(0), sm.q_full(), p.bhsd, w.h[0], w.q0 + w.s0[0], w.tb, pol_q);
-        load_tile(mq, sm.q_tile(1), sm.q_full(), p.bhsd, w.h[1], w.q0 + w.s0[1], w.tb, pol_q);
-    }
-    if (p.prefetch_ahead > 0 && (int)blockIdx.x + p.prefetch_ahead < p.n_full_units) {
-        // Short units (few K/V tiles) spend much of their time loading Q:
-        // start the Q of the unit about one wave ahead into L2, so the CTA
-        // that gets it finds it there.
-        const Unit nx = unit_coords(p, (int)blockIdx.x + p.prefetch_ahead);
-        for (int t = 0; t < 2; ++t) {
-            const Coord4 lo = coord4(p.bhsd, 0, t ? nx.h[1] : nx.h[0], t ? nx.s0[1] : nx.s0[0], nx.b);
-            const Coord4 hi = coord4(p.bhsd, 64, t ? nx.h[1] : nx.h[0], t ? nx.s0[1] : nx.s0[0], nx.b);
-            ptx::tma_prefetch_4d(mq, lo.c0, lo.c1, lo.c2, lo.c3);
-            ptx::tma_prefetch_4d(mq, hi.c0, hi.c1, hi.c2, hi.c3);
+    int n = 0;                 // ring items issued
+    int qn[2] = {0, 0};        // Q loads issued per tile
+    int u = 0;                 // units handed out
+    bool ok = true;
+    Unit w = next_unit<KIND>(p, true);
+    while (ok && w.n_kv >= 0) {
+        Unit nx;
+        nx.n_kv = -1;
+        if (!publish_unit(sm, wc, u++, w)) {
+            ok = false;
+            break;
         }
+        // Q tiles, each once the previous unit's last S product has read its
+        // buffer; then the next unit (its claim and offsets) while they load.
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+            if (qn[t] > 0 && !wait_bounded(sm.q_free(t), (qn[t] - 1) & 1, wc, kSiteProducerQ)) {
+                ok = false;
+                break;
+            }
+            ptx::mbar_arrive_expect_tx(sm.q_full(t), TILE_BYTES);
+            load_tile(mq, sm.q_tile(t), sm.q_full(t), p.bhsd, t ? w.h[1] : w.h[0], w.q0 + (t ? w.s0[1] : w.s0[0]),
+                      w.tb, pol_q);
+            ++qn[t];
+        }
+        if (!ok) break;
+        nx = next_unit<KIND>(p, false);
+        if (p.prefetch_ahead > 0) prefetch_q(p, mq, nx);
+        const int total = ring_items(w);
+        for (int i = 0; i < total; ++i) {
+            const int slot = n % NSLOT;
+            if (n >= NSLOT && !wait_bounded(sm.kv_empty(slot), ((n / NSLOT) - 1) & 1, wc, kSiteProducerEmpty)) {
+                ok = false;
+                break;
+            }
+            if (i < 2 * w.n_kv) {
+                ptx::mbar_arrive_expect_tx(sm.kv_full(slot), TILE_BYTES);
+                load_tile((i & 1) ? mv : mk, sm.slot(slot), sm.kv_full(slot), p.bhsd, w.g,
+                          w.k0 + (w.j_lo + (i >> 1)) * BN, w.tb, pol_kv);
+            } else {
+                ptx::mbar_arrive(sm.kv_full(slot));  // an output staging slot
+            }
+            ++n;
+        }
+        w = nx;
     }
-    const int total = 2 * w.n_kv;
-    int issued = EARLY ? first : 0;
-    for (int n = issued; n < total; ++n) {
-        const int slot = n % NSLOT;
-        const int round = n / NSLOT;
-        if (round > 0 && !wait_bounded(sm.kv_empty(slot), (round - 1) & 1, wc, kSiteProducerEmpty)) break;
-        ptx::mbar_arrive_expect_tx(sm.kv_full(slot), TILE_BYTES);
-        load_tile((n & 1) ? mv : mk, sm.slot(slot), sm.kv_full(slot), p.bhsd, w.g, w.k0 + (w.j_lo + (n >> 1)) * BN,
-                  w.tb, pol_kv);
-        ++issued;
-    }
+    if (ok) publish_unit(sm, wc, u, w);  // end of the list (n_kv = -1)
     // On the way out make sure no copy is still writing into shared memory.
-    drain_wait(sm.q_full(), 0, wc);
-    if (EARLY) drain_wait(sm.q_full1(), 0, wc);
-    for (int n = max(0, issued - NSLOT); n < issued; ++n) drain_wait(sm.kv_full(n % NSLOT), (n / NSLOT) & 1, wc);
+    for (int t = 0; t < 2; ++t)
+        if (qn[t] > 0) drain_wait(sm.q_full(t), (qn[t] - 1) & 1, wc);
+    for (int i = max(0, n - NSLOT); i < n; ++i) drain_wait(sm.kv_full(i % NSLOT), (i / NSLOT) & 1, wc);
 }
 
 // Paged K/V: the whole warp 0 produces.  A K/V tile is 8 pages; lane i < 8
 // reads table entry i of the tile and issues the one 4 KiB box (16 rows, both
 // 64-column halves) of page i, so the table loads and the 16 copies of a tile
 // pair go out in parallel instead of one after another from a single lane.
-// Lane 0 arms each barrier before any lane issues into it.  Pages past the
+// Lane 0 arms each barrier before any lane issues into it, finds and hands
+// out the units, loads Q and hands out the staging slots as the dense
+// producer does.  Pages past the
 // sequence's last one, and bad entries (reported), get a row past the pool:
-// the copy then fills zeros.
-// When the tile's 8 pages are consecutive in the pool (an engine that hands a
-// sequence pages in order), lane 0 loads the tile with one 128-row box of the
-// run maps mk8/mv8 instead.
-__device__ void producer_paged(const PrefillParams &p, const Unit &w, const SmemLayout &sm, const WaitCtx &wc,
-                               int lane, const CUtensorMap *mq, const CUtensorMap *mk, const CUtensorMap *mv,
+// the copy then fills zeros.  When the tile's 8 pages are consecutive in the
+// pool (an engine that hands a sequence pages in order), lane 0 loads the
+// tile with one 128-row box of the run maps mk8/mv8 instead.
+__device__ void producer_paged(const PrefillParams &p, const SmemLayout &sm, const WaitCtx &wc, int lane,
+                               const CUtensorMap *mq, const CUtensorMap *mk, const CUtensorMap *mv,
                                const CUtensorMap *mk8, const CUtensorMap *mv8) {
-    if (p.inject == 1 || w.n_kv == 0) return;
+    if (p.inject == 1) return;
     const uint64_t pol_q = ptx::policy_evict_first();
     const uint64_t pol_kv = ptx::policy_evict_last();
-    if (lane == 0) {
-        ptx::mbar_arrive_expect_tx(sm.q_full(), 2 * TILE_BYTES);
-        load_tile(mq, sm.q_tile(0), sm.q_full(), p.bhsd, w.h[0], w.q0 + w.s0[0], w.tb, pol_q);
-        load_tile(mq, sm.q_tile(1), sm.q_full(), p.bhsd, w.h[1], w.q0 + w.s0[1], w.tb, pol_q);
-    }
-    const int total = 2 * w.n_kv;
-    const int n_pages = (w.Sk + 15) / 16;
-    const int *row = p.block_table + (int64_t)w.b * p.max_blocks;
-    int issued = 0;
-    int page_row = p.num_pages * 16;  // this lane's page of the current tile (lanes < 8)
-    bool run = false;                 // the current tile's pages are one run in the pool
-    for (int n = 0; n < total; ++n) {
-        const int slot = n % NSLOT;
-        const int round = n / NSLOT;
-        if ((n & 1) == 0 && lane < BN / 16) {
-            const int page = (w.j_lo + (n >> 1)) * (BN / 16) + lane;
-            const int phys = page < n_pages ? row[page] : -1;
-            const bool ok_page = phys >= 0 && phys < p.num_pages;
-            if (!ok_page && page < n_pages) report_status(p.status, kStatusDeviceBounds, kSitePagedTable);
-            page_row = ok_page ? phys * 16 : p.num_pages * 16;
-        }
-        bool ok = true;
-        if (lane == 0) {
-            ok = round == 0 || wait_bounded(sm.kv_empty(slot), (round - 1) & 1, wc, kSiteProducerEmpty);
-            if (ok) ptx::mbar_arrive_expect_tx(sm.kv_full(slot), TILE_BYTES);
-        }
+    int n = 0;            // ring items issued
+    int qn[2] = {0, 0};   // Q loads issued per tile (lane 0)
+    int u = 0;            // units handed out (lane 0)
+    bool ok = true;
+    // Lane 0 finds and publishes each unit; the other lanes read it back from
+    // the item ring.
+    Unit w;
+    w.n_kv = -1;
+    if (lane == 0) w = next_unit<kPaged>(p, true);
+    while (ok) {
+        if (lane == 0) ok = publish_unit(sm, wc, u, w);
         if (!__shfl_sync(0xffffffffu, ok, 0)) break;
-        if ((n & 1) == 0) {
-            // (after the slot wait, which the table loads overlap)
-            const int first = __shfl_sync(0xffffffffu, page_row, 0);
-            const bool in_run = lane >= BN / 16 || (page_row == first + 16 * lane && first < p.num_pages * 16);
-            run = __all_sync(0xffffffffu, in_run);
+        __syncwarp();
+        if (lane != 0) {
+            const volatile int *d = sm.item_ring(u % ITEM_RING);
+            w.b = d[0]; w.g = d[1]; w.h[0] = d[2]; w.h[1] = d[3]; w.s0[0] = d[4]; w.s0[1] = d[5]; w.n_kv = d[6];
+            w.j_lo = d[7]; w.Sq = d[10]; w.Sk = d[11]; w.q0 = d[12]; w.tb = d[14];
         }
-        // The pool maps are in 8-row groups (see the paged tile layout): a
-        // page is one 4 KiB box at group page_row / 8, a run one box of 16.
-        if (run) {
-            if (lane == 0)
-                ptx::tma_load_5d_hint(sm.slot(slot), (n & 1) ? mv8 : mk8, sm.kv_full(slot), 0, 0, 0, page_row / 8,
-                                      w.g, pol_kv);
-        } else if (lane < BN / 16) {
-            ptx::tma_load_5d_hint(sm.slot(slot) + lane * PAGE_BOX_BYTES, (n & 1) ? mv : mk, sm.kv_full(slot), 0, 0, 0,
-                                  page_row / 8, w.g, pol_kv);
+        ++u;
+        if (w.n_kv < 0) break;  // end of the list
+        Unit nx;  // (lane 0)
+        nx.n_kv = -1;
+        const int total = 2 * w.n_kv;
+        const int n_pages = (w.Sk + 15) / 16;
+        const int *row = p.block_table + (int64_t)w.b * p.max_blocks;
+        int page_row = p.num_pages * 16;  // this lane's page of the current tile (lanes < 8)
+        bool run = false;                 // the current tile's pages are one run in the pool
+        if (lane == 0) {
+            for (int t = 0; t < 2 && ok; ++t) {
+                if (qn[t] > 0 && !wait_bounded(sm.q_free(t), (qn[t] - 1) & 1, wc, kSiteProducerQ)) {
+                    ok = false;
+                    break;
+                }
+                ptx::mbar_arrive_expect_tx(sm.q_full(t), TILE_BYTES);
+                load_tile(mq, sm.q_tile(t), sm.q_full(t), p.bhsd, t ? w.h[1] : w.h[0],
+                          w.q0 + (t ? w.s0[1] : w.s0[0]), w.tb, pol_q);
+                ++qn[t];
+            }
+            if (ok) nx = next_unit<kPaged>(p, false);  // the next unit while this one's Q loads
         }
-        issued = n + 1;
+        if (!__shfl_sync(0xffffffffu, ok, 0)) {
+            ok = false;
+            break;
+        }
+        for (int i = 0; i < total + 2; ++i) {
+            const int slot = n % NSLOT;
+            if (i < total && (i & 1) == 0 && lane < BN / 16) {
+                const int page = (w.j_lo + (i >> 1)) * (BN / 16) + lane;
+                const int phys = page < n_pages ? row[page] : -1;
+                const bool ok_page = phys >= 0 && phys < p.num_pages;
+                if (!ok_page && page < n_pages) report_status(p.status, kStatusDeviceBounds, kSitePagedTable);
+                page_row = ok_page ? phys * 16 : p.num_pages * 16;
+            }
+            bool got = true;
+            if (lane == 0) {
+                got = n < NSLOT || wait_bounded(sm.kv_empty(slot), ((n / NSLOT) - 1) & 1, wc, kSiteProducerEmpty);
+                if (got) {
+                    if (i < total)
+                        ptx::mbar_arrive_expect_tx(sm.kv_full(slot), TILE_BYTES);
+                    else
+                        ptx::mbar_arrive(sm.kv_full(slot));  // an output staging slot
+                }
+            }
+            if (!__shfl_sync(0xffffffffu, got, 0)) {
+                ok = false;
+                break;
+            }
+            if (i < total) {
+                if ((i & 1) == 0) {
+                    // (after the slot wait, which the table loads overlap)
+                    const int first = __shfl_sync(0xffffffffu, page_row, 0);
+                    const bool in_run =
+                        lane >= BN / 16 || (page_row == first + 16 * lane && first < p.num_pages * 16);
+                    run = __all_sync(0xffffffffu, in_run);
+                }
+                // The pool maps are in 8-row groups (see the paged tile layout):
+                // a page is one 4 KiB box at group page_row / 8, a run one box of 16.
+                if (run) {
+                    if (lane == 0)
+                        ptx::tma_load_5d_hint(sm.slot(slot), (i & 1) ? mv8 : mk8, sm.kv_full(slot), 0, 0, 0,
+                                              page_row / 8, w.g, pol_kv);
+                } else if (lane < BN / 16) {
+                    ptx::tma_load_5d_hint(sm.slot(slot) + lane * PAGE_BOX_BYTES, (i & 1) ? mv : mk, sm.kv_full(slot),
+                                          0, 0, 0, page_row / 8, w.g, pol_kv);
+                }
+            }
+            ++n;
+        }
+        if (lane == 0) w = nx;
     }
     // On the way out make sure no copy is still writing into shared memory.
     if (lane == 0) {
-        drain_wait(sm.q_full(), 0, wc);
-        for (int n = max(0, issued - NSLOT); n < issued; ++n) drain_wait(sm.kv_full(n % NSLOT), (n / NSLOT) & 1, wc);
+        for (int t = 0; t < 2; ++t)
+            if (qn[t] > 0) drain_wait(sm.q_full(t), (qn[t] - 1) & 1, wc);
+        for (int i = max(0, n - NSLOT); i < n; ++i) drain_wait(sm.kv_full(i % NSLOT), (i / NSLOT) & 1, wc);
     }
 }
 
@@ -432,66 +604,84 @@ __device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t tmem_p, uint6
 
 // One issuing thread per tile (stream t), in the order
 //   S_t(0), then for every K/V tile j:  S_t(j+1), PV_t(j)
-// The score tiles go through one shared S buffer in the order
-// S_0(0), S_1(0), S_0(1), S_1(1), ...: each is issued once the softmax that
+// for each unit in turn.  The score tiles go through one shared S buffer in
+// the order S_0(0), S_1(0), S_0(1), S_1(1), ... counted across the CTA's
+// units (g below is that running index): each is issued once the softmax that
 // consumed the one before (the other tile's) has loaded it.  Each group has
-// its own s_free barrier: S_1(j) waits for phase j of s_free(0), S_0(j+1) for
-// phase j of s_free(1).  (A single barrier for both would let a stream that
+// its own s_free barrier: S_1(g) waits for phase g of s_free(0), S_0(g) for
+// phase g-1 of s_free(1).  (A single barrier for both would let a stream that
 // runs ahead pass on the parity of a phase two back.)
 // An issuing thread is held while its products execute, and a P V product
 // waits for its tile's whole softmax; with one stream per tile, neither holds
 // up the other tile's products, and one thread's waits and commits overlap
 // the other's products.
-//   S_t(j)  needs K_j and the other group's s_free (phase j for S_1(j), j-1 for S_0(j));
+//   S_t(j)  needs Q_t, K_j and the other group's s_free;
 //   PV_t(j) needs P_t(j) (p_full[t]) and V_j.
 // A ring slot takes one release per stream (a commit after the stream's
-// product that reads it).
-template <int T, bool PAGED, bool EARLY>
-__device__ void mma_stream(const Unit &w, const SmemLayout &sm, const WaitCtx &wc, uint32_t tmem_base) {
-    if (w.n_kv == 0) return;  // nothing to multiply (and no Q is loaded)
-    if (!wait_spin(EARLY && T == 1 ? sm.q_full1() : sm.q_full(), 0, wc, kSiteMmaQ)) return;
-    ptx::tc_fence_after();
+// product that reads it).  After a unit's last S product the stream commits
+// q_free[t]: once that product has completed, Q_t may be replaced by the next
+// unit's, while this unit's last softmax, P V and output still run.
+template <int T, bool PAGED>
+__device__ void mma_stream(const PrefillParams &p, const SmemLayout &sm, const WaitCtx &wc, uint32_t tmem_base) {
     const uint64_t q_desc = ptx::desc_kmajor_sw128(ptx::smem_addr(sm.q_tile(T)));
     const uint32_t slot0 = ptx::smem_addr(sm.slot(0));
     auto slot_of = [](int n) { return n % NSLOT; };
     auto par_of = [](int n) { return (uint32_t)((n / NSLOT) & 1); };
-
-    auto do_s = [&](int j) -> bool {
-        const int item = 2 * j;  // ring item holding K_j
-        // the score tile before this one: S_0(j) for S_1(j), S_1(j-1) for S_0(j)
-        const int prev = T == 1 ? j : j - 1;
-        if (prev >= 0 && !wait_spin(sm.s_free(1 - T), (uint32_t)(prev & 1), wc, kSiteMmaPoll)) return false;
-        if (!wait_spin(sm.kv_full(slot_of(item)), par_of(item), wc, kSiteMmaPoll)) return false;
+    int nb = 0;  // ring number of the unit's first K/V item
+    int g0 = 0;  // running index of the unit's first S / P V product
+    for (int u = 0;; ++u) {
+        Unit w;
+        if (!read_unit(sm, wc, u, true, w)) return;  // giving up
+        ptx::mbar_arrive(sm.item_empty(u % ITEM_RING));
+        if (w.n_kv < 0) return;  // end of the list
+        if (!wait_spin(sm.q_full(T), (uint32_t)(u & 1), wc, kSiteMmaQ)) return;
         ptx::tc_fence_after();
-        const uint32_t k_addr = slot0 + slot_of(item) * TILE_BYTES;
-        // K-major, 128-byte swizzle; 8-row atoms 1 KiB apart, or 2 KiB in the paged layout
-        const uint64_t k_desc = PAGED ? ptx::smem_desc(k_addr, 16, PG_GROUP_BYTES, ptx::kLayoutSwizzle128B)
-                                      : ptx::desc_kmajor_sw128(k_addr);
-        issue_s<PAGED>(tmem_base + TM_S, q_desc, k_desc);
-        ptx::umma_commit(sm.s_full(T));
-        ptx::umma_commit(sm.kv_empty(slot_of(item)));  // this stream is done with K_j
-        return true;
-    };
-    auto do_pv = [&](int j) -> bool {
-        const int item = 2 * j + 1;  // ring item holding V_j
-        if (!wait_spin(sm.p_full(T), (uint32_t)(j & 1), wc, kSiteMmaPoll)) return false;
-        if (!wait_spin(sm.kv_full(slot_of(item)), par_of(item), wc, kSiteMmaPoll)) return false;
-        ptx::tc_fence_after();
-        const uint32_t v_addr = slot0 + slot_of(item) * TILE_BYTES;
-        // MN-major, 128-byte swizzle: the two 64-column halves HALF_BYTES apart
-        // and 8-key atoms 1 KiB apart, or 1 KiB and 2 KiB in the paged layout
-        const uint64_t v_desc = PAGED ? ptx::smem_desc(v_addr, PG_HALF_BYTES, PG_GROUP_BYTES, ptx::kLayoutSwizzle128B)
-                                      : ptx::desc_mnmajor_sw128(v_addr, HALF_BYTES);
-        issue_pv<PAGED>(tmem_base + tm_o(T), tmem_base + tm_p(T), v_desc, j > 0 ? 1u : 0u);
-        ptx::umma_commit(sm.o_full(T));
-        ptx::umma_commit(sm.kv_empty(slot_of(item)));  // this stream is done with V_j
-        return true;
-    };
 
-    if (!do_s(0)) return;
-    for (int j = 0; j < w.n_kv; ++j) {
-        if (j + 1 < w.n_kv && !do_s(j + 1)) return;
-        if (!do_pv(j)) return;
+        auto do_s = [&](int j) -> bool {
+            const int g = g0 + j;
+            const int item = nb + 2 * j;  // ring item holding K_j
+            // the score tile before this one: S_0(g) for S_1(g), S_1(g-1) for S_0(g)
+            const int prev = T == 1 ? g : g - 1;
+            if (prev >= 0 && !wait_spin(sm.s_free(1 - T), (uint32_t)(prev & 1), wc, kSiteMmaPoll)) return false;
+            if (!wait_spin(sm.kv_full(slot_of(item)), par_of(item), wc, kSiteMmaPoll)) return false;
+            ptx::tc_fence_after();
+            const uint32_t k_addr = slot0 + slot_of(item) * TILE_BYTES;
+            // K-major, 128-byte swizzle; 8-row atoms 1 KiB apart, or 2 KiB in the paged layout
+            const uint64_t k_desc = PAGED ? ptx::smem_desc(k_addr, 16, PG_GROUP_BYTES, ptx::kLayoutSwizzle128B)
+                                          : ptx::desc_kmajor_sw128(k_addr);
+            issue_s<PAGED>(tmem_base + TM_S, q_desc, k_desc);
+            ptx::umma_commit(sm.s_full(T));
+            ptx::umma_commit(sm.kv_empty(slot_of(item)));  // this stream is done with K_j
+            if (j == w.n_kv - 1) ptx::umma_commit(sm.q_free(T));  // ... and with Q_t
+            return true;
+        };
+        auto do_pv = [&](int j) -> bool {
+            const int item = nb + 2 * j + 1;  // ring item holding V_j
+            if (!wait_spin(sm.p_full(T), (uint32_t)((g0 + j) & 1), wc, kSiteMmaPoll)) return false;
+            if (!wait_spin(sm.kv_full(slot_of(item)), par_of(item), wc, kSiteMmaPoll)) return false;
+            ptx::tc_fence_after();
+            const uint32_t v_addr = slot0 + slot_of(item) * TILE_BYTES;
+            // MN-major, 128-byte swizzle: the two 64-column halves HALF_BYTES apart
+            // and 8-key atoms 1 KiB apart, or 1 KiB and 2 KiB in the paged layout
+            const uint64_t v_desc = PAGED ? ptx::smem_desc(v_addr, PG_HALF_BYTES, PG_GROUP_BYTES, ptx::kLayoutSwizzle128B)
+                                          : ptx::desc_mnmajor_sw128(v_addr, HALF_BYTES);
+            issue_pv<PAGED>(tmem_base + tm_o(T), tmem_base + tm_p(T), v_desc, j > 0 ? 1u : 0u);
+            ptx::umma_commit(sm.o_full(T));
+            ptx::umma_commit(sm.kv_empty(slot_of(item)));  // this stream is done with V_j
+            return true;
+        };
+
+        if (w.n_kv == 0) {
+            ptx::umma_commit(sm.q_free(T));  // nothing to multiply: Q_t is free at once
+        } else {
+            if (!do_s(0)) return;
+            for (int j = 0; j < w.n_kv; ++j) {
+                if (j + 1 < w.n_kv && !do_s(j + 1)) return;
+                if (!do_pv(j)) return;
+            }
+        }
+        nb += ring_items(w);
+        g0 += w.n_kv;
     }
 }
 
@@ -543,234 +733,269 @@ __device__ __forceinline__ void warp_arrive(uint64_t *bar, int lane) {
     if (lane == 0) ptx::mbar_arrive(bar);
 }
 
-__device__ void softmax_wg(const PrefillParams &p, const Unit &w, const SmemLayout &sm, const WaitCtx &wc,
-                           uint32_t tmem_base, int t, int quarter, int lane, const CUtensorMap *mo) {
+template <int KIND>
+__device__ void softmax_wg(const PrefillParams &p, const SmemLayout &sm, const WaitCtx &wc, uint32_t tmem_base,
+                           int t, int quarter, int lane, const CUtensorMap *mo) {
+    constexpr bool PACKED = KIND != kDense;  // per-sequence offsets: packed batches and paged caches
+    constexpr bool PAGED = KIND == kPaged;
     const int r = quarter * 32 + lane;  // row within the tile == TMEM lane
     const uint32_t lanes = tmem_base + ((uint32_t)(quarter * 32) << 16);
     const uint32_t tS = lanes + TM_S;     // shared score buffer
     const uint32_t tP = lanes + tm_p(t);  // this tile's bf16 P
     const uint32_t tO = lanes + tm_o(t);  // this tile's O accumulator
-    // Selects, not a runtime index: an indexed Unit array would live in local memory.
-    const int s0 = t ? w.s0[1] : w.s0[0];
-    const int head = t ? w.h[1] : w.h[0];
-    const int lim_row = p.causal ? min(s0 + r + w.Sk - w.Sq, w.Sk - 1) : w.Sk - 1;
-    const int lim_tile = p.causal ? min(s0 + w.Sk - w.Sq, w.Sk - 1) : w.Sk - 1;
     const float sl2 = p.scale_log2;
-    float m_run = -INFINITY, l_run = 0.f;
-    bool ok = true;
+    int nb = 0;  // ring number of the unit's first K/V item
+    int g0 = 0;  // running index of the unit's first score tile
+    for (int u = 0;; ++u) {
+        Unit w;
+        const bool got = read_unit(sm, wc, u, false, w);
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(sm.item_empty(u % ITEM_RING));
+        if (!got || w.n_kv < 0) break;  // giving up, or the end of the list (every warp of the group alike)
+        // Selects, not a runtime index: an indexed Unit array would live in local memory.
+        const int s0 = t ? w.s0[1] : w.s0[0];
+        const int head = t ? w.h[1] : w.h[0];
+        const int lim_row = p.causal ? min(s0 + r + w.Sk - w.Sq, w.Sk - 1) : w.Sk - 1;
+        const int lim_tile = p.causal ? min(s0 + w.Sk - w.Sq, w.Sk - 1) : w.Sk - 1;
+        float m_run = -INFINITY, l_run = 0.f;
+        bool ok = true;
 
-    for (int j = 0; j < w.n_kv; ++j) {
-        if (!wait_bounded(sm.s_full(t), j & 1, wc, kSiteSoftmaxS)) {
-            ok = false;
-            break;
-        }
-        ptx::tc_fence_after();
-        float2 s[64];
-        {
-            uint32_t a[32], b[32], c[32], d[32];
-            ptx::tmem_ld32(tS + 0, a);
-            ptx::tmem_ld32(tS + 32, b);
-            ptx::tmem_ld32(tS + 64, c);
-            ptx::tmem_ld32(tS + 96, d);
-            ptx::tmem_wait_ld();
-            // The scores are in registers: release the shared S buffer so the
-            // other tile's next Q K^T can start while this tile's softmax runs.
-            warp_arrive(sm.s_free(t), lane);
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                s[i] = make_float2(__uint_as_float(a[2 * i]), __uint_as_float(a[2 * i + 1]));
-                s[16 + i] = make_float2(__uint_as_float(b[2 * i]), __uint_as_float(b[2 * i + 1]));
-                s[32 + i] = make_float2(__uint_as_float(c[2 * i]), __uint_as_float(c[2 * i + 1]));
-                s[48 + i] = make_float2(__uint_as_float(d[2 * i]), __uint_as_float(d[2 * i + 1]));
-            }
-        }
-        const int kbase = (w.j_lo + j) * BN;  // absolute first key of this tile
-        const bool masked = kbase + BN - 1 > lim_tile;
-        float mx;
-        if (masked) {
-            // Scores of keys the row may not see take no part in the max.
-            float2 sm2[64];
-#pragma unroll
-            for (int i = 0; i < 64; ++i) {
-                sm2[i].x = (kbase + 2 * i <= lim_row) ? s[i].x : -INFINITY;
-                sm2[i].y = (kbase + 2 * i + 1 <= lim_row) ? s[i].y : -INFINITY;
-            }
-            mx = row_max(sm2);
-        } else {
-            mx = row_max(s);
-        }
-        const float m_tile = (mx == -INFINITY) ? -INFINITY : mx * sl2;
-        bool need = false;
-        float m_new = m_tile;
-        if (j > 0) {
-            need = m_tile > m_run + RESCALE_LOG2;
-            m_new = need ? m_tile : m_run;
-        }
-        const float alpha = need ? ptx::ex2(m_run - m_new) : 1.f;
-        const float m_sub = (m_new == -INFINITY) ? 0.f : m_new;
-        uint32_t pk[64];
-        const float rowsum = masked ? softmax_tile<true>(s, pk, sl2, m_sub, kbase, lim_row)
-                                    : softmax_tile<false>(s, pk, sl2, m_sub, kbase, lim_row);
-        // P_t(j-1) and O_t are read / written by PV_t(j-1): wait for it before
-        // overwriting P_t or rescaling O_t (normally it finished long ago).
-        if (j > 0) {
-            if (!wait_bounded(sm.o_full(t), (j - 1) & 1, wc, kSiteSoftmaxO)) {
+        for (int j = 0; j < w.n_kv; ++j) {
+            const int g = g0 + j;
+            if (!wait_bounded(sm.s_full(t), (uint32_t)(g & 1), wc, kSiteSoftmaxS)) {
                 ok = false;
                 break;
             }
             ptx::tc_fence_after();
-        }
-        {
-            uint32_t lo[32], hi[32];
+            float2 s[64];
+            {
+                uint32_t a[32], b[32], c[32], d[32];
+                ptx::tmem_ld32(tS + 0, a);
+                ptx::tmem_ld32(tS + 32, b);
+                ptx::tmem_ld32(tS + 64, c);
+                ptx::tmem_ld32(tS + 96, d);
+                ptx::tmem_wait_ld();
+                // The scores are in registers: release the shared S buffer so the
+                // other tile's next Q K^T can start while this tile's softmax runs.
+                warp_arrive(sm.s_free(t), lane);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                lo[i] = pk[i];
-                hi[i] = pk[32 + i];
+                for (int i = 0; i < 16; ++i) {
+                    s[i] = make_float2(__uint_as_float(a[2 * i]), __uint_as_float(a[2 * i + 1]));
+                    s[16 + i] = make_float2(__uint_as_float(b[2 * i]), __uint_as_float(b[2 * i + 1]));
+                    s[32 + i] = make_float2(__uint_as_float(c[2 * i]), __uint_as_float(c[2 * i + 1]));
+                    s[48 + i] = make_float2(__uint_as_float(d[2 * i]), __uint_as_float(d[2 * i + 1]));
+                }
             }
-            ptx::tmem_st32(tP + 0, lo);
-            ptx::tmem_st32(tP + 32, hi);
+            const int kbase = (w.j_lo + j) * BN;  // absolute first key of this tile
+            const bool masked = kbase + BN - 1 > lim_tile;
+            float mx;
+            if (masked) {
+                // Scores of keys the row may not see take no part in the max.
+                float2 sm2[64];
+#pragma unroll
+                for (int i = 0; i < 64; ++i) {
+                    sm2[i].x = (kbase + 2 * i <= lim_row) ? s[i].x : -INFINITY;
+                    sm2[i].y = (kbase + 2 * i + 1 <= lim_row) ? s[i].y : -INFINITY;
+                }
+                mx = row_max(sm2);
+            } else {
+                mx = row_max(s);
+            }
+            const float m_tile = (mx == -INFINITY) ? -INFINITY : mx * sl2;
+            bool need = false;
+            float m_new = m_tile;
+            if (j > 0) {
+                // Past a 2^8 growth, or a new maximum whose P = 2^(m_tile - m_run)
+                // would exceed half of the running sum l_run.
+                need = m_tile > m_run + RESCALE_LOG2 || (m_tile > m_run && m_tile - m_run > ptx::lg2(l_run) - 1.0f);
+                m_new = need ? m_tile : m_run;
+            }
+            const float alpha = need ? ptx::ex2(m_run - m_new) : 1.f;
+            const float m_sub = (m_new == -INFINITY) ? 0.f : m_new;
+            uint32_t pk[64];
+            const float rowsum = masked ? softmax_tile<true>(s, pk, sl2, m_sub, kbase, lim_row)
+                                        : softmax_tile<false>(s, pk, sl2, m_sub, kbase, lim_row);
+            // P_t(g-1) and O_t are read / written by PV_t(g-1): wait for it before
+            // overwriting P_t or rescaling O_t (normally it finished long ago).
+            // The previous unit's last P V was waited for by its epilogue.
+            if (j > 0) {
+                if (!wait_bounded(sm.o_full(t), (uint32_t)((g - 1) & 1), wc, kSiteSoftmaxO)) {
+                    ok = false;
+                    break;
+                }
+                ptx::tc_fence_after();
+            }
+            {
+                uint32_t lo[32], hi[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    lo[i] = pk[i];
+                    hi[i] = pk[32 + i];
+                }
+                ptx::tmem_st32(tP + 0, lo);
+                ptx::tmem_st32(tP + 32, hi);
+            }
+            if (j > 0 && __any_sync(0xffffffffu, need)) {
+                // O still holds the sum over tiles < j scaled by the old max:
+                // rescale this warp's 32 rows in place, 64 columns per round trip
+                // (two loads in flight per wait).
+                const float2 a2 = make_float2(alpha, alpha);
+#pragma unroll 1
+                for (int ch = 0; ch < 4; ch += 2) {
+                    uint32_t o[32], o2[32];
+                    ptx::tmem_ld32(tO + ch * 32, o);
+                    ptx::tmem_ld32(tO + ch * 32 + 32, o2);
+                    ptx::tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const float2 v =
+                            __fmul2_rn(make_float2(__uint_as_float(o[2 * i]), __uint_as_float(o[2 * i + 1])), a2);
+                        o[2 * i] = __float_as_uint(v.x);
+                        o[2 * i + 1] = __float_as_uint(v.y);
+                        const float2 v2 =
+                            __fmul2_rn(make_float2(__uint_as_float(o2[2 * i]), __uint_as_float(o2[2 * i + 1])), a2);
+                        o2[2 * i] = __float_as_uint(v2.x);
+                        o2[2 * i + 1] = __float_as_uint(v2.y);
+                    }
+                    ptx::tmem_st32(tO + ch * 32, o);
+                    ptx::tmem_st32(tO + ch * 32 + 32, o2);
+                }
+            }
+            ptx::tmem_wait_st();
+            l_run = l_run * alpha + rowsum;
+            m_run = m_new;
+            if (PACKED && kbase + BN > w.Sk) {
+                // Last tile of a packed or paged sequence: the V rows past its end
+                // hold other data (the next sequence's rows, or whatever a page's
+                // unused slots contain).  Their P is 0, but 0 * NaN is NaN, so each
+                // group zeroes those rows in shared memory once the tile has
+                // landed, before releasing its P (the two streams' P V products
+                // are not ordered; both groups write the same zeros).
+                const int item = nb + 2 * j + 1;
+                uint8_t *vt = sm.slot(item % NSLOT);
+                if (!wait_bounded(sm.kv_full(item % NSLOT), (uint32_t)((item / NSLOT) & 1), wc, kSiteSoftmaxV)) {
+                    ok = false;
+                    break;
+                }
+                if (kbase + r >= w.Sk) {
+                    const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+                    // row r, both halves (dense or paged tile layout)
+                    uint8_t *h0 = PAGED ? vt + (r >> 3) * PG_GROUP_BYTES + (r & 7) * 128 : vt + r * 128;
+                    uint8_t *h1 = h0 + (PAGED ? PG_HALF_BYTES : HALF_BYTES);
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        reinterpret_cast<uint4 *>(h0)[c] = z;
+                        reinterpret_cast<uint4 *>(h1)[c] = z;
+                    }
+                }
+                ptx::fence_proxy_async_smem();
+            }
+            warp_arrive(sm.p_full(t), lane);
         }
-        if (j > 0 && __any_sync(0xffffffffu, need)) {
-            // O still holds the sum over tiles < j scaled by the old max:
-            // rescale this warp's 32 rows in place.
-            const float2 a2 = make_float2(alpha, alpha);
+
+        // Epilogue: O / l -> bf16 into this tile's output staging slot of the
+        // ring, then a TMA store from there.  Every warp of the group reaches
+        // the group barrier once per unit, whether or not it gave up on a wait,
+        // and the barrier ANDs everyone's "all well" so that the whole group
+        // takes the same decision to go on or to stop.
+        if (ok && w.n_kv > 0) ok = wait_bounded(sm.o_full(t), (uint32_t)((g0 + w.n_kv - 1) & 1), wc, kSiteEpilogueO);
+        const int o_item = nb + 2 * w.n_kv + t;
+        uint8_t *stage = sm.slot(o_item % NSLOT);
+        if (ok) ok = wait_bounded(sm.kv_full(o_item % NSLOT), (uint32_t)((o_item / NSLOT) & 1), wc, kSiteEpilogueSlot);
+        if (!PACKED && ok && w.part >= 0) {
+            // A key-range part of a split unit: its O (normalised within the range)
+            // and log-sum-exp go to the workspace in fp32 for the merge kernel.
+            ptx::tc_fence_after();
+            const float inv = l_run > 0.f ? 1.0f / l_run : 0.f;
+            const int64_t row = w.ws_row + t * BM + r;
+            float4 *dst = reinterpret_cast<float4 *>(p.ws_o + (row * p.split_parts + w.part) * D);
 #pragma unroll 1
             for (int ch = 0; ch < 4; ++ch) {
                 uint32_t o[32];
                 ptx::tmem_ld32(tO + ch * 32, o);
                 ptx::tmem_wait_ld();
 #pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    float4 x = make_float4(__uint_as_float(o[4 * i]) * inv, __uint_as_float(o[4 * i + 1]) * inv,
+                                           __uint_as_float(o[4 * i + 2]) * inv, __uint_as_float(o[4 * i + 3]) * inv);
+                    if (!(l_run > 0.f)) x = make_float4(0.f, 0.f, 0.f, 0.f);
+                    dst[ch * 8 + i] = x;
+                }
+            }
+            p.ws_lse[row * p.split_parts + w.part] = l_run > 0.f ? (m_run + ptx::lg2(l_run)) * LN2 : -INFINITY;
+        } else if (ok) {
+            ptx::tc_fence_after();
+            const float inv = l_run > 0.f ? 1.0f / l_run : 0.f;
+#pragma unroll 1
+            for (int ch = 0; ch < 4; ++ch) {
+                uint32_t o[32];
+                ptx::tmem_ld32(tO + ch * 32, o);
+                ptx::tmem_wait_ld();
+                uint32_t wv[16];
+#pragma unroll
                 for (int i = 0; i < 16; ++i) {
-                    const float2 v = __fmul2_rn(make_float2(__uint_as_float(o[2 * i]), __uint_as_float(o[2 * i + 1])), a2);
-                    o[2 * i] = __float_as_uint(v.x);
-                    o[2 * i + 1] = __float_as_uint(v.y);
+                    float2 x = __fmul2_rn(make_float2(__uint_as_float(o[2 * i]), __uint_as_float(o[2 * i + 1])),
+                                          make_float2(inv, inv));
+                    if (!(l_run > 0.f)) x = make_float2(0.f, 0.f);
+                    wv[i] = pack_bf16x2_mode(x.x, x.y, p.round_mode);
                 }
-                ptx::tmem_st32(tO + ch * 32, o);
-            }
-        }
-        ptx::tmem_wait_st();
-        l_run = l_run * alpha + rowsum;
-        m_run = m_new;
-        if (p.cu_q != nullptr && kbase + BN > w.Sk) {
-            // Last tile of a packed or paged sequence: the V rows past its end
-            // hold other data (the next sequence's rows, or whatever a page's
-            // unused slots contain).  Their P is 0, but 0 * NaN is NaN, so each
-            // group zeroes those rows in shared memory once the tile has
-            // landed, before releasing its P (the two streams' P V products
-            // are not ordered; both groups write the same zeros).
-            const int item = 2 * j + 1;
-            uint8_t *vt = sm.slot(item % NSLOT);
-            if (!wait_bounded(sm.kv_full(item % NSLOT), (uint32_t)((item / NSLOT) & 1), wc, kSiteSoftmaxV)) {
-                ok = false;
-                break;
-            }
-            if (kbase + r >= w.Sk) {
-                const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-                // row r, both halves (dense or paged tile layout)
-                uint8_t *h0 = p.block_table != nullptr ? vt + (r >> 3) * PG_GROUP_BYTES + (r & 7) * 128 : vt + r * 128;
-                uint8_t *h1 = h0 + (p.block_table != nullptr ? PG_HALF_BYTES : HALF_BYTES);
+                // 32 columns = 64 bytes = four 16-byte chunks of the 128-B swizzled row.
+                uint8_t *rowp = stage + (ch >> 1) * HALF_BYTES + r * 128;
 #pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    reinterpret_cast<uint4 *>(h0)[c] = z;
-                    reinterpret_cast<uint4 *>(h1)[c] = z;
+                for (int kk = 0; kk < 4; ++kk) {
+                    const int cc = (ch & 1) * 4 + kk;
+                    *reinterpret_cast<uint4 *>(rowp + ((cc ^ (r & 7)) << 4)) =
+                        make_uint4(wv[4 * kk], wv[4 * kk + 1], wv[4 * kk + 2], wv[4 * kk + 3]);
                 }
             }
-            ptx::fence_proxy_async_smem();
-        }
-        warp_arrive(sm.p_full(t), lane);
-    }
-
-    // Epilogue: O / l -> bf16 into the (now free) Q tile buffer, then TMA store.
-    // Every warp of the group reaches the named barrier exactly once, whether
-    // or not it gave up on a wait, so the barrier itself can never hang; a warp
-    // that gave up has raised the abort flag before arriving, and the leader
-    // checks it after the barrier.
-    if (ok && w.n_kv > 0) ok = wait_bounded(sm.o_full(t), (w.n_kv - 1) & 1, wc, kSiteEpilogueO);
-    uint8_t *stage = sm.q_tile(t);
-    if (ok && w.part >= 0) {
-        // A key-range part of a split unit: its O (normalised within the range)
-        // and log-sum-exp go to the workspace in fp32 for the merge kernel.
-        ptx::tc_fence_after();
-        const float inv = l_run > 0.f ? 1.0f / l_run : 0.f;
-        const int64_t row = w.ws_row + t * BM + r;
-        float4 *dst = reinterpret_cast<float4 *>(p.ws_o + (row * p.split_parts + w.part) * D);
-#pragma unroll 1
-        for (int ch = 0; ch < 4; ++ch) {
-            uint32_t o[32];
-            ptx::tmem_ld32(tO + ch * 32, o);
-            ptx::tmem_wait_ld();
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                float4 x = make_float4(__uint_as_float(o[4 * i]) * inv, __uint_as_float(o[4 * i + 1]) * inv,
-                                       __uint_as_float(o[4 * i + 2]) * inv, __uint_as_float(o[4 * i + 3]) * inv);
-                if (!(l_run > 0.f)) x = make_float4(0.f, 0.f, 0.f, 0.f);
-                dst[ch * 8 + i] = x;
+            const int srow = s0 + r;
+            if (p.lse != nullptr && srow < w.Sq) {
+                const float lse = l_run > 0.f ? (m_run + ptx::lg2(l_run)) * LN2 : -INFINITY;
+                const int64_t li = PACKED ? (int64_t)head * p.total_q + w.q0 + srow
+                                          : ((int64_t)w.b * p.Hq + head) * p.Sq + srow;
+                p.lse[li] = lse;
             }
         }
-        p.ws_lse[row * p.split_parts + w.part] = l_run > 0.f ? (m_run + ptx::lg2(l_run)) * LN2 : -INFINITY;
-    } else if (ok) {
-        ptx::tc_fence_after();
-        const float inv = l_run > 0.f ? 1.0f / l_run : 0.f;
-#pragma unroll 1
-        for (int ch = 0; ch < 4; ++ch) {
-            uint32_t o[32];
-            ptx::tmem_ld32(tO + ch * 32, o);
-            ptx::tmem_wait_ld();
-            uint32_t wv[16];
+        ptx::tc_fence_before();
+        ptx::fence_proxy_async_smem();
+        if (!ptx::named_bar_and(1 + t, 128, ok && !*wc.abort_flag)) break;
+        const bool leader = quarter == 0 && lane == 0;
+        if (PACKED && s0 + BM > w.Sq) {
+            // Last row block of a packed sequence: a full box would spill into the
+            // next sequence's rows, so each thread stores its own row (if valid)
+            // from the swizzled staging tile; the group then waits for all rows
+            // before the slot is handed back.
+            if (s0 + r < w.Sq) {
+                uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.out) +
+                                                       ((int64_t)(w.q0 + s0 + r) * p.Hq + head) * D);
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                float2 x = __fmul2_rn(make_float2(__uint_as_float(o[2 * i]), __uint_as_float(o[2 * i + 1])),
-                                      make_float2(inv, inv));
-                if (!(l_run > 0.f)) x = make_float2(0.f, 0.f);
-                wv[i] = pack_bf16x2_mode(x.x, x.y, p.round_mode);
+                for (int c = 0; c < 16; ++c)
+                    dst[c] = *reinterpret_cast<const uint4 *>(stage + (c >> 3) * HALF_BYTES + r * 128 +
+                                                               (((c & 7) ^ (r & 7)) << 4));
             }
-            // 32 columns = 64 bytes = four 16-byte chunks of the 128-B swizzled row.
-            uint8_t *rowp = stage + (ch >> 1) * HALF_BYTES + r * 128;
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const int cc = (ch & 1) * 4 + k;
-                *reinterpret_cast<uint4 *>(rowp + ((cc ^ (r & 7)) << 4)) =
-                    make_uint4(wv[4 * k], wv[4 * k + 1], wv[4 * k + 2], wv[4 * k + 3]);
-            }
+            ptx::named_bar_sync(1 + t, 128);
+        } else if (leader && s0 < w.Sq && (PACKED || w.part < 0)) {
+            const Coord4 lo = coord4(p.bhsd, 0, head, w.q0 + s0, w.tb);
+            const Coord4 hi = coord4(p.bhsd, 64, head, w.q0 + s0, w.tb);
+            // O is written once and not read again here: evict-first, so its dirty
+            // lines leave L2 early instead of crowding out K/V and later work.
+            const uint64_t pol_o = ptx::policy_evict_first();
+            ptx::tma_store_4d_hint(mo, stage, lo.c0, lo.c1, lo.c2, lo.c3, pol_o);
+            ptx::tma_store_4d_hint(mo, stage + HALF_BYTES, hi.c0, hi.c1, hi.c2, hi.c3, pol_o);
+            ptx::bulk_commit_group();
+            ptx::bulk_wait_group_read0();
         }
-        const int srow = s0 + r;
-        if (p.lse != nullptr && srow < w.Sq) {
-            const float lse = l_run > 0.f ? (m_run + ptx::lg2(l_run)) * LN2 : -INFINITY;
-            const int64_t li = p.cu_q != nullptr ? (int64_t)head * p.total_q + w.q0 + srow
-                                                 : ((int64_t)w.b * p.Hq + head) * p.Sq + srow;
-            p.lse[li] = lse;
-        }
-    }
-    ptx::fence_proxy_async_smem();
-    ptx::named_bar_sync(1 + t, 128);
-    if (p.cu_q != nullptr && s0 + BM > w.Sq) {
-        // Last row block of a packed sequence: a full box would spill into the
-        // next sequence's rows, so each thread stores its own row (if valid)
-        // from the swizzled staging tile.
-        if (s0 + r < w.Sq && !*wc.abort_flag) {
-            uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.out) +
-                                                   ((int64_t)(w.q0 + s0 + r) * p.Hq + head) * D);
-#pragma unroll
-            for (int c = 0; c < 16; ++c)
-                dst[c] = *reinterpret_cast<const uint4 *>(stage + (c >> 3) * HALF_BYTES + r * 128 +
-                                                           (((c & 7) ^ (r & 7)) << 4));
-        }
-    } else if (quarter == 0 && lane == 0 && s0 < w.Sq && w.part < 0 && !*wc.abort_flag) {
-        const Coord4 lo = coord4(p.bhsd, 0, head, w.q0 + s0, w.tb);
-        const Coord4 hi = coord4(p.bhsd, 64, head, w.q0 + s0, w.tb);
-        // O is written once and not read again here: evict-first, so its dirty
-        // lines leave L2 early instead of crowding out K/V and later work.
-        const uint64_t pol_o = ptx::policy_evict_first();
-        ptx::tma_store_4d_hint(mo, stage, lo.c0, lo.c1, lo.c2, lo.c3, pol_o);
-        ptx::tma_store_4d_hint(mo, stage + HALF_BYTES, hi.c0, hi.c1, hi.c2, hi.c3, pol_o);
-        ptx::bulk_commit_group();
-        ptx::bulk_wait_group_read0();
+        // The slot is free again once the store has read it (one arrival for
+        // each of the two streams that release K/V slots).
+        if (leader) ptx::mbar_arrive_cnt(sm.kv_empty(o_item % NSLOT), 2);
+        nb += ring_items(w);
+        g0 += w.n_kv;
     }
 }
 
 // ------------------------------------------------------------------ kernel
 
-template <bool EARLY>
+template <int KIND>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                    const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_o,
@@ -784,18 +1009,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const Unit w = decode_unit(p, blockIdx.x);
-    // A unit whose rows all lie past its sequence's end (packed batches, whose
-    // grid is sized by the longest sequence) has nothing to do.
-    if (w.s0[0] >= w.Sq) return;
 
-    int first = 0;  // ring items issued before the CTA-wide barrier (thread 0, EARLY)
     if (threadIdx.x == 0) {
-        ptx::mbar_init(sm.q_full(), 1);
-        ptx::mbar_init(sm.q_full1(), 1);
+        for (int t = 0; t < 2; ++t) {
+            ptx::mbar_init(sm.q_full(t), 1);
+            ptx::mbar_init(sm.q_free(t), 1);  // one commit by the tile's issuing stream
+        }
         for (int s = 0; s < NSLOT; ++s) {
             ptx::mbar_init(sm.kv_full(s), 1);
-            ptx::mbar_init(sm.kv_empty(s), 2);  // one release per issuing stream
+            ptx::mbar_init(sm.kv_empty(s), 2);  // one release per issuing stream (or a staging slot's 2)
         }
         // Softmax-side barriers take one arrival per warp (lane 0, after the
         // warp's tcgen05 fence and __syncwarp).
@@ -803,18 +1025,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             ptx::mbar_init(sm.s_full(t), 1);
             ptx::mbar_init(sm.p_full(t), 4);
             ptx::mbar_init(sm.o_full(t), 1);
+            ptx::mbar_init(sm.s_free(t), 4);
         }
-        ptx::mbar_init(sm.s_free(0), 4);
-        ptx::mbar_init(sm.s_free(1), 4);
         ptx::mbar_init(sm.fin(), 2);  // one commit per issuing stream
+        for (int i = 0; i < ITEM_RING; ++i) {
+            ptx::mbar_init(sm.item_full(i), 1);
+            ptx::mbar_init(sm.item_empty(i), ITEM_READERS);
+        }
         *sm.abort_flag() = 0;
         ptx::fence_mbar_init();
         ptx::prefetch_tensormap(&map_q);
         ptx::prefetch_tensormap(&map_k);
         ptx::prefetch_tensormap(&map_v);
         ptx::prefetch_tensormap(&map_o);
-        if (EARLY && p.block_table == nullptr && p.inject != 1 && w.n_kv > 0)
-            first = producer_start(p, w, sm, &map_q, &map_k, &map_v);
     }
     if (warp == 1) {
         ptx::tmem_alloc(sm.tmem_slot(), 512);
@@ -829,19 +1052,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (warp < 4) {
         ptx::setmaxnreg_dec<REGS_CONTROL>();
         if (warp == 0) {
-            if (p.block_table != nullptr)
-                producer_paged(p, w, sm, wc, lane, &map_q, &map_k, &map_v, &map_k8, &map_v8);
+            if (KIND == kPaged)
+                producer_paged(p, sm, wc, lane, &map_q, &map_k, &map_v, &map_k8, &map_v8);
             else if (lane == 0)
-                producer<EARLY>(p, w, sm, wc, &map_q, &map_k, &map_v, first);
+                producer<KIND>(p, sm, wc, &map_q, &map_k, &map_v);
         } else if (warp == 1 || warp == 2) {
             if (lane == 0) {
-                const bool paged = p.block_table != nullptr;
                 if (warp == 1)
-                    paged ? mma_stream<0, true, false>(w, sm, wc, tmem_base)
-                          : mma_stream<0, false, EARLY>(w, sm, wc, tmem_base);
+                    mma_stream<0, KIND == kPaged>(p, sm, wc, tmem_base);
                 else
-                    paged ? mma_stream<1, true, false>(w, sm, wc, tmem_base)
-                          : mma_stream<1, false, EARLY>(w, sm, wc, tmem_base);
+                    mma_stream<1, KIND == kPaged>(p, sm, wc, tmem_base);
                 // Whatever happened, wait until every product issued (by
                 // either stream) has completed before tensor memory is released.
                 ptx::umma_commit(sm.fin());
@@ -852,7 +1072,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     } else {
         ptx::setmaxnreg_inc<REGS_SOFTMAX>();
         const int t = (warp - 4) >> 2;
-        softmax_wg(p, w, sm, wc, tmem_base, t, warp & 3, lane, &map_o);
+        softmax_wg<KIND>(p, sm, wc, tmem_base, t, warp & 3, lane, &map_o);
         __syncwarp();
     }
 
@@ -863,6 +1083,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (warp == 1) {
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem_base, 512);
+    }
+    if (threadIdx.x == 0 && (int)gridDim.x < p.n_items) {
+        // The last CTA to finish (every producer has stopped claiming by then)
+        // returns the launch's counter to zero for the next launch that uses it.
+        if (atomicAdd(p.sched + 1, 1u) == gridDim.x - 1) {
+            atomicExch(p.sched, 0u);
+            atomicExch(p.sched + 1, 0u);
+        }
     }
 }
 
@@ -879,20 +1107,27 @@ cudaError_t launch_prefill(const CUtensorMap &mq, const CUtensorMap &mk, const C
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (configured_device != dev) {
-        e = cudaFuncSetAttribute(g1::prefill_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        e = cudaFuncSetAttribute(g1::prefill_kernel<g1::kDense>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(g1::prefill_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+            e = cudaFuncSetAttribute(g1::prefill_kernel<g1::kPacked>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     smem);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(g1::prefill_kernel<g1::kPaged>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     smem);
         if (e != cudaSuccess) return e;
         configured_device = dev;
     }
-    // Short non-causal units (few K/V tiles) start their first copies before
-    // the CTA-wide barrier; every other launch runs the plain instantiation.
-    if (p.early_start && p.block_table == nullptr)
-        g1::prefill_kernel<true><<<num_ctas, g1::NUM_THREADS, smem, stream>>>(mq, mk, mv, mo, mk8, mv8, p);
+    // One instantiation per kind of launch, each with only its own paths.
+    if (p.block_table != nullptr)
+        g1::prefill_kernel<g1::kPaged><<<num_ctas, g1::NUM_THREADS, smem, stream>>>(mq, mk, mv, mo, mk8, mv8, p);
+    else if (p.cu_q != nullptr)
+        g1::prefill_kernel<g1::kPacked><<<num_ctas, g1::NUM_THREADS, smem, stream>>>(mq, mk, mv, mo, mk8, mv8, p);
     else
-        g1::prefill_kernel<false><<<num_ctas, g1::NUM_THREADS, smem, stream>>>(mq, mk, mv, mo, mk8, mv8, p);
+        g1::prefill_kernel<g1::kDense><<<num_ctas, g1::NUM_THREADS, smem, stream>>>(mq, mk, mv, mo, mk8, mv8, p);
     return cudaGetLastError();
 }
+
+int prefill_grid(int n_items, int num_sms) { return n_items < num_sms ? n_items : num_sms; }
 
 int prefill_num_units(const PrefillParams &p) {
     if (p.pair_heads) return p.B * p.Hkv * (p.G / 2) * p.n_m;

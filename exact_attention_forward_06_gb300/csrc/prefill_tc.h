@@ -24,8 +24,12 @@ struct PrefillParams {
     // split_units units is cut into split_parts key ranges, one CTA each, whose
     // fp32 partials go to ws_o [split_units*256][split_parts][128] and
     // ws_lse [split_units*256][split_parts] and are merged afterwards.
-    int prefetch_ahead;  // > 0: L2-prefetch the Q tiles of the unit this many CTAs ahead
-    int early_start;     // 1: a unit's first copies go out before the CTA-wide barrier
+    int prefetch_ahead;  // > 0: L2-prefetch the Q tiles of a CTA's next unit (or of the
+                         // unit this many items ahead when every CTA has one unit)
+    int n_items;         // work items: whole units, then the parts of split units; with
+                         // fewer CTAs than items each CTA claims the next free item
+    unsigned *sched;     // [2] device counters of this launch: next item, CTAs done (both
+                         // zero at launch; the last CTA resets them)
     int n_full_units;
     int kv_major;        // 1: units ordered by sequence and KV head (see unit_coords)
     int split_units;
@@ -52,8 +56,12 @@ struct PrefillParams {
 
 int prefill_smem_bytes();
 int prefill_num_units(const PrefillParams &p);
+// Grid for n_items work items on a device with num_sms SMs: one CTA per SM,
+// each looping over its items, when there are more items than SMs.
+int prefill_grid(int n_items, int num_sms);
 // mk8/mv8: paged K/V only, the same pool maps with 128-row boxes (a run of 8
-// consecutive pages); pass mk/mv otherwise.
+// consecutive pages); pass mk/mv otherwise.  num_ctas <= p.n_items: with
+// fewer CTAs than items each CTA loops over its items (persistent grid).
 cudaError_t launch_prefill(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
                            const CUtensorMap &mo, const CUtensorMap &mk8, const CUtensorMap &mv8,
                            const PrefillParams &p, int num_ctas, cudaStream_t stream);

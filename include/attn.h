@@ -92,6 +92,16 @@ typedef enum {
  * value >= 0 is accepted.
  * Results are deterministic: the same call on the same device returns
  * bitwise-identical out and lse.
+ *
+ * Scheduling.  The work is cut into units of two 128-row Q tiles.  When there
+ * are more units than SMs the kernel runs one CTA per SM, and each CTA takes
+ * the next free unit from a counter in device memory as it finishes one
+ * (which unit a CTA gets changes nothing in the result).  The library owns a
+ * pool of 256 such counters per device and gives each launch the next one in
+ * turn, and a launch's last CTA sets its counter back to zero: so at most 256
+ * of these launches (attn_fwd, attn_fwd_rounded, attn_fwd_varlen,
+ * attn_fwd_paged, attn_fwd_host) may be in flight on one device at the same
+ * time.  Launches on one stream, and graph replays, are always fine.
  */
 attn_status_t attn_fwd(const void *q, const void *k, const void *v, void *out, float *lse,
                        int B, int Hq, int Hkv, int Sq, int Sk, int d,

@@ -69,6 +69,10 @@ SMALL = [
     ("bhsd_gqa_causal", 1, 4, 2, 1024, 1024, "bhsd", True),
     ("three_row_blocks_g1", 1, 2, 2, 384, 384, "bshd", False),
     ("short_causal_g1", 1, 1, 1, 130, 130, "bshd", True),
+    # more units than SMs, so each CTA loops over several: units whose rows see
+    # no key (causal, Sq > Sk) between ordinary ones, and an odd group size
+    ("looping_units_masked_rows", 4, 32, 8, 2048, 512, "bshd", True),
+    ("looping_units_odd_group", 8, 6, 2, 1000, 1000, "bhsd", True),
 ]
 
 

@@ -47,6 +47,7 @@ static attn::PrefillParams params(int B, int Hq, int Hkv, int Sq, int Sk, bool c
     p.kv_major = kv_major;
     p.split_parts = 1;
     p.n_full_units = attn::prefill_num_units(p);
+    p.n_items = p.n_full_units;
     return p;
 }
 
