@@ -439,7 +439,7 @@ def run_sustained(prefill, decode, flops, step_ms, dev, stream, peaks, peak_src,
 
 # Prefill workloads reported beside the headline, in this order.
 OTHER_WORKLOADS = [inputs.TINY_BHSD.name, inputs.MQA_CAUSAL.name, inputs.RAGGED_SELF.name, inputs.RAGGED_CROSS.name,
-                   inputs.VARLEN_CAUSAL.name, inputs.PAGED_PREFILL.name]
+                   inputs.VARLEN_CAUSAL.name, inputs.PAGED_PREFILL.name, inputs.GQA_SHORT_QUERY.name]
 L2_BYTES = 129 << 20         # GB300's L2
 L2_FLUSH_BYTES = 256 << 20   # about twice the L2
 

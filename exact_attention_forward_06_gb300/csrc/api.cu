@@ -97,8 +97,11 @@ uint64_t budget() { return g_budget.load(std::memory_order_relaxed); }
 
 // 4-D bf16 map over a dense BSHD ([B][S][H][d], dims {d,H,S,B}) or BHSD
 // ([B][H][S][d], dims {d,S,H,B}) tensor; box = 64 head-dim elements (128 B,
-// 128-byte swizzle) x `rows` sequence positions of one head.
-bool make_map_4d(CUtensorMap *m, const void *ptr, bool bhsd, int B, int S, int H, int d, int rows) {
+// 128-byte swizzle) x `rows` sequence positions x `heads` heads.  With one
+// head the box is `rows` rows of one head; with G heads and 128 / G rows it
+// is a head-packed Q or O tile, whose 128 rows land in shared memory as
+// (position, head) pairs, head fastest in BSHD (position fastest in BHSD).
+bool make_map_4d(CUtensorMap *m, const void *ptr, bool bhsd, int B, int S, int H, int d, int rows, int heads = 1) {
     const cuuint64_t e = 2;
     cuuint64_t dims[4], strides[3];
     cuuint32_t box[4];
@@ -107,13 +110,13 @@ bool make_map_4d(CUtensorMap *m, const void *ptr, bool bhsd, int B, int S, int H
         strides[0] = (cuuint64_t)d * e;
         strides[1] = (cuuint64_t)S * d * e;
         strides[2] = (cuuint64_t)H * S * d * e;
-        box[0] = 64; box[1] = rows; box[2] = 1; box[3] = 1;
+        box[0] = 64; box[1] = rows; box[2] = heads; box[3] = 1;
     } else {
         dims[0] = d; dims[1] = H; dims[2] = S; dims[3] = B;
         strides[0] = (cuuint64_t)d * e;
         strides[1] = (cuuint64_t)H * d * e;
         strides[2] = (cuuint64_t)S * H * d * e;
-        box[0] = 64; box[1] = 1; box[2] = rows; box[3] = 1;
+        box[0] = 64; box[1] = heads; box[2] = rows; box[3] = 1;
     }
     const cuuint32_t es[4] = {1, 1, 1, 1};
     CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(ptr), dims, strides, box, es,
@@ -190,6 +193,24 @@ attn_status_t fill_prefill_params(attn::PrefillParams *p, const DeviceInfo *di, 
     p->lse = lse;
     p->n_m = (Sq + 127) / 128;
     p->pair_heads = (p->G % 2 == 0) ? 1 : 0;
+    // GQA Q-head packing: a Q tile holds 128 / G positions of all G heads of
+    // a KV group, so one K/V tile staged in shared memory serves every head
+    // of the group, and short query lengths still fill the tile's 128 rows.
+    // Possible when G divides 128 (dense launches; the packed-batch entry
+    // points turn it off).  Used when it pads fewer rows than head pairing:
+    // a unit then covers 2 * 128 / G positions instead of 128 (or 256).  On
+    // long sequences, where neither pads, the two measure the same within
+    // half a percent (pairing ahead), so a tie keeps pairing.
+    {
+        const bool can_pack = p->G >= 2 && 128 % p->G == 0;
+        const int span_pack = can_pack ? 2 * (128 / p->G) : 0;
+        const int span_pair = p->pair_heads ? 128 : 256;
+        const int64_t pad_pack = can_pack ? (int64_t)span_pack * ((Sq + span_pack - 1) / span_pack) - Sq : 0;
+        const int64_t pad_pair = (int64_t)span_pair * ((Sq + span_pair - 1) / span_pair) - Sq;
+        p->pack_heads = (can_pack && pad_pack < pad_pair) ? 1 : 0;
+    }
+    p->pack_pos = p->pack_heads ? 128 / p->G : 0;
+    p->n_pk = p->pack_heads ? (Sq + 2 * p->pack_pos - 1) / (2 * p->pack_pos) : 0;
     p->status = di->status;
     p->budget_ns = budget();
     p->inject = 0;
@@ -236,9 +257,12 @@ attn_status_t attn_fwd_rounded(const void *q, const void *k, const void *v, void
     p.round_mode = round_mode;
     p.inject = g_inject.exchange(0);
     const bool bhsd = p.bhsd != 0;
+    // Q and O boxes: one head x 128 positions, or with head packing the
+    // group's G heads x 128 / G positions.
+    const int q_rows = p.pack_heads ? p.pack_pos : 128, q_heads = p.pack_heads ? p.G : 1;
     CUtensorMap mq, mk, mv, mo;
-    if (!make_map_4d(&mq, q, bhsd, B, Sq, Hq, d, 128) || !make_map_4d(&mk, k, bhsd, B, Sk, Hkv, d, 128) ||
-        !make_map_4d(&mv, v, bhsd, B, Sk, Hkv, d, 128) || !make_map_4d(&mo, out, bhsd, B, Sq, Hq, d, 128))
+    if (!make_map_4d(&mq, q, bhsd, B, Sq, Hq, d, q_rows, q_heads) || !make_map_4d(&mk, k, bhsd, B, Sk, Hkv, d, 128) ||
+        !make_map_4d(&mv, v, bhsd, B, Sk, Hkv, d, 128) || !make_map_4d(&mo, out, bhsd, B, Sq, Hq, d, q_rows, q_heads))
         return ATTN_ERR_CUDA;
     const int units = attn::prefill_num_units(p);
     int ctas = units;
@@ -294,6 +318,7 @@ attn_status_t attn_fwd_varlen(const void *q, const void *k, const void *v, void 
     p.round_mode = round_mode;
     p.cu_q = cu_seqlens_q;
     p.prefetch_ahead = 0;  // (dense coordinates only)
+    p.pack_heads = 0;      // (dense launches only)
     p.cu_k = cu_seqlens_k;
     // Keys much longer than queries (chunks against a context): K/V-first order.
     p.kv_major = max_seqlen_k >= 2 * max_seqlen_q ? 1 : 0;
@@ -341,6 +366,7 @@ attn_status_t attn_fwd_paged(const void *q, const void *k_pages, const void *v_p
     p.round_mode = round_mode;
     p.cu_q = cu_seqlens_q;
     p.prefetch_ahead = 0;  // (dense coordinates only)
+    p.pack_heads = 0;      // (dense launches only)
     p.total_q = total_q;
     p.out = out;
     p.block_table = block_table;

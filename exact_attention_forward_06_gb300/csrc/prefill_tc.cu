@@ -165,8 +165,9 @@ struct Unit {
 __host__ __device__ __forceinline__ void unit_kv_range(const PrefillParams &p, Unit &w) {
     const int n_full = (w.Sk + BN - 1) / BN;
     if (p.causal) {
-        int last_row = w.s0[0] + BM - 1;
-        if (w.s0[1] < w.Sq) last_row = last_row > w.s0[1] + BM - 1 ? last_row : w.s0[1] + BM - 1;
+        const int span = p.pack_heads ? p.pack_pos : BM;  // positions a tile covers
+        int last_row = w.s0[0] + span - 1;
+        if (w.s0[1] < w.Sq) last_row = last_row > w.s0[1] + span - 1 ? last_row : w.s0[1] + span - 1;
         last_row = last_row < w.Sq - 1 ? last_row : w.Sq - 1;
         const int lim = last_row + w.Sk - w.Sq;  // last visible key of the lowest row
         w.n_kv = lim < 0 ? 0 : (n_full < lim / BN + 1 ? n_full : lim / BN + 1);
@@ -186,7 +187,25 @@ __host__ __device__ __forceinline__ Unit unit_coords(const PrefillParams &p, int
     // block reads a long context (non-causal launches, whose units are all
     // alike, and chunks against a cache); the host chooses.
     const bool kv_major = p.kv_major != 0;
-    if (p.pair_heads) {
+    if (p.pack_heads) {
+        // Both tiles hold every head of KV group g, at positions
+        // [s, s + pack_pos) and [s + pack_pos, s + 2 pack_pos).
+        int bg;
+        if (kv_major) {
+            bg = u / p.n_pk;
+            m_step = u % p.n_pk;
+        } else {
+            const int per = p.B * p.Hkv;
+            m_step = u / per;
+            bg = u % per;
+        }
+        w.b = bg / p.Hkv;
+        w.g = bg % p.Hkv;
+        const int mb = p.causal ? (p.n_pk - 1 - m_step) : m_step;  // causal: longest units first
+        w.h[0] = w.h[1] = w.g * p.G;
+        w.s0[0] = mb * 2 * p.pack_pos;
+        w.s0[1] = w.s0[0] + p.pack_pos;
+    } else if (p.pair_heads) {
         const int pairs = p.G / 2;
         int r;
         if (kv_major) {
@@ -754,8 +773,17 @@ __device__ void softmax_wg(const PrefillParams &p, const SmemLayout &sm, const W
         if (!got || w.n_kv < 0) break;  // giving up, or the end of the list (every warp of the group alike)
         // Selects, not a runtime index: an indexed Unit array would live in local memory.
         const int s0 = t ? w.s0[1] : w.s0[0];
-        const int head = t ? w.h[1] : w.h[0];
-        const int lim_row = p.causal ? min(s0 + r + w.Sk - w.Sq, w.Sk - 1) : w.Sk - 1;
+        const int h0 = t ? w.h[1] : w.h[0];
+        // This thread's row: position `pos` of head `head` (with head packing
+        // the tile holds every head of the group at fewer positions).
+        int pos = s0 + r, head = h0;
+        if (!PACKED && p.pack_heads) {
+            const int hr = p.bhsd ? r / p.pack_pos : r % p.G;
+            pos = s0 + (p.bhsd ? r % p.pack_pos : r / p.G);
+            head = h0 + hr;
+        }
+        const int lim_row = p.causal ? min(pos + w.Sk - w.Sq, w.Sk - 1) : w.Sk - 1;
+        // the tile's first position is its smallest
         const int lim_tile = p.causal ? min(s0 + w.Sk - w.Sq, w.Sk - 1) : w.Sk - 1;
         float m_run = -INFINITY, l_run = 0.f;
         bool ok = true;
@@ -948,11 +976,10 @@ __device__ void softmax_wg(const PrefillParams &p, const SmemLayout &sm, const W
                         make_uint4(wv[4 * kk], wv[4 * kk + 1], wv[4 * kk + 2], wv[4 * kk + 3]);
                 }
             }
-            const int srow = s0 + r;
-            if (p.lse != nullptr && srow < w.Sq) {
+            if (p.lse != nullptr && pos < w.Sq) {
                 const float lse = l_run > 0.f ? (m_run + ptx::lg2(l_run)) * LN2 : -INFINITY;
-                const int64_t li = PACKED ? (int64_t)head * p.total_q + w.q0 + srow
-                                          : ((int64_t)w.b * p.Hq + head) * p.Sq + srow;
+                const int64_t li = PACKED ? (int64_t)head * p.total_q + w.q0 + pos
+                                          : ((int64_t)w.b * p.Hq + head) * p.Sq + pos;
                 p.lse[li] = lse;
             }
         }
@@ -965,9 +992,9 @@ __device__ void softmax_wg(const PrefillParams &p, const SmemLayout &sm, const W
             // next sequence's rows, so each thread stores its own row (if valid)
             // from the swizzled staging tile; the group then waits for all rows
             // before the slot is handed back.
-            if (s0 + r < w.Sq) {
+            if (pos < w.Sq) {
                 uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.out) +
-                                                       ((int64_t)(w.q0 + s0 + r) * p.Hq + head) * D);
+                                                       ((int64_t)(w.q0 + pos) * p.Hq + head) * D);
 #pragma unroll
                 for (int c = 0; c < 16; ++c)
                     dst[c] = *reinterpret_cast<const uint4 *>(stage + (c >> 3) * HALF_BYTES + r * 128 +
@@ -975,8 +1002,9 @@ __device__ void softmax_wg(const PrefillParams &p, const SmemLayout &sm, const W
             }
             ptx::named_bar_sync(1 + t, 128);
         } else if (leader && s0 < w.Sq && (PACKED || w.part < 0)) {
-            const Coord4 lo = coord4(p.bhsd, 0, head, w.q0 + s0, w.tb);
-            const Coord4 hi = coord4(p.bhsd, 64, head, w.q0 + s0, w.tb);
+            // (with head packing the output map's box covers the group's heads)
+            const Coord4 lo = coord4(p.bhsd, 0, h0, w.q0 + s0, w.tb);
+            const Coord4 hi = coord4(p.bhsd, 64, h0, w.q0 + s0, w.tb);
             // O is written once and not read again here: evict-first, so its dirty
             // lines leave L2 early instead of crowding out K/V and later work.
             const uint64_t pol_o = ptx::policy_evict_first();
@@ -1130,6 +1158,7 @@ cudaError_t launch_prefill(const CUtensorMap &mq, const CUtensorMap &mk, const C
 int prefill_grid(int n_items, int num_sms) { return n_items < num_sms ? n_items : num_sms; }
 
 int prefill_num_units(const PrefillParams &p) {
+    if (p.pack_heads) return p.B * p.Hkv * p.n_pk;
     if (p.pair_heads) return p.B * p.Hkv * (p.G / 2) * p.n_m;
     return p.B * p.Hq * ((p.n_m + 1) / 2);
 }
@@ -1176,9 +1205,13 @@ __global__ void __launch_bounds__(D) merge_kernel(__nv_bfloat16 *__restrict__ ou
     const int t = (row / BM) & 1;
     const int r = row % BM;
     const Unit w = unit_coords(p, p.n_full_units + su);
-    const int s = (t ? w.s0[1] : w.s0[0]) + r;
+    int s = (t ? w.s0[1] : w.s0[0]) + r;
+    int h = t ? w.h[1] : w.h[0];
+    if (p.pack_heads) {  // row r of a packed tile: its position and head
+        s = (t ? w.s0[1] : w.s0[0]) + (p.bhsd ? r % p.pack_pos : r / p.G);
+        h += p.bhsd ? r / p.pack_pos : r % p.G;
+    }
     if (s >= p.Sq) return;
-    const int h = t ? w.h[1] : w.h[0];
     const int e = threadIdx.x;
     const float *ls = p.ws_lse + (int64_t)row * p.split_parts;
     float M = -INFINITY;

@@ -16,6 +16,11 @@ struct PrefillParams {
     float *lse;        // [B][Hq][Sq] or nullptr
     int n_m;           // ceil(Sq / 128)
     int pair_heads;    // 1: a unit is two heads of one KV group at the same rows
+    int pack_heads;    // 1: a Q tile is pack_pos positions x all G heads of one KV group
+                       //    (row r: position r / G, head r % G in BSHD; head r / pack_pos,
+                       //    position r % pack_pos in BHSD); dense launches only
+    int pack_pos;      // 128 / G when packing
+    int n_pk;          // units per (batch, KV group) when packing: ceil(Sq / (2 * pack_pos))
     unsigned *status;  // device status word [code, site]
     uint64_t budget_ns;
     int inject;        // 1: producer issues nothing (fault-injection test)

@@ -145,7 +145,12 @@ RAGGED_SELF = PrefillWorkload("ragged_self_2x12_32760", 2, 12, 12, 32760, 32760,
 RAGGED_CROSS = PrefillWorkload("ragged_cross_2x12_32760x512", 2, 12, 12, 32760, 512, seed=40)
 PAGED_DECODE = DecodeWorkload("paged_decode_32seq_32q8kv")
 
-PREFILL_WORKLOADS = {w.name: w for w in (TINY_BHSD, GQA_CAUSAL, MQA_CAUSAL, RAGGED_SELF, RAGGED_CROSS)}
+# A short query chunk against a long context (a speculative-decoding verify
+# step): not one of the benchmark's configurations; shows GQA head packing.
+GQA_SHORT_QUERY = PrefillWorkload("gqa_short_query_32x32q4kv_16x4096", 32, 32, 4, 16, 4096, seed=41)
+
+PREFILL_WORKLOADS = {w.name: w for w in (TINY_BHSD, GQA_CAUSAL, MQA_CAUSAL, RAGGED_SELF, RAGGED_CROSS,
+                                         GQA_SHORT_QUERY)}
 # A packed batch of 16 GQA sequences of mixed lengths, causal (the varlen case).
 VARLEN_CAUSAL = VarlenWorkload("varlen_causal_16seq_32q8kv", 16, 32, 8, len_lo=256, len_hi=8192, causal=True,
                                seed=6)

@@ -73,6 +73,12 @@ SMALL = [
     # no key (causal, Sq > Sk) between ordinary ones, and an odd group size
     ("looping_units_masked_rows", 4, 32, 8, 2048, 512, "bshd", True),
     ("looping_units_odd_group", 8, 6, 2, 1000, 1000, "bhsd", True),
+    # GQA head packing with short query lengths (a tile: 128 / G positions x G heads)
+    ("packed_short_q_g8_causal", 8, 32, 4, 16, 4096, "bshd", True),
+    ("packed_short_q_g32_bhsd", 2, 32, 1, 5, 700, "bhsd", False),
+    ("packed_g8_ragged_causal", 3, 16, 2, 70, 300, "bshd", True),
+    ("packed_g4_ragged_bhsd", 2, 8, 2, 45, 130, "bhsd", True),
+    ("packed_looping_units", 40, 32, 8, 40, 600, "bshd", True),   # 320 packed units: every CTA loops
 ]
 
 
@@ -181,7 +187,8 @@ def test_output_guard_regions_untouched(A):
 
 # ---------------------------------------------------------------- full-size workloads, every output
 
-FULL = [inputs.TINY_BHSD, inputs.GQA_CAUSAL, inputs.MQA_CAUSAL, inputs.RAGGED_SELF, inputs.RAGGED_CROSS]
+FULL = [inputs.TINY_BHSD, inputs.GQA_CAUSAL, inputs.MQA_CAUSAL, inputs.RAGGED_SELF, inputs.RAGGED_CROSS,
+        inputs.GQA_SHORT_QUERY]
 
 
 def _run_as_benched(A, w, q, k, v):

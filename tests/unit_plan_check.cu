@@ -11,7 +11,11 @@
 //      tile of a non-causal unit;
 //   3. the tail-split plan cuts the partial last wave into parts of at least
 //      4 K/V tiles that fill it, only for non-causal launches;
-//   4. the decode split plan covers every page with 16 to 256 pages a split.
+//   4. the decode split plan covers every page with 16 to 256 pages a split;
+//   5. with GQA head packing, the units cover every (batch, head, position)
+//      of a launch exactly once, a tile holding the 128 / G positions of all
+//      G heads of one KV group, and a causal unit's K/V tile count is again
+//      the brute-force count for its last position.
 #include <cstdio>
 #include <cstdlib>
 #include <set>
@@ -92,6 +96,37 @@ static void check_units(int B, int Hq, int Hkv, int Sq, int Sk, bool causal, int
           tiles);
 }
 
+static void check_packed_units(int B, int Hq, int Hkv, int Sq, int Sk, bool causal, int kv_major) {
+    attn::PrefillParams p = params(B, Hq, Hkv, Sq, Sk, causal, kv_major);
+    p.pack_heads = 1;
+    p.pack_pos = 128 / p.G;
+    p.n_pk = (Sq + 2 * p.pack_pos - 1) / (2 * p.pack_pos);
+    const int units = attn::prefill_num_units(p);
+    const int P = p.pack_pos;
+    std::set<std::tuple<int, int, int>> seen;  // (b, head, position)
+    for (int u = 0; u < units; ++u) {
+        const attn::g1::Unit w = attn::g1::unit_coords(p, u);
+        CHECK(w.b >= 0 && w.b < B && w.g >= 0 && w.g < Hkv, "packed unit %d: batch %d group %d", u, w.b, w.g);
+        CHECK(w.h[0] == w.g * p.G && w.h[1] == w.g * p.G, "packed unit %d: first heads %d %d", u, w.h[0], w.h[1]);
+        CHECK(w.s0[1] == w.s0[0] + P, "packed unit %d: tiles at %d and %d", u, w.s0[0], w.s0[1]);
+        int lo = 1 << 30, hi = -1;
+        for (int t = 0; t < 2; ++t)
+            for (int r = 0; r < 128; ++r) {  // row r of tile t, in the BSHD order (head fastest)
+                const int pos = w.s0[t] + r / p.G, head = w.h[t] + r % p.G;
+                if (pos >= Sq) continue;
+                CHECK(seen.insert(std::make_tuple(w.b, head, pos)).second, "packed unit %d: (b %d, h %d, s %d) twice",
+                      u, w.b, head, pos);
+                lo = pos < lo ? pos : lo;
+                hi = pos + 1 > hi ? pos + 1 : hi;
+            }
+        if (hi > lo)
+            CHECK(w.n_kv == brute_n_kv(p, lo, hi), "packed unit %d (causal %d, Sq %d, Sk %d): n_kv %d, expected %d",
+                  u, (int)causal, Sq, Sk, w.n_kv, brute_n_kv(p, lo, hi));
+    }
+    CHECK(seen.size() == (size_t)B * Hq * Sq, "packed B %d Hq %d Hkv %d Sq %d: %zu rows covered of %zu", B, Hq, Hkv,
+          Sq, seen.size(), (size_t)B * Hq * Sq);
+}
+
 static void check_split_plan(int B, int Hq, int Hkv, int Sq, int Sk, bool causal, int sms) {
     const attn::PrefillParams p = params(B, Hq, Hkv, Sq, Sk, causal, 0);
     int su = -1, parts = -1;
@@ -128,6 +163,11 @@ int main() {
             check_units(2, 8, 2, 520, 130, causal, kv_major);     // Sk < Sq: rows that see no key
             check_units(5, 2, 1, 1, 1, causal, kv_major);         // single rows and keys
             check_units(2, 4, 4, 129, 129, causal, kv_major);
+            check_packed_units(4, 32, 8, 4096, 4096, causal, kv_major);  // G = 4: 32 positions a tile
+            check_packed_units(1, 32, 1, 1000, 1000, causal, kv_major);  // MQA: 4 positions a tile
+            check_packed_units(3, 16, 8, 97, 300, causal, kv_major);     // G = 2, ragged, Sk > Sq
+            check_packed_units(2, 64, 8, 5, 33, causal, kv_major);       // G = 8, a few queries
+            check_packed_units(2, 16, 2, 300, 100, causal, kv_major);    // Sk < Sq: rows that see no key
         }
     for (int sms : {132, 148, 152})
         for (bool causal : tf) {
