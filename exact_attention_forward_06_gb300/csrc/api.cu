@@ -222,6 +222,7 @@ attn_status_t fill_prefill_params(attn::PrefillParams *p, const DeviceInfo *di, 
     // KV head costs no balance; it keeps the units that read the same K/V
     // together, which pays once the K/V of all heads exceed L2.
     p->kv_major = (!causal && (double)B * Hkv * Sk * 128 * 4 > 64.0 * (1 << 20)) ? 1 : 0;
+    p->seq_group = 0;
     // L2 prefetch of the next wave's Q for short non-causal units (few K/V tiles).
     p->prefetch_ahead = (!causal && Sk <= 1024) ? di->sm_count : 0;
     p->split_units = 0;
@@ -322,6 +323,17 @@ attn_status_t attn_fwd_varlen(const void *q, const void *k, const void *v, void 
     p.cu_k = cu_seqlens_k;
     // Keys much longer than queries (chunks against a context): K/V-first order.
     p.kv_major = max_seqlen_k >= 2 * max_seqlen_q ? 1 : 0;
+    // Self-attention batches: sequences in groups of about 160 MB of K/V at
+    // the longest length, row block first within a group (the causal balance
+    // of row block first, with the K/V of only a few sequences in use at
+    // once).  On the 16-sequence workload: groups of 5 run 4% faster than one
+    // group of all 16 and move 1.49 GB from DRAM instead of 5.65 GB (floor
+    // 1.41 GB); groups of 3 and of 1 gave 1.41 and 1.36 GB at +3% and -1.5%.
+    if (!p.kv_major) {
+        const double kv_seq = (double)max_seqlen_k * Hkv * 128 * 2 * 2;
+        const int grp = (int)(160.0 * (1 << 20) / kv_seq);
+        p.seq_group = grp < 1 ? 1 : (grp >= B ? 0 : grp);
+    }
     p.total_q = total_q;
     p.total_k = total_k;
     p.out = out;

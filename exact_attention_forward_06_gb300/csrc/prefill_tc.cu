@@ -208,7 +208,18 @@ __host__ __device__ __forceinline__ Unit unit_coords(const PrefillParams &p, int
     } else if (p.pair_heads) {
         const int pairs = p.G / 2;
         int r;
-        if (kv_major) {
+        if (p.seq_group > 0) {
+            // Sequences in groups of seq_group, row block first within a group
+            // (longest row blocks of the group's sequences first), the groups
+            // one after another: the K/V in use at once is one group's.
+            const int per_seq = p.Hkv * pairs;              // units of one sequence per row-block step
+            const int per_group = p.seq_group * per_seq * p.n_m;
+            const int grp = u / per_group;
+            r = u % per_group;
+            const int nseq = min(p.seq_group, p.B - grp * p.seq_group);
+            m_step = r / (nseq * per_seq);
+            r = (grp * p.seq_group) * per_seq + r % (nseq * per_seq);  // (b, g, pair) index
+        } else if (kv_major) {
             const int bg = u / (p.n_m * pairs);
             r = u % (p.n_m * pairs);
             m_step = r / pairs;
@@ -230,7 +241,15 @@ __host__ __device__ __forceinline__ Unit unit_coords(const PrefillParams &p, int
         const int per = p.B * p.Hq;
         const int n_mp = (p.n_m + 1) / 2;
         m_step = kv_major ? u % n_mp : u / per;
-        const int r = kv_major ? u / n_mp : u % per;
+        int r = kv_major ? u / n_mp : u % per;
+        if (p.seq_group > 0) {  // as above, one head per unit
+            const int per_group = p.seq_group * p.Hq * n_mp;
+            const int grp = u / per_group;
+            const int rr = u % per_group;
+            const int nseq = min(p.seq_group, p.B - grp * p.seq_group);
+            m_step = rr / (nseq * p.Hq);
+            r = grp * p.seq_group * p.Hq + rr % (nseq * p.Hq);
+        }
         w.b = r / p.Hq;
         const int h = r % p.Hq;
         w.g = h / p.G;

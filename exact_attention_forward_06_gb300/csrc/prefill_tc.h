@@ -37,6 +37,8 @@ struct PrefillParams {
                          // zero at launch; the last CTA resets them)
     int n_full_units;
     int kv_major;        // 1: units ordered by sequence and KV head (see unit_coords)
+    int seq_group;       // > 0 (with kv_major = 0): sequences taken seq_group at a time,
+                         // row block first within each group (see unit_coords)
     int split_units;
     int split_parts;
     float *ws_o;

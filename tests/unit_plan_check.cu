@@ -68,8 +68,9 @@ static int brute_n_kv(const attn::PrefillParams &p, int s_lo, int s_hi) {
     return t < n_full ? t : n_full;
 }
 
-static void check_units(int B, int Hq, int Hkv, int Sq, int Sk, bool causal, int kv_major) {
-    const attn::PrefillParams p = params(B, Hq, Hkv, Sq, Sk, causal, kv_major);
+static void check_units(int B, int Hq, int Hkv, int Sq, int Sk, bool causal, int kv_major, int seq_group = 0) {
+    attn::PrefillParams p = params(B, Hq, Hkv, Sq, Sk, causal, kv_major);
+    p.seq_group = seq_group;
     const int units = attn::prefill_num_units(p);
     std::set<std::tuple<int, int, int>> seen;  // (b, head, row block)
     for (int u = 0; u < units; ++u) {
@@ -163,6 +164,11 @@ int main() {
             check_units(2, 8, 2, 520, 130, causal, kv_major);     // Sk < Sq: rows that see no key
             check_units(5, 2, 1, 1, 1, causal, kv_major);         // single rows and keys
             check_units(2, 4, 4, 129, 129, causal, kv_major);
+            if (kv_major == 0)
+                for (int sg : {1, 2, 3, 5}) {  // sequences in groups, the last group shorter
+                    check_units(7, 32, 8, 1000, 1000, causal, 0, sg);
+                    check_units(5, 3, 1, 700, 900, causal, 0, sg);
+                }
             check_packed_units(4, 32, 8, 4096, 4096, causal, kv_major);  // G = 4: 32 positions a tile
             check_packed_units(1, 32, 1, 1000, 1000, causal, kv_major);  // MQA: 4 positions a tile
             check_packed_units(3, 16, 8, 97, 300, causal, kv_major);     // G = 2, ragged, Sk > Sq
