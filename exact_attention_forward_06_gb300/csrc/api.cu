@@ -125,25 +125,8 @@ bool make_map_4d(CUtensorMap *m, const void *ptr, bool bhsd, int B, int S, int H
     return r == CUDA_SUCCESS;
 }
 
-// 3-D map over a page pool [P][16][Hkv][d]: dims {d, Hkv, 16P}, box = one
-// page of one KV head (16 rows x 128 elements, 4 KiB, no swizzle).
-bool make_map_pool(CUtensorMap *m, const void *ptr, int num_pages, int Hkv, int d) {
-    const cuuint64_t e = 2;
-    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)Hkv, (cuuint64_t)num_pages * 16};
-    cuuint64_t strides[2] = {(cuuint64_t)d * e, (cuuint64_t)Hkv * d * e};
-    cuuint32_t box[3] = {(cuuint32_t)d, 1, 16};
-    const cuuint32_t es[3] = {1, 1, 1};
-    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box, es,
-                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS;
-}
-
-// 3-D map over a page pool [P][16][Hkv][d] for the tensor-core prefill:
-// dims {d, Hkv, 16P}, box = 64 head-dim elements (128 B, 128-byte swizzle) x
-// `rows` pool rows of one KV head (16: one page; 128: a run of 8 pages).
-// Page-pool map for the prefill: one box holds whole 16-row pages of one KV
-// head, both 64-column halves, ordered in shared memory as
+// Page-pool map (paged prefill and decode): one box holds whole 16-row pages
+// of one KV head, both 64-column halves, ordered in shared memory as
 // [8-row group][half][8 rows][64 columns] (1 KiB per 8-row half, 128-byte
 // swizzle), so a 128-row tile is 8 boxes of 4 KiB (or one box of 16 row
 // groups for 8 consecutive pages).  Dims, innermost first: 64 columns, 8 rows
@@ -495,7 +478,10 @@ static attn_status_t decode_impl(const void *q, const void *k_new, const void *v
     DeviceInfo *di = nullptr;
     if ((st = device_info(&di)) != ATTN_OK) return st;
     CUtensorMap mk, mv;
-    if (!make_map_pool(&mk, k_pages, num_pages, Hkv, d) || !make_map_pool(&mv, v_pages, num_pages, Hkv, d))
+    // One box per page and tensor: two 8-row groups, the layout the decode's
+    // ldmatrix reads expect.
+    if (!make_map_pool_groups(&mk, k_pages, num_pages, Hkv, d, 2) ||
+        !make_map_pool_groups(&mv, v_pages, num_pages, Hkv, d, 2))
         return ATTN_ERR_CUDA;
     attn::DecodeParams p;
     p.q = q;

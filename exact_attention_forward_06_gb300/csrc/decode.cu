@@ -4,29 +4,43 @@
 // 推理优化": 16-token pages, an int32 block_table per sequence); the split over
 // the keys with a merge of the partial results is the Flash-Decoding style
 // tail split of the MoonMath HIP kernel page.  Decode reads every K/V byte
-// once and does ~4 flops per byte, so it is bound by HBM bandwidth and runs on
-// the CUDA cores; the tensor cores would only add a reshape.
+// once and does ~4 flops per byte, so it is bound by HBM bandwidth.
 //
 // Split kernel: one CTA per (group of up to 4 query heads sharing a KV head,
 // split, sequence); when a KV group has more heads, its head groups are
 // adjacent in the grid so that their reads of the same pages meet in L2.  The
-// CTAs are small (one producer warp and four consumer warps, about 128
-// registers a thread) so three of them share an SM.  The producer lane gathers
-// the split's pages with one 3-D TMA copy per page and tensor (the 16 rows of
-// one KV head in a page are 2 KiB apart in the pool) into an 8-page
-// shared-memory ring.  A consumer warp handles at most 2 heads; with 4 heads
-// two warps read each staged page (one per head pair), so the four warps form
-// two page streams that take pages alternately (four streams of one warp with
-// 1 or 2 heads).  In a warp, lane (tg, ds) =
-// (lane/8, lane%8) owns head-dim elements [8 ds, 8 ds + 8) and
-// [64 + 8 ds, 64 + 8 ds + 8) of tokens tg, tg+4, tg+8, tg+12 of the page (two
-// 16-byte chunks, so the eight lanes of a token read one 256-byte row without
-// bank conflicts).  Dot products are reduced over the 8 lanes of a token with
-// three shuffles, the page max over the token groups with two more, and each
-// warp keeps its own running max / sum / accumulator (online softmax, with the
-// max moved only past a 2^8 growth).  At the end the page streams are merged in
-// shared memory and the split writes its normalised partial output and
-// log-sum-exp.  The merge kernel then combines the splits in a fixed order.
+// CTAs are small (one producer warp and four consumer warps) so three of them
+// share an SM.  The producer lane gathers the split's pages with one TMA box
+// per page and tensor into an 8-page shared-memory ring.  A box is the page's
+// 16 rows of one KV head in two 8-row groups, each as two 64-column halves of
+// 128-byte rows with the 128-byte swizzle (the layout of the paged prefill's
+// tiles), so that 8 consecutive rows at one column chunk sit in 8 distinct
+// bank groups.
+//
+// Consumer warp w takes pages w, w + 4, ...: four page streams.  A page is two
+// warp-level tensor-core products (mma.sync m16n8k16, bf16 in, fp32 out), the
+// 16 tokens of the page as M:
+//   S^T = K Q^T   (16 tokens x 8 head columns, k = the 128 head-dim elements;
+//                  K straight from shared memory with ldmatrix, Q^T held in
+//                  registers, columns past the CTA's heads zero),
+//   O^T += V^T P^T (8 m-tiles of 16 head-dim elements x 8 head columns,
+//                  k = the 16 tokens; V^T by transposing ldmatrix).
+// A lane's fragment columns are the same two heads in both products, so the
+// online softmax (running max, rescale, row sum) needs no data movement
+// beyond the max over the page's tokens; P goes from the S^T fragment to the
+// B operand of the second product with one 8x8 transpose (movmatrix) per
+// 8 tokens.  Measured on 32 sequences of 1024 to 8192 tokens (Hq=32,
+// Hkv=8), the same loop with the page math left out runs at 0.91 of the copy
+// bandwidth, and the earlier CUDA-core form (bf16 -> fp32 unpacking and
+// packed FMAs) at 0.78: the unpacking, not the memory system, held decode
+// below the roofline.
+//
+// P is rounded to bf16 for the second product (as in the prefill).  The
+// running max is raised whenever a page's max exceeds it, so the largest key
+// of a row has P = 1 exactly and a dominant key keeps its weight.  At the end
+// the page streams are merged in shared memory and the split writes its
+// normalised partial output and log-sum-exp; the merge kernel then combines
+// the splits in a fixed order.
 #include <cstdint>
 #include <type_traits>
 #include <cuda_bf16.h>
@@ -40,55 +54,39 @@ namespace dec {
 
 constexpr int PAGE = 16;
 constexpr int D = 128;
-constexpr int NCW = 4;   // consumer warps
+constexpr int NCW = 4;   // consumer warps = page streams
 constexpr int NST = 8;   // pages in flight per CTA
-constexpr int GH_MAX = 2;
+constexpr int GH_MAX = 4;
 constexpr int NTHREADS = (NCW + 1) * 32;
 constexpr uint32_t PAGE_BYTES = PAGE * D * 2;        // one tensor, one KV head: 4 KiB
 constexpr uint32_t STAGE_BYTES = 2 * PAGE_BYTES;     // K + V
 constexpr uint32_t SMEM_STAGES = NST * STAGE_BYTES;  // 64 KiB
+// Page box layout: row r, 16-byte chunk c (of 16) at
+// (r / 8) * GROUP_BYTES + (c / 8) * HALF_BYTES + (r % 8) * 128 + ((c % 8) ^ (r % 8)) * 16.
+constexpr uint32_t GROUP_BYTES = 2048;
+constexpr uint32_t HALF_BYTES = 1024;
 constexpr uint32_t SMEM_MERGE = NCW * GH_MAX * (D + 2) * 4;
 constexpr uint32_t SMEM_MISC = 1536;
-constexpr uint32_t SMEM_ALIGN = 1024;
+constexpr uint32_t SMEM_ALIGN = 1024;  // the 128-byte swizzle repeats every 1 KiB
 constexpr uint32_t SMEM_BYTES = SMEM_ALIGN + SMEM_STAGES + SMEM_MERGE + SMEM_MISC;
 constexpr int MAX_PAGES_PER_SPLIT = 256;
 constexpr int TARGET_SPLIT_CTAS = 2048;  // split CTAs the plan aims for (assuming four heads per CTA)
 // barriers, per-stage flags, the abort flag and the split's page ids
 static_assert(2 * NST * 8 + (NST + 4 + MAX_PAGES_PER_SPLIT) * 4 <= SMEM_MISC, "misc shared area too small");
-constexpr float RESCALE_LOG2 = 8.0f;
+static_assert(3 * (SMEM_BYTES + 1024) <= 233472, "three CTAs must share an SM");
 constexpr float LN2 = 0.6931471805599453f;
 constexpr float LOG2E = 1.4426950408889634f;
 
-// Eight bf16 values (one 16-byte chunk) as four fp32 pairs, in element order.
-__device__ __forceinline__ void bf16x8_to_float2(const uint4 &u, float2 *x) {
-    x[0] = make_float2(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u));
-    x[1] = make_float2(__uint_as_float(u.y << 16), __uint_as_float(u.y & 0xffff0000u));
-    x[2] = make_float2(__uint_as_float(u.z << 16), __uint_as_float(u.z & 0xffff0000u));
-    x[3] = make_float2(__uint_as_float(u.w << 16), __uint_as_float(u.w & 0xffff0000u));
-}
+__device__ __forceinline__ float bf16_lo(uint32_t u) { return __uint_as_float(u << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t u) { return __uint_as_float(u & 0xffff0000u); }
 
-__device__ __forceinline__ void bf16x8_to_float(const uint4 &u, float *x) {
-    x[0] = __uint_as_float(u.x << 16);
-    x[1] = __uint_as_float(u.x & 0xffff0000u);
-    x[2] = __uint_as_float(u.y << 16);
-    x[3] = __uint_as_float(u.y & 0xffff0000u);
-    x[4] = __uint_as_float(u.z << 16);
-    x[5] = __uint_as_float(u.z & 0xffff0000u);
-    x[6] = __uint_as_float(u.w << 16);
-    x[7] = __uint_as_float(u.w & 0xffff0000u);
-}
-
-// GH query heads per CTA (1, 2 or 4, all of one KV head).  Each consumer warp
-// handles HG <= 2 of them, so the NHG = GH / HG warps of a "page stream" read
-// every staged page together and the page is fetched once for all GH heads.
+// GH query heads per CTA (1, 2 or 4, all of one KV head): head columns
+// 0 .. GH-1 of the 8-wide MMA tiles.
 template <int GH>
 __global__ void __launch_bounds__(NTHREADS, 3)
     split_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
                  const DecodeParams p) {
-    constexpr int HG = GH >= 2 ? 2 : 1;    // heads per consumer warp
-    constexpr int NHG = GH / HG;           // warps reading each page
-    constexpr int STREAMS = NCW / NHG;     // pages consumed in parallel
-    static_assert(STREAMS * GH <= NCW * GH_MAX, "merge scratch too small");
+    static_assert(GH >= 1 && GH <= GH_MAX, "heads per CTA");
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = ptx::smem_addr(smem_raw);
     uint8_t *base = smem_raw + ((SMEM_ALIGN - (raw & (SMEM_ALIGN - 1))) & (SMEM_ALIGN - 1));
@@ -130,7 +128,7 @@ __global__ void __launch_bounds__(NTHREADS, 3)
     if (threadIdx.x == 0) {
         for (int s = 0; s < NST; ++s) {
             ptx::mbar_init(full + s, 1);
-            ptx::mbar_init(empty + s, NHG);
+            ptx::mbar_init(empty + s, 1);
             stage_bad[s] = 0;
         }
         *abort_flag = 0;
@@ -185,9 +183,10 @@ __global__ void __launch_bounds__(NTHREADS, 3)
                     ptx::mbar_arrive(full + slot);
                 } else {
                     stage_bad[slot] = 0;
+                    // one box per tensor: 8-row groups 2 phys and 2 phys + 1 of KV head g
                     ptx::mbar_arrive_expect_tx(full + slot, STAGE_BYTES);
-                    ptx::tma_load_3d_hint(dst, &map_k, full + slot, 0, g, phys * PAGE, pol);
-                    ptx::tma_load_3d_hint(dst + PAGE_BYTES, &map_v, full + slot, 0, g, phys * PAGE, pol);
+                    ptx::tma_load_5d_hint(dst, &map_k, full + slot, 0, 0, 0, phys * 2, g, pol);
+                    ptx::tma_load_5d_hint(dst + PAGE_BYTES, &map_v, full + slot, 0, 0, 0, phys * 2, g, pol);
                 }
                 ++issued;
             }
@@ -195,181 +194,202 @@ __global__ void __launch_bounds__(NTHREADS, 3)
         }
         __syncwarp();
     } else {
-        // ---------------- consumers
-        const int tg = lane >> 3;  // token group
-        const int ds = lane & 7;   // head-dim chunks ds and 8 + ds
-        const int hg = warp % NHG;       // this warp's heads: hg * HG .. hg * HG + HG - 1
-        const int stream = warp / NHG;   // this warp's pages: stream, stream + STREAMS, ...
-        const int64_t wrow0 = row0 + hg * HG;
-        // Dot products and the P V accumulation run on fp32 pairs (packed
-        // FFMA2): element pairs (2i, 2i+1) of the lane's 16 head-dim elements.
-        float2 qf[HG][8];
+        // ---------------- consumers: warp w takes pages w, w + NCW, ...
+        // Fragment coordinates: r4 is the row group (a token of S^T, a
+        // head-dim row of O^T), c4 the column pair (heads 2 c4 and 2 c4 + 1).
+        const int r4 = lane >> 2;
+        const int c4 = lane & 3;
+        // ldmatrix row addresses: lanes 8 i .. 8 i + 7 give the 8 rows of
+        // matrix i.  K (S^T's A operand, 16 tokens x 16 head-dim elements per
+        // k step): matrix i is tokens 8 (i & 1) .., chunk 2 ks + (i >> 1).
+        // V (O^T's A operand through the transpose, 16 head-dim elements x 16
+        // tokens per m-tile): matrix i is tokens 8 (i >> 1) .., chunk
+        // 2 mt + (i & 1).  Row rr = lane % 8 of a matrix is token rr of its
+        // 8-row group, so its swizzle phase is rr.
+        const int mat = lane >> 3, rr = lane & 7;
+        const uint32_t k_row = (uint32_t)(mat & 1) * GROUP_BYTES + rr * 128;
+        const uint32_t k_x = (uint32_t)((mat >> 1) ^ rr);
+        const uint32_t v_row = (uint32_t)(mat >> 1) * GROUP_BYTES + rr * 128;
+        const uint32_t v_x = (uint32_t)((mat & 1) ^ rr);
+        // Q^T as the B operand: head r4 (zero past the CTA's heads), head-dim
+        // elements 16 ks + 2 c4 (+1) and 16 ks + 8 + 2 c4 (+1).
+        uint32_t qb[8][2];
+        {
+            const uint32_t *qrow = reinterpret_cast<const uint32_t *>(p.q) + (row0 + r4) * (D / 2);
 #pragma unroll
-        for (int h = 0; h < HG; ++h) {
-            const uint4 *qp = reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(p.q) +
-                                                              (wrow0 + h) * D);
-            bf16x8_to_float2(qp[ds], qf[h]);
-            bf16x8_to_float2(qp[8 + ds], qf[h] + 4);
-            const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) qf[h][e] = __fmul2_rn(qf[h][e], sc2);
+            for (int ks = 0; ks < 8; ++ks) {
+                qb[ks][0] = r4 < GH ? qrow[ks * 8 + c4] : 0u;
+                qb[ks][1] = r4 < GH ? qrow[ks * 8 + 4 + c4] : 0u;
+            }
         }
-        float m[HG], lsum[HG], msub[HG];  // msub: m, or 0 while m is -inf
-        float2 acc[HG][8];
+        const float sl2 = p.scale_log2;
+        // Running max (log2 units) and partial row sum of heads 2 c4, 2 c4 + 1,
+        // and O^T: acc[mt] = rows 16 mt + r4 and 16 mt + r4 + 8, those heads.
+        float m[2] = {-INFINITY, -INFINITY};
+        float lsum[2] = {0.f, 0.f};
+        float acc[8][4];
 #pragma unroll
-        for (int h = 0; h < HG; ++h) {
-            m[h] = -INFINITY;
-            msub[h] = 0.f;
-            lsum[h] = 0.f;
+        for (int mt = 0; mt < 8; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.f;
+
+        // Raise the running max of the lane's heads to mn0 / mn1 when any lane
+        // of the warp needs it (so the branch is uniform), rescaling the sums.
+        auto raise_max = [&](float mn0, float mn1) {
+            if (__any_sync(0xffffffffu, mn0 > m[0] || mn1 > m[1])) {
+                const float a0 = mn0 == -INFINITY ? 1.f : ptx::ex2(m[0] - mn0);  // m = -inf: 0
+                const float a1 = mn1 == -INFINITY ? 1.f : ptx::ex2(m[1] - mn1);
+                lsum[0] *= a0;
+                lsum[1] *= a1;
 #pragma unroll
-            for (int e = 0; e < 8; ++e) acc[h][e] = make_float2(0.f, 0.f);
-        }
-        for (int i = stream; i < np; i += STREAMS) {
+                for (int mt = 0; mt < 8; ++mt) {
+                    acc[mt][0] *= a0;
+                    acc[mt][1] *= a1;
+                    acc[mt][2] *= a0;
+                    acc[mt][3] *= a1;
+                }
+                m[0] = mn0;
+                m[1] = mn1;
+            }
+        };
+
+        for (int i = warp; i < np; i += NCW) {
             const int slot = i % NST;
             if (!wait_bounded(full + slot, (i / NST) & 1, wc, kSiteDecodeFull)) break;
-            const uint8_t *ks = base + slot * STAGE_BYTES;
-            const uint8_t *vs = ks + PAGE_BYTES;
-            const bool bad = stage_bad[slot] != 0;
-            const int tok0 = (page0 + i) * PAGE;
-            // A page whose 16 slots all hold keys of the sequence needs no
-            // masking: it takes a copy of the page step without the selects.
-            auto page_step = [&](auto full_tag) {
-                constexpr bool FULL = decltype(full_tag)::value;
-                float sc[4][HG];
+            // A page whose block-table entry could not be read holds nothing of
+            // the sequence: it is skipped.
+            if (stage_bad[slot] == 0) {
+                const uint32_t ks_addr = ptx::smem_addr(base + slot * STAGE_BYTES);
+                const uint32_t vs_addr = ks_addr + PAGE_BYTES;
+                const int nvalid = L - (page0 + i) * PAGE;  // tokens of the sequence in this page (>= 1)
+                // A page whose 16 slots all hold keys of the sequence needs no
+                // masking: it takes a copy of the page step without the selects.
+                auto page_step = [&](auto full_tag) {
+                    constexpr bool FULL = decltype(full_tag)::value;
+                    float s[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                for (int ps = 0; ps < 4; ++ps) {
-                    const int t = ps * 4 + tg;
-                    const uint4 *kp = reinterpret_cast<const uint4 *>(ks + t * (D * 2));
-                    float2 kf[8];
-                    bf16x8_to_float2(kp[ds], kf);
-                    bf16x8_to_float2(kp[8 + ds], kf + 4);
-#pragma unroll
-                    for (int h = 0; h < HG; ++h) {
-                        float2 d2 = __fmul2_rn(qf[h][0], kf[0]);
-#pragma unroll
-                        for (int e = 1; e < 8; ++e) d2 = __ffma2_rn(qf[h][e], kf[e], d2);
-                        float dot = d2.x + d2.y;
-                        dot += __shfl_xor_sync(0xffffffffu, dot, 1);
-                        dot += __shfl_xor_sync(0xffffffffu, dot, 2);
-                        dot += __shfl_xor_sync(0xffffffffu, dot, 4);
-                        sc[ps][h] = (FULL || (!bad && tok0 + t < L)) ? dot : -INFINITY;
+                    for (int ks = 0; ks < 8; ++ks) {
+                        uint32_t a[4];
+                        ptx::ldsm_x4(ks_addr + k_row + (ks >> 2) * HALF_BYTES + (((2u * (ks & 3)) ^ k_x) << 4), a);
+                        ptx::mma_bf16_16816(s, a, qb[ks][0], qb[ks][1]);
                     }
-                }
-                float pr[4][HG];
+                    // s[0], s[1]: token r4, heads 2 c4, 2 c4 + 1; s[2], s[3]: token r4 + 8.
 #pragma unroll
-                for (int h = 0; h < HG; ++h) {
-                    float pm = ptx::max3(sc[0][h], sc[1][h], fmaxf(sc[2][h], sc[3][h]));
-                    pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 8));
-                    pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 16));
-                    if (pm > m[h] + RESCALE_LOG2) {  // warp-uniform
-                        const float alpha = ptx::ex2(m[h] - pm);
-                        lsum[h] *= alpha;
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) acc[h][e] = __fmul2_rn(acc[h][e], make_float2(alpha, alpha));
-                        m[h] = pm;
-                        msub[h] = pm;
+                    for (int j = 0; j < 4; ++j) s[j] *= sl2;
+                    if (!FULL) {
+                        // Slots past the sequence end hold arbitrary bits: select, not add.
+                        if (r4 >= nvalid) s[0] = s[1] = -INFINITY;
+                        if (r4 + 8 >= nvalid) s[2] = s[3] = -INFINITY;
                     }
+                    float pm0 = fmaxf(s[0], s[2]), pm1 = fmaxf(s[1], s[3]);
 #pragma unroll
-                    for (int ps = 0; ps < 4; ++ps) {
-                        // a masked score (-inf) gives ex2(-inf) = 0 with no select
-                        pr[ps][h] = ptx::ex2(sc[ps][h] - msub[h]);
-                        lsum[h] += pr[ps][h];
+                    for (int off = 4; off < 32; off <<= 1) {
+                        pm0 = fmaxf(pm0, __shfl_xor_sync(0xffffffffu, pm0, off));
+                        pm1 = fmaxf(pm1, __shfl_xor_sync(0xffffffffu, pm1, off));
                     }
-                }
-                // Slots past the sequence end (and pages that could not be
-                // read) hold arbitrary bits: their P is 0, but 0 * NaN is NaN,
-                // so on such a page the V of invalid tokens is replaced by 0.
-#pragma unroll
-                for (int ps = 0; ps < 4; ++ps) {
-                    const int t = ps * 4 + tg;
-                    const uint4 *vp = reinterpret_cast<const uint4 *>(vs + t * (D * 2));
-                    float2 vf[8];
-                    bf16x8_to_float2(vp[ds], vf);
-                    bf16x8_to_float2(vp[8 + ds], vf + 4);
-                    if (!FULL && (bad || tok0 + t >= L)) {
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) vf[e] = make_float2(0.f, 0.f);
+                    raise_max(fmaxf(m[0], pm0), fmaxf(m[1], pm1));
+                    const float ms0 = m[0] == -INFINITY ? 0.f : m[0];
+                    const float ms1 = m[1] == -INFINITY ? 0.f : m[1];
+                    // P rounded to bf16 for the product only; the row sum (and
+                    // with it the log-sum-exp) adds the fp32 values.
+                    const float p0 = ptx::ex2(s[0] - ms0), p1 = ptx::ex2(s[1] - ms1);
+                    const float p2 = ptx::ex2(s[2] - ms0), p3 = ptx::ex2(s[3] - ms1);
+                    lsum[0] += p0 + p2;
+                    lsum[1] += p1 + p3;
+                    const uint32_t p_lo = ptx::pack_bf16x2(p0, p1);
+                    const uint32_t p_hi = ptx::pack_bf16x2(p2, p3);
+                    // P^T as the B operand: tokens 2 c4 (+1) and 8 + 2 c4 (+1), head r4.
+                    const uint32_t pb0 = ptx::movmatrix_trans(p_lo);
+                    const uint32_t pb1 = ptx::movmatrix_trans(p_hi);
+                    // The V^T fragment holds tokens 2 c4, 2 c4 + 1 (a[0], a[1]) and
+                    // those + 8 (a[2], a[3]); past the end P is 0 but 0 * NaN is
+                    // NaN, so there V is zeroed.
+                    uint32_t keep_lo = 0xffffffffu, keep_hi = 0xffffffffu;
+                    if (!FULL) {
+                        keep_lo = (2 * c4 < nvalid ? 0x0000ffffu : 0u) | (2 * c4 + 1 < nvalid ? 0xffff0000u : 0u);
+                        keep_hi = (2 * c4 + 8 < nvalid ? 0x0000ffffu : 0u) | (2 * c4 + 9 < nvalid ? 0xffff0000u : 0u);
                     }
 #pragma unroll
-                    for (int h = 0; h < HG; ++h) {
-                        const float2 p2 = make_float2(pr[ps][h], pr[ps][h]);
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) acc[h][e] = __ffma2_rn(p2, vf[e], acc[h][e]);
+                    for (int mt = 0; mt < 8; ++mt) {
+                        uint32_t a[4];
+                        ptx::ldsm_x4_trans(vs_addr + v_row + (mt >> 2) * HALF_BYTES + (((2u * (mt & 3)) ^ v_x) << 4),
+                                           a);
+                        if (!FULL) {
+                            a[0] &= keep_lo;
+                            a[1] &= keep_lo;
+                            a[2] &= keep_hi;
+                            a[3] &= keep_hi;
+                        }
+                        ptx::mma_bf16_16816(acc[mt], a, pb0, pb1);
                     }
-                }
-            };
-            if (!bad && tok0 + PAGE <= L)
-                page_step(std::true_type{});
-            else
-                page_step(std::false_type{});
+                };
+                if (nvalid >= PAGE)
+                    page_step(std::true_type{});
+                else
+                    page_step(std::false_type{});
+            }
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(empty + slot);
         }
-        if (new_token && stream == 0) {
+        if (new_token && warp == 0) {
             // The appended token, read from k_new / v_new rather than the
-            // cache: every token group computes the same score and only
-            // group 0 adds the token to its sums.
+            // cache.  Lane l forms the partial dot products of head-dim
+            // elements 4 l .. 4 l + 3 for every head, reduced over the warp;
+            // the token is added to the sums once (by the lanes of row group 0).
             const int64_t src = ((int64_t)b * p.Hkv + g) * D;
-            const uint4 *kn = reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(p.k_new) + src);
-            const uint4 *vn = reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(p.v_new) + src);
-            float2 kf[8], vf[8];
-            bf16x8_to_float2(kn[ds], kf);
-            bf16x8_to_float2(kn[8 + ds], kf + 4);
-            bf16x8_to_float2(vn[ds], vf);
-            bf16x8_to_float2(vn[8 + ds], vf + 4);
+            const __nv_bfloat16 *kn = static_cast<const __nv_bfloat16 *>(p.k_new) + src;
+            const __nv_bfloat16 *vn = static_cast<const __nv_bfloat16 *>(p.v_new) + src;
+            const uint2 ku = reinterpret_cast<const uint2 *>(kn)[lane];
+            float sh0 = 0.f, sh1 = 0.f;  // scores of heads 2 c4, 2 c4 + 1 (0 past the CTA's heads)
 #pragma unroll
-            for (int h = 0; h < HG; ++h) {
-                float2 d2 = __fmul2_rn(qf[h][0], kf[0]);
+            for (int h = 0; h < GH; ++h) {
+                const uint2 qu = reinterpret_cast<const uint2 *>(static_cast<const __nv_bfloat16 *>(p.q) +
+                                                                 (row0 + h) * D)[lane];
+                float dot = bf16_lo(qu.x) * bf16_lo(ku.x);
+                dot = fmaf(bf16_hi(qu.x), bf16_hi(ku.x), dot);
+                dot = fmaf(bf16_lo(qu.y), bf16_lo(ku.y), dot);
+                dot = fmaf(bf16_hi(qu.y), bf16_hi(ku.y), dot);
 #pragma unroll
-                for (int e = 1; e < 8; ++e) d2 = __ffma2_rn(qf[h][e], kf[e], d2);
-                float sc = d2.x + d2.y;
-                sc += __shfl_xor_sync(0xffffffffu, sc, 1);
-                sc += __shfl_xor_sync(0xffffffffu, sc, 2);
-                sc += __shfl_xor_sync(0xffffffffu, sc, 4);
-                if (sc > m[h] + RESCALE_LOG2) {  // warp-uniform
-                    const float alpha = ptx::ex2(m[h] - sc);
-                    lsum[h] *= alpha;
+                for (int off = 1; off < 32; off <<= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
+                if (h == 2 * c4) sh0 = dot * sl2;
+                if (h == 2 * c4 + 1) sh1 = dot * sl2;
+            }
+            raise_max(fmaxf(m[0], sh0), fmaxf(m[1], sh1));
+            const float e0 = ptx::ex2(sh0 - m[0]);
+            const float e1 = ptx::ex2(sh1 - m[1]);
+            if (r4 == 0) {
+                lsum[0] += e0;
+                lsum[1] += e1;
+            }
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) acc[h][e] = __fmul2_rn(acc[h][e], make_float2(alpha, alpha));
-                    m[h] = sc;
-                }
-                const float pr = tg == 0 ? ptx::ex2(sc - m[h]) : 0.f;
-                lsum[h] += pr;
-                const float2 p2 = make_float2(pr, pr);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) acc[h][e] = __ffma2_rn(p2, vf[e], acc[h][e]);
+            for (int mt = 0; mt < 8; ++mt) {
+                const float va = __bfloat162float(vn[16 * mt + r4]);
+                const float vb = __bfloat162float(vn[16 * mt + r4 + 8]);
+                acc[mt][0] = fmaf(e0, va, acc[mt][0]);
+                acc[mt][1] = fmaf(e1, va, acc[mt][1]);
+                acc[mt][2] = fmaf(e0, vb, acc[mt][2]);
+                acc[mt][3] = fmaf(e1, vb, acc[mt][3]);
             }
         }
-        // Sum the four token groups (lanes 8 and 16 apart share a slice).
+        // Row sums over the 16 token rows of the fragments (row groups r4).
 #pragma unroll
-        for (int h = 0; h < HG; ++h) {
-            lsum[h] += __shfl_xor_sync(0xffffffffu, lsum[h], 8);
-            lsum[h] += __shfl_xor_sync(0xffffffffu, lsum[h], 16);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                acc[h][e].x += __shfl_xor_sync(0xffffffffu, acc[h][e].x, 8);
-                acc[h][e].y += __shfl_xor_sync(0xffffffffu, acc[h][e].y, 8);
-                acc[h][e].x += __shfl_xor_sync(0xffffffffu, acc[h][e].x, 16);
-                acc[h][e].y += __shfl_xor_sync(0xffffffffu, acc[h][e].y, 16);
-            }
+        for (int off = 4; off < 32; off <<= 1) {
+            lsum[0] += __shfl_xor_sync(0xffffffffu, lsum[0], off);
+            lsum[1] += __shfl_xor_sync(0xffffffffu, lsum[1], off);
         }
-        // merge scratch row of (page stream, head): stream * GH + head
-        float *mw = merge + (stream * GH + hg * HG) * (D + 2);
+        // merge scratch row of (page stream, head): warp * GH + head
 #pragma unroll
-        for (int h = 0; h < HG; ++h) {
-            float *row = mw + h * (D + 2);
-            if (tg == 0) {
+        for (int j = 0; j < 2; ++j) {
+            const int h = 2 * c4 + j;
+            if (h < GH) {
+                float *row = merge + (warp * GH + h) * (D + 2);
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    row[ds * 8 + 2 * e] = acc[h][e].x;
-                    row[ds * 8 + 2 * e + 1] = acc[h][e].y;
-                    row[64 + ds * 8 + 2 * e] = acc[h][4 + e].x;
-                    row[64 + ds * 8 + 2 * e + 1] = acc[h][4 + e].y;
+                for (int mt = 0; mt < 8; ++mt) {
+                    row[16 * mt + r4] = acc[mt][j];
+                    row[16 * mt + r4 + 8] = acc[mt][2 + j];
                 }
-            }
-            if (lane == 0) {
-                row[D] = m[h];
-                row[D + 1] = lsum[h];
+                if (r4 == 0) {
+                    row[D] = m[j];
+                    row[D + 1] = lsum[j];
+                }
             }
         }
     }
@@ -384,11 +404,11 @@ __global__ void __launch_bounds__(NTHREADS, 3)
         for (int h = 0; h < GH; ++h) {
             float M = -INFINITY;
 #pragma unroll
-            for (int w = 0; w < STREAMS; ++w) M = fmaxf(M, merge[(w * GH + h) * (D + 2) + D]);
+            for (int w = 0; w < NCW; ++w) M = fmaxf(M, merge[(w * GH + h) * (D + 2) + D]);
             float Ls = 0.f, o = 0.f;
             if (M != -INFINITY) {
 #pragma unroll
-                for (int w = 0; w < STREAMS; ++w) {
+                for (int w = 0; w < NCW; ++w) {
                     const float *row = merge + (w * GH + h) * (D + 2);
                     const float f = ptx::ex2(row[D] - M);  // -inf -> 0
                     Ls += row[D + 1] * f;

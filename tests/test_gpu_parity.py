@@ -287,6 +287,31 @@ def test_paged_decode_ignores_garbage_past_sequence_end(A):
     check_lse(lse, ref_l, "garbage past the end")
 
 
+def test_paged_decode_dominant_keys(A):
+    # Two keys per sequence score far above the rest for the first head of
+    # each KV group (about 34 and 33.7 in natural-log units) and carry opposite
+    # values u and -u: that head's output is u times the difference of their
+    # two weights, so a lost or misrounded weight on the largest key moves it
+    # by about |u| times the error.  The other heads of the group see those
+    # keys at scores of a few units.
+    w = inputs.DecodeWorkload("dominant", B=4, Hq=8, Hkv=2, max_blocks=256, seed=23)
+    q, kp, vp, table, lens = inputs.make_decode(w, seqlens=[4000, 1, 17, 4096])
+    gen = torch.Generator().manual_seed(5)
+    G = w.Hq // w.Hkv
+    u = (2.0 * torch.randn(w.Hkv, w.d, generator=gen)).to(vp.dtype)
+    for b, L in enumerate(lens.tolist()):
+        for j, t in enumerate(torch.randperm(L, generator=gen)[:2].tolist()):
+            page, slot = int(table[b, t // 16]), t % 16
+            for kvh in range(w.Hkv):
+                kp[page, slot, kvh] = (3.0 * (1.0 - 0.01 * j) * q[b, kvh * G].float()).to(kp.dtype)
+                vp[page, slot, kvh] = u[kvh] if j == 0 else -u[kvh]
+    out, lse = A.decode_paged(q.cuda(), kp.cuda(), vp.cuda(), table.cuda(), lens.cuda(), scale=w.scale)
+    torch.cuda.synchronize()
+    ref_o, ref_l = oracle.decode_paged(q, kp, vp, table, lens, scale=w.scale)
+    check_out(out, ref_o, "dominant keys")
+    check_lse(lse, ref_l, "dominant keys")
+
+
 def test_paged_decode_deterministic(A):
     w = inputs.PAGED_DECODE
     q, kp, vp, table, lens = (t.cuda() for t in inputs.make_decode(w))
