@@ -56,6 +56,12 @@ constexpr int PAGE = 16;
 constexpr int D = 128;
 constexpr int NCW = 4;   // consumer warps = page streams
 constexpr int NST = 8;   // pages in flight per CTA
+// Page i goes to slot i % NST and to consumer warp i % NCW.  With NST a
+// multiple of NCW every slot has one consumer warp, which waits on the slot's
+// phases in order; otherwise a warp could wait on parity r of a slot whose
+// phase r - 1 is still open, and a parity wait on the phase two back returns
+// at once.
+static_assert(NST % NCW == 0, "each ring slot must have a single consumer warp");
 constexpr int GH_MAX = 4;
 constexpr int NTHREADS = (NCW + 1) * 32;
 constexpr uint32_t PAGE_BYTES = PAGE * D * 2;        // one tensor, one KV head: 4 KiB
