@@ -191,6 +191,7 @@ class DenseCase:
         self.config = {"B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "Sq": w.Sq, "Sk": w.Sk, "d": w.d, "layout": w.layout,
                        "causal": w.causal}
         self.flop_note = "4*B*Hq*Sq*Sk*d" + ("/2" if w.causal else "")
+        self.bytes = byte_floor(w.B * w.Sq, w.Hq, w.B * w.Sk, w.Hkv, w.d)
         self.api = "exact_attention_forward_06_gb300.fwd (C ABI attn_fwd)"
 
     def workspace_bytes(self, A):
@@ -222,6 +223,7 @@ class VarlenCase:
                        "lengths": f"U[{w.len_lo},{w.len_hi}] seed {w.seed}", "max_seqlen": max(self.lq), "d": w.d,
                        "layout": "thd (packed)", "causal": w.causal}
         self.flop_note = "sum over sequences of 4*Hq*Lq*Lk*d" + ("/2" if w.causal else "")
+        self.bytes = byte_floor(total_q, w.Hq, self.host[1].shape[0], w.Hkv, w.d)
         self.api = "exact_attention_forward_06_gb300.fwd_varlen (C ABI attn_fwd_varlen)"
 
     def workspace_bytes(self, A):
@@ -253,6 +255,7 @@ class PagedCase(VarlenCase):
                        "seed": w.seed, "cache_tokens": sum(self.lk), "page_size": w.page_size, "d": w.d,
                        "layout": "thd chunks, paged cache", "causal": w.causal}
         self.flop_note = "4*Hq*d per visible pair; causal pairs Lq*(Lk-Lq) + Lq^2/2 per sequence"
+        self.bytes = byte_floor(total_q, w.Hq, sum(self.lk), w.Hkv, w.d)
         self.api = "exact_attention_forward_06_gb300.fwd_paged (C ABI attn_fwd_paged)"
 
     def call(self, A, dev_in, out, lse, stream):
@@ -262,6 +265,12 @@ class PagedCase(VarlenCase):
 
     def oracle_sample(self, seconds, seed):
         return _oracle_sample_paged(self, seconds, seed)
+
+
+def byte_floor(total_q, Hq, total_k, Hkv, d):
+    """The fewest bytes a launch can move: Q read and O written once, K and V
+    read once, the fp32 log-sum-exp written once."""
+    return 2 * total_q * Hq * d * 2 + 2 * total_k * Hkv * d * 2 + total_q * Hq * 4
 
 
 def make_case(name):
@@ -444,13 +453,37 @@ L2_BYTES = 129 << 20         # GB300's L2
 L2_FLUSH_BYTES = 256 << 20   # about twice the L2
 
 
+def workload_roofline(case, ms, peaks, peak_src, traffic):
+    """The roofline a prefill workload sits under: the tensor peak when its
+    flops per byte of the byte floor exceed the ridge point (burst tensor peak
+    over copy bandwidth), else HBM, with the byte floor as the algorithmic
+    bytes (a short query against long keys streams K and V)."""
+    intensity = case.flops / case.bytes
+    ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    if intensity >= ridge:
+        tf = case.flops / (ms * 1e-3) / 1e12
+        return {"bound": "tensor", "achieved": round(tf, 2), "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": round(tf / peaks["bf16_tflops"], 4), "traffic": traffic,
+                "peak_source": f"{peak_src} bf16_tflops (burst: one launch at a time)",
+                "kernel": "attn::g1::prefill_kernel",
+                "algorithmic": f"{case.flops:.4g} flop per launch ({case.flop_note})",
+                "intensity_flop_per_byte": round(intensity, 1), "ridge_flop_per_byte": round(ridge, 1)}
+    gbs = case.bytes / (ms * 1e-3) / 1e9
+    return {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": round(gbs / peaks["hbm_gbs"], 4), "traffic": traffic,
+            "peak_source": f"{peak_src} hbm_gbs", "kernel": "attn::g1::prefill_kernel",
+            "algorithmic": f"{case.bytes} B per launch (Q and O once, K and V once, fp32 lse)",
+            "intensity_flop_per_byte": round(intensity, 1), "ridge_flop_per_byte": round(ridge, 1)}
+
+
 def run_workloads(A, args, dev, stream, peaks, peak_src, skip=None):
     """Each prefill workload on its own: CUDA events around every launch, at
     least `args.steps` launches and about half a second of them.  A workload
     whose inputs and outputs together exceed L2 runs back to back like the
     headline; a smaller one gets an L2 flush (a 256 MB write, outside the
-    timed events) before every launch.  Reports value, roofline fraction
-    against the burst peak, and the DRAM traffic of the workload's own ncu
+    timed events) before every launch.  Reports value, the roofline fraction
+    (against the burst tensor peak, or HBM for a workload whose intensity is
+    below the ridge point), and the DRAM traffic of the workload's own ncu
     capture."""
     flush = torch.empty(L2_FLUSH_BYTES, device=dev, dtype=torch.uint8)
     result = {}
@@ -501,12 +534,7 @@ def run_workloads(A, args, dev, stream, peaks, peak_src, skip=None):
             "config": case.config, "api": case.api, "tail_split_workspace_bytes": fws_bytes,
             "l2": ("flushed (256 MB write) before every timed launch" if needs_flush else
                    f"inputs and outputs ({resident / 1e6:.0f} MB) larger than L2 (no flush)"),
-            "roofline": {"bound": "tensor", "achieved": round(tf, 2), "peak": peaks["bf16_tflops"],
-                         "unit": "TFLOP/s", "frac": round(tf / peaks["bf16_tflops"], 4),
-                         "traffic": traffic_for(name, PREFILL_KERNEL_SRC),
-                         "peak_source": f"{peak_src} bf16_tflops (burst: one launch at a time)",
-                         "kernel": "attn::g1::prefill_kernel",
-                         "algorithmic": f"{case.flops:.4g} flop per launch ({case.flop_note})"},
+            "roofline": workload_roofline(case, ms, peaks, peak_src, traffic_for(name, PREFILL_KERNEL_SRC)),
             "clocks": clocks.summary(),
         }
         del dev_in, out, lse, fws
