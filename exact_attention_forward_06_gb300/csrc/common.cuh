@@ -37,6 +37,7 @@ enum WaitSite : unsigned {
     kSiteProducerQ = 17,
     kSiteEpilogueSlot = 18,
     kSiteItem = 19,
+    kSiteStoreCmd = 20,
 };
 
 // First error wins; the site is informative only.

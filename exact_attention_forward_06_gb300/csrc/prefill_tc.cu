@@ -94,14 +94,15 @@ constexpr int ITEM_RING = 4;
 // eight softmax warps.
 constexpr uint32_t ITEM_READERS = 2 + 8;
 // q_full[2], q_free[2], kv_full[NSLOT], kv_empty[NSLOT], s_full[2], s_free[2],
-// p_full[2], o_full[2], fin, item_full[ITEM_RING], item_empty[ITEM_RING]
-constexpr int NBARS = 2 + 2 + 2 * NSLOT + 2 + 2 + 2 + 2 + 1 + 2 * ITEM_RING;
+// p_full[2], o_full[2], fin, item_full[ITEM_RING], item_empty[ITEM_RING],
+// stage_ready[2], stage_taken[2]
+constexpr int NBARS = 2 + 2 + 2 * NSLOT + 2 + 2 + 2 + 2 + 1 + 2 * ITEM_RING + 2 + 2;
 constexpr uint32_t SMEM_MISC = 768;
 constexpr uint32_t SMEM_ALIGN = 1024;
 constexpr float RESCALE_LOG2 = 8.0f;  // move the running max past a 2^8 growth (and see softmax_wg)
 constexpr float LN2 = 0.6931471805599453f;
 
-static_assert(NBARS * 8 + 8 + 64 * ITEM_RING <= SMEM_MISC, "barrier area too small");
+static_assert(NBARS * 8 + 8 + 64 * ITEM_RING + 2 * 32 <= SMEM_MISC, "barrier area too small");
 
 constexpr uint32_t IDESC_S = ptx::idesc_bf16_f32(128, 128, 0, 0);   // Q K^T: both K-major
 constexpr uint32_t IDESC_PV = ptx::idesc_bf16_f32(128, 128, 0, 1);  // P V: V is N(d)-major
@@ -134,11 +135,20 @@ struct SmemLayout {
     // every reader has taken it.
     __device__ uint64_t *item_full(int i) const { return bars + 13 + 2 * NSLOT + i; }
     __device__ uint64_t *item_empty(int i) const { return bars + 13 + 2 * NSLOT + ITEM_RING + i; }
+    // stage_ready(t): softmax group t has written a store command for its
+    // output tile; stage_taken(t): the store lane has read it.
+    __device__ uint64_t *stage_ready(int t) const { return bars + 13 + 2 * NSLOT + 2 * ITEM_RING + t; }
+    __device__ uint64_t *stage_taken(int t) const { return bars + 15 + 2 * NSLOT + 2 * ITEM_RING + t; }
     __device__ uint32_t *tmem_slot() const { return reinterpret_cast<uint32_t *>(bars + NBARS); }
     __device__ volatile int *abort_flag() const { return reinterpret_cast<volatile int *>(bars + NBARS) + 1; }
     // Entry i of the item ring: a decoded unit (16 ints), 8-byte aligned.
     __device__ volatile int *item_ring(int i) const {
         return reinterpret_cast<volatile int *>(bars + NBARS + 1) + 16 * i;
+    }
+    // Store command of tile t: kind (0: no more, 1: store), ring slot, the box's
+    // four coordinates (first 64-column half).
+    __device__ volatile int *stage_cmd(int t) const {
+        return reinterpret_cast<volatile int *>(bars + NBARS + 1) + 16 * ITEM_RING + 8 * t;
     }
     __device__ uint8_t *q_tile(int t) const { return base + (t ? SMEM_Q1 : SMEM_Q0); }
     // Ring slot s: a K or V tile, or a tile's output staging area.
@@ -763,6 +773,33 @@ __device__ __forceinline__ float softmax_tile(const float2 (&s)[64], uint32_t (&
     return a.x + a.y;
 }
 
+// Output stores of tile t, one lane of an otherwise idle control warp: for
+// each command of softmax group t, the TMA store of the staged tile (both
+// 64-column halves), then, once the store has read the slot, the slot goes
+// back to the ring.  The group itself moves on to its next unit as soon as the
+// command is written, so the store's read of shared memory is off the path
+// from one unit's last P to the next unit's first S.
+__device__ void store_lane(const SmemLayout &sm, const WaitCtx &wc, int t, const CUtensorMap *mo) {
+    // O is written once and not read again here: evict-first, so its dirty
+    // lines leave L2 early instead of crowding out K/V and later work.
+    const uint64_t pol_o = ptx::policy_evict_first();
+    for (int n = 0;; ++n) {
+        if (!wait_bounded(sm.stage_ready(t), (uint32_t)(n & 1), wc, kSiteStoreCmd)) return;
+        volatile int *cmd = sm.stage_cmd(t);
+        const int kind = cmd[0], slot = cmd[1];
+        const int c0 = cmd[2], c1 = cmd[3], c2 = cmd[4], c3 = cmd[5];
+        ptx::mbar_arrive(sm.stage_taken(t));
+        if (kind == 0) return;  // the group has no more tiles
+        const uint8_t *stage = sm.slot(slot);
+        ptx::tma_store_4d_hint(mo, stage, c0, c1, c2, c3, pol_o);
+        ptx::tma_store_4d_hint(mo, stage + HALF_BYTES, c0 + 64, c1, c2, c3, pol_o);
+        ptx::bulk_commit_group();
+        ptx::bulk_wait_group_read0();
+        // one arrival for each of the two streams that release K/V slots
+        ptx::mbar_arrive_cnt(sm.kv_empty(slot), 2);
+    }
+}
+
 // Hand a barrier one arrival for the whole warp once every lane's tensor-memory
 // accesses are complete.
 __device__ __forceinline__ void warp_arrive(uint64_t *bar, int lane) {
@@ -784,6 +821,24 @@ __device__ void softmax_wg(const PrefillParams &p, const SmemLayout &sm, const W
     const float sl2 = p.scale_log2;
     int nb = 0;  // ring number of the unit's first K/V item
     int g0 = 0;  // running index of the unit's first score tile
+    const bool leader = quarter == 0 && lane == 0;
+    int n_cmd = 0;  // store commands handed to this tile's store lane
+    // The leader writes command n_cmd once the store lane has read the one
+    // before (kind 0: no more tiles).
+    auto send_cmd = [&](int kind, int slot, const Coord4 &c) -> bool {
+        if (n_cmd > 0 && !wait_bounded(sm.stage_taken(t), (uint32_t)((n_cmd - 1) & 1), wc, kSiteStoreCmd))
+            return false;
+        volatile int *cmd = sm.stage_cmd(t);
+        cmd[0] = kind;
+        cmd[1] = slot;
+        cmd[2] = c.c0;
+        cmd[3] = c.c1;
+        cmd[4] = c.c2;
+        cmd[5] = c.c3;
+        ++n_cmd;
+        ptx::mbar_arrive(sm.stage_ready(t));
+        return true;
+    };
     for (int u = 0;; ++u) {
         Unit w;
         const bool got = read_unit(sm, wc, u, false, w);
@@ -1005,7 +1060,7 @@ __device__ void softmax_wg(const PrefillParams &p, const SmemLayout &sm, const W
         ptx::tc_fence_before();
         ptx::fence_proxy_async_smem();
         if (!ptx::named_bar_and(1 + t, 128, ok && !*wc.abort_flag)) break;
-        const bool leader = quarter == 0 && lane == 0;
+        bool handed = false;  // the store lane releases the slot
         if (PACKED && s0 + BM > w.Sq) {
             // Last row block of a packed sequence: a full box would spill into the
             // next sequence's rows, so each thread stores its own row (if valid)
@@ -1021,23 +1076,18 @@ __device__ void softmax_wg(const PrefillParams &p, const SmemLayout &sm, const W
             }
             ptx::named_bar_sync(1 + t, 128);
         } else if (leader && s0 < w.Sq && (PACKED || w.part < 0)) {
-            // (with head packing the output map's box covers the group's heads)
-            const Coord4 lo = coord4(p.bhsd, 0, h0, w.q0 + s0, w.tb);
-            const Coord4 hi = coord4(p.bhsd, 64, h0, w.q0 + s0, w.tb);
-            // O is written once and not read again here: evict-first, so its dirty
-            // lines leave L2 early instead of crowding out K/V and later work.
-            const uint64_t pol_o = ptx::policy_evict_first();
-            ptx::tma_store_4d_hint(mo, stage, lo.c0, lo.c1, lo.c2, lo.c3, pol_o);
-            ptx::tma_store_4d_hint(mo, stage + HALF_BYTES, hi.c0, hi.c1, hi.c2, hi.c3, pol_o);
-            ptx::bulk_commit_group();
-            ptx::bulk_wait_group_read0();
+            // The TMA store goes to the store lane (with head packing the
+            // output map's box covers the group's heads).  The staged rows were
+            // made visible to the async proxy before the group barrier.
+            handed = send_cmd(1, o_item % NSLOT, coord4(p.bhsd, 0, h0, w.q0 + s0, w.tb));
         }
-        // The slot is free again once the store has read it (one arrival for
-        // each of the two streams that release K/V slots).
-        if (leader) ptx::mbar_arrive_cnt(sm.kv_empty(o_item % NSLOT), 2);
+        // Otherwise the slot is free again now (one arrival for each of the two
+        // streams that release K/V slots).
+        if (leader && !handed) ptx::mbar_arrive_cnt(sm.kv_empty(o_item % NSLOT), 2);
         nb += ring_items(w);
         g0 += w.n_kv;
     }
+    if (leader) send_cmd(0, 0, Coord4{0, 0, 0, 0});  // the store lane stops (if it still waits)
 }
 
 // ------------------------------------------------------------------ kernel
@@ -1079,6 +1129,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             ptx::mbar_init(sm.item_full(i), 1);
             ptx::mbar_init(sm.item_empty(i), ITEM_READERS);
         }
+        for (int t = 0; t < 2; ++t) {
+            ptx::mbar_init(sm.stage_ready(t), 1);
+            ptx::mbar_init(sm.stage_taken(t), 1);
+        }
         *sm.abort_flag() = 0;
         ptx::fence_mbar_init();
         ptx::prefetch_tensormap(&map_q);
@@ -1103,6 +1157,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 producer_paged(p, sm, wc, lane, &map_q, &map_k, &map_v, &map_k8, &map_v8);
             else if (lane == 0)
                 producer<KIND>(p, sm, wc, &map_q, &map_k, &map_v);
+        } else if (warp == 3) {
+            if (lane < 2) store_lane(sm, wc, lane, &map_o);
         } else if (warp == 1 || warp == 2) {
             if (lane == 0) {
                 if (warp == 1)

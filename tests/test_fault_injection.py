@@ -37,9 +37,10 @@ def test_expired_wait_is_reported_and_context_survives(A):
         A.fwd(dq, dk, dv, scale=w.scale)
         code, site = A.device_status()       # synchronises
         assert code == 4, f"expected ATTN_ERR_TIMEOUT, got {code}"
-        # a wait of the MMA-issuing or softmax side gave up: for its work item
-        # (19), its Q tile (1), a K/V tile (2) or a score tile (4, 5, 6)
-        assert site in (1, 2, 4, 5, 6, 19), site
+        # a wait of the MMA-issuing, softmax or store side gave up: for its
+        # work item (19), its Q tile (1), a K/V tile (2), a score tile (4, 5,
+        # 6) or a store command (20)
+        assert site in (1, 2, 4, 5, 6, 19, 20), site
         assert A.device_status()[0] == 0      # reading clears it
     finally:
         A.debug_inject(0)
