@@ -684,6 +684,11 @@ __device__ void mma_stream(const PrefillParams &p, const SmemLayout &sm, const W
         if (w.n_kv < 0) return;  // end of the list
         if (!wait_spin(sm.q_full(T), (uint32_t)(u & 1), wc, kSiteMmaQ)) return;
         ptx::tc_fence_after();
+        // A tile wholly past its sequence's end (the second tile of a unit whose
+        // rows all fit in the first: a short query with packed heads, or the odd
+        // last row block) keeps the barrier protocol -- its S and P V products
+        // are "done" at once and its ring slots released -- without any MMA.
+        const bool dead = (T == 0 ? w.s0[0] : w.s0[1]) >= w.Sq;
 
         auto do_s = [&](int j) -> bool {
             const int g = g0 + j;
@@ -719,8 +724,38 @@ __device__ void mma_stream(const PrefillParams &p, const SmemLayout &sm, const W
             return true;
         };
 
+        // A dead tile's turns: the same waits, in the same order, then plain
+        // arrivals (no products to wait for).  Waiting for each K/V item too
+        // keeps its release counting for the item in the slot, so it never
+        // runs ahead of the ring.
+        auto dead_s = [&](int j) -> bool {
+            const int g = g0 + j;
+            const int item = nb + 2 * j;
+            const int prev = T == 1 ? g : g - 1;
+            if (prev >= 0 && !wait_spin(sm.s_free(1 - T), (uint32_t)(prev & 1), wc, kSiteMmaPoll)) return false;
+            if (!wait_spin(sm.kv_full(slot_of(item)), par_of(item), wc, kSiteMmaPoll)) return false;
+            ptx::mbar_arrive(sm.s_full(T));
+            ptx::mbar_arrive(sm.kv_empty(slot_of(item)));
+            if (j == w.n_kv - 1) ptx::mbar_arrive(sm.q_free(T));
+            return true;
+        };
+        auto dead_pv = [&](int j) -> bool {
+            const int item = nb + 2 * j + 1;
+            if (!wait_spin(sm.p_full(T), (uint32_t)((g0 + j) & 1), wc, kSiteMmaPoll)) return false;
+            if (!wait_spin(sm.kv_full(slot_of(item)), par_of(item), wc, kSiteMmaPoll)) return false;
+            ptx::mbar_arrive(sm.o_full(T));
+            ptx::mbar_arrive(sm.kv_empty(slot_of(item)));
+            return true;
+        };
+
         if (w.n_kv == 0) {
             ptx::umma_commit(sm.q_free(T));  // nothing to multiply: Q_t is free at once
+        } else if (dead) {
+            if (!dead_s(0)) return;
+            for (int j = 0; j < w.n_kv; ++j) {
+                if (j + 1 < w.n_kv && !dead_s(j + 1)) return;
+                if (!dead_pv(j)) return;
+            }
         } else {
             if (!do_s(0)) return;
             for (int j = 0; j < w.n_kv; ++j) {
@@ -856,13 +891,34 @@ __device__ void softmax_wg(const PrefillParams &p, const SmemLayout &sm, const W
             pos = s0 + (p.bhsd ? r % p.pack_pos : r / p.G);
             head = h0 + hr;
         }
+        // A tile wholly past the sequence's end computes nothing (its MMA
+        // stream issues no products either) and stores nothing.
+        const bool dead = s0 >= w.Sq;
         const int lim_row = p.causal ? min(pos + w.Sk - w.Sq, w.Sk - 1) : w.Sk - 1;
         // the tile's first position is its smallest
         const int lim_tile = p.causal ? min(s0 + w.Sk - w.Sq, w.Sk - 1) : w.Sk - 1;
         float m_run = -INFINITY, l_run = 0.f;
         bool ok = true;
 
-        for (int j = 0; j < w.n_kv; ++j) {
+        // No rows of the sequence: pass the score and P turns on.  The wait for
+        // P V(g-1) stays, as on the live path: it keeps this group from
+        // completing p_full(g+1) before the MMA stream has waited for p_full(g)
+        // (the stream issues S(g+1) first), which would make that parity wait
+        // miss its phase.
+        for (int j = 0; dead && j < w.n_kv; ++j) {
+            const int g = g0 + j;
+            if (!wait_bounded(sm.s_full(t), (uint32_t)(g & 1), wc, kSiteSoftmaxS)) {
+                ok = false;
+                break;
+            }
+            warp_arrive(sm.s_free(t), lane);
+            if (j > 0 && !wait_bounded(sm.o_full(t), (uint32_t)((g - 1) & 1), wc, kSiteSoftmaxO)) {
+                ok = false;
+                break;
+            }
+            warp_arrive(sm.p_full(t), lane);
+        }
+        for (int j = 0; !dead && j < w.n_kv; ++j) {
             const int g = g0 + j;
             if (!wait_bounded(sm.s_full(t), (uint32_t)(g & 1), wc, kSiteSoftmaxS)) {
                 ok = false;
@@ -1025,7 +1081,7 @@ __device__ void softmax_wg(const PrefillParams &p, const SmemLayout &sm, const W
                 }
             }
             p.ws_lse[row * p.split_parts + w.part] = l_run > 0.f ? (m_run + ptx::lg2(l_run)) * LN2 : -INFINITY;
-        } else if (ok) {
+        } else if (ok && !dead) {
             ptx::tc_fence_after();
             const float inv = l_run > 0.f ? 1.0f / l_run : 0.f;
 #pragma unroll 1

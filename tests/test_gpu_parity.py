@@ -30,6 +30,8 @@ def _run(A, w, q, k, v, fn="fwd"):
     dq, dk, dv = (t.cuda() for t in (q, k, v))
     out, lse = getattr(A, fn)(dq, dk, dv, causal=w.causal, scale=w.scale, layout=w.layout)
     torch.cuda.synchronize()
+    code, site = A.device_status()
+    assert code == 0, f"{w.name}: device status {code} at wait site {site}"
     return out, lse
 
 
@@ -69,6 +71,8 @@ SMALL = [
     ("bhsd_gqa_causal", 1, 4, 2, 1024, 1024, "bhsd", True),
     ("three_row_blocks_g1", 1, 2, 2, 384, 384, "bshd", False),
     ("short_causal_g1", 1, 1, 1, 130, 130, "bshd", True),
+    # five row blocks in pairs: the last pair's second tile lies past the end
+    ("odd_row_blocks_g1_causal", 2, 2, 2, 640, 640, "bhsd", True),
     # more units than SMs, so each CTA loops over several: units whose rows see
     # no key (causal, Sq > Sk) between ordinary ones, and an odd group size
     ("looping_units_masked_rows", 4, 32, 8, 2048, 512, "bshd", True),
