@@ -35,7 +35,7 @@ def _worker(rank, world, port, results):
 def test_max_over_two_gloo_ranks():
     world = 2
     port = _free_port()
-    with mp.Manager() as m:
+    with mp.get_context("spawn").Manager() as m:  # no fork of this multi-threaded process
         results = m.dict()
         mp.spawn(_worker, args=(world, port, results), nprocs=world, join=True)
         assert dict(results) == {0: 11.0, 1: 11.0}
