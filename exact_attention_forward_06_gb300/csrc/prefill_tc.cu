@@ -550,6 +550,15 @@ __device__ void producer_paged(const PrefillParams &p, const SmemLayout &sm, con
         const int *row = p.block_table + (int64_t)w.b * p.max_blocks;
         int page_row = p.num_pages * 16;  // this lane's page of the current tile (lanes < 8)
         bool run = false;                 // the current tile's pages are one run in the pool
+        // Block-table entries are read one tile ahead (lanes < 8: one page
+        // each), so a load's latency never sits between a free slot and the
+        // tile's copies; the first tile's are read before the Q loads.
+        auto table_entry = [&](int jt) -> int {
+            const int page = (w.j_lo + jt) * (BN / 16) + lane;
+            return page < n_pages ? row[page] : -1;
+        };
+        int next_phys = -1;
+        if (lane < BN / 16 && total > 0) next_phys = table_entry(0);
         if (lane == 0) {
             for (int t = 0; t < 2 && ok; ++t) {
                 if (qn[t] > 0 && !wait_bounded(sm.q_free(t), (qn[t] - 1) & 1, wc, kSiteProducerQ)) {
@@ -571,7 +580,8 @@ __device__ void producer_paged(const PrefillParams &p, const SmemLayout &sm, con
             const int slot = n % NSLOT;
             if (i < total && (i & 1) == 0 && lane < BN / 16) {
                 const int page = (w.j_lo + (i >> 1)) * (BN / 16) + lane;
-                const int phys = page < n_pages ? row[page] : -1;
+                const int phys = next_phys;
+                if ((i >> 1) + 1 < w.n_kv) next_phys = table_entry((i >> 1) + 1);
                 const bool ok_page = phys >= 0 && phys < p.num_pages;
                 if (!ok_page && page < n_pages) report_status(p.status, kStatusDeviceBounds, kSitePagedTable);
                 page_row = ok_page ? phys * 16 : p.num_pages * 16;
