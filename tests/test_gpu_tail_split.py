@@ -67,3 +67,34 @@ def test_tail_split_matches_oracle_and_unsplit(A, layout, Hq, Hkv, Sk):
     assert torch.equal(o_split[head], o_whole[head]) and torch.equal(l_split[head], l_whole[head])
     # and the split units agree with the unsplit result to within the tolerance
     check_out(o_split[B - tail_b:], o_whole[B - tail_b:].double().cpu().numpy(), "split vs whole")
+
+
+def test_tail_split_with_dead_second_tiles(A):
+    # One head (G = 1) and 300 query rows: each batch has a unit of row blocks
+    # 0 and 1 and a unit of row block 2 whose second tile lies wholly past the
+    # end.  The second kind come last in the unit order, so the split tail
+    # units are of that kind: their dead tile passes its turns and its parts
+    # carry nothing.  Every output element is compared with the oracle.
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    B, Sq, Sk = sms + 8, 300, 2048
+    w = inputs.PrefillWorkload("tail_dead", B, 1, 1, Sq, Sk, seed=73)
+    need = A.fwd_workspace_bytes(B, 1, 1, Sq, Sk, causal=False)
+    assert need > 0, "this shape is meant to get a tail split"
+    q, k, v = inputs.make_prefill(w)
+    dq, dk, dv = q.cuda(), k.cuda(), v.cuda()
+    o_whole, l_whole = A.fwd(dq, dk, dv, scale=w.scale)
+    ws = torch.empty(need, device="cuda", dtype=torch.uint8)
+    try:
+        A.set_workspace(ws)
+        o_split, l_split = A.fwd(dq, dk, dv, scale=w.scale)
+        o_again, l_again = A.fwd(dq, dk, dv, scale=w.scale)
+        torch.cuda.synchronize()
+    finally:
+        A.set_workspace(None)
+    assert A.device_status()[0] == 0
+    assert torch.equal(o_split, o_again) and torch.equal(l_split, l_again)
+    ref_o, ref_l = oracle.attention(q, k, v, B=B, Hq=1, Hkv=1, Sq=Sq, Sk=Sk, d=w.d, layout=w.layout, causal=False,
+                                    scale=w.scale)
+    check_out(o_split, ref_o, "tail split, dead second tiles")
+    check_lse(l_split, ref_l, "tail split, dead second tiles")
+    check_out(o_whole, ref_o, "no split, dead second tiles")
