@@ -123,6 +123,18 @@ __global__ void __launch_bounds__(NTHREADS, 3)
     const int64_t row0 = (int64_t)b * p.Hq + h0;  // first (b, h) row of this CTA
     // With a fused append, split 0 also attends to the new token (position L).
     const bool new_token = p.k_new != nullptr && split == 0 && !bad_len;
+    // The producer warp starts the split's block-table reads at once, for the
+    // entries of the split that lie within the table row, so that their
+    // latency overlaps the length check and the set-up; the first np of
+    // them are used.
+    constexpr int TAB = MAX_PAGES_PER_SPLIT / 32;
+    int tab[TAB];
+    if (warp == NCW) {
+        const int lim = min(p.pages_per_split, p.max_blocks - page0);
+        const int32_t *row = p.block_table + (int64_t)b * p.max_blocks + page0;
+#pragma unroll
+        for (int q = 0; q < TAB; ++q) tab[q] = lane + 32 * q < lim ? row[lane + 32 * q] : -1;
+    }
 
     if (np == 0 && !new_token) {  // nothing to attend to in this split
         for (int i = threadIdx.x; i < GH * D; i += NTHREADS)
@@ -145,9 +157,12 @@ __global__ void __launch_bounds__(NTHREADS, 3)
 
     if (warp == NCW) {
         // ---------------- producer
-        // The whole warp reads the split's block-table entries in one go, so
-        // the copy-issuing lane never waits on a global load per page.
-        for (int k = lane; k < np; k += 32) split_pages[k] = p.block_table[(int64_t)b * p.max_blocks + page0 + k];
+        // The whole warp puts the split's block-table entries (read at entry)
+        // into shared memory, so the copy-issuing lane never waits on a
+        // global load per page.
+#pragma unroll
+        for (int q = 0; q < TAB; ++q)
+            if (lane + 32 * q < np) split_pages[lane + 32 * q] = tab[q];
         if (new_token && h0 % p.G == 0) {
             // Fused append: one CTA per (sequence, KV head) writes the new
             // token's K and V rows (256 B each) into slot L % 16 of page
