@@ -110,3 +110,19 @@ def test_missing_page_for_the_new_token_is_reported(A):
     # sequence 1's token was written; sequence 0's pages are as they were
     assert torch.equal(_bits(dkp[int(table[1, 1])][4]), _bits(k_new[1]))
     assert torch.equal(_bits(dkp[int(table[0, 0])]), _bits(kp[int(table[0, 0])]))
+
+
+def test_append_long_context(A):
+    # The new token lands at position 65 535, the last slot of the last of
+    # 4096 pages, of a sequence split 256 ways; the short sequence appends to
+    # its first page.  Split 0 of each sequence attends to the new token.
+    w, q, kp, vp, table, lens, k_new, v_new = _case([65535, 3], Hq=8, Hkv=2, seed=113, max_blocks=4096)
+    ref_o, ref_l, ref_kp, ref_vp = oracle.decode_paged_append(q, k_new, v_new, kp, vp, table, lens, scale=w.scale)
+    dkp, dvp = kp.cuda(), vp.cuda()
+    out, lse = A.decode_paged_append(q.cuda(), k_new.cuda(), v_new.cuda(), dkp, dvp, table.cuda(), lens.cuda(),
+                                     scale=w.scale)
+    torch.cuda.synchronize()
+    assert A.device_status()[0] == 0
+    check_out(out, ref_o, "append, 65536 keys")
+    check_lse(lse, ref_l, "append, 65536 keys")
+    assert torch.equal(_bits(dkp), _bits(ref_kp)) and torch.equal(_bits(dvp), _bits(ref_vp))

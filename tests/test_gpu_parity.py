@@ -291,6 +291,17 @@ def test_paged_decode_ignores_garbage_past_sequence_end(A):
     check_lse(lse, ref_l, "garbage past the end")
 
 
+def test_paged_decode_long_context(A):
+    # 65 536 keys (4096 pages: the split plan's floor of 16 pages a split gives
+    # 256 splits, all of them full) beside a 3-token sequence whose splits are
+    # all empty but the first.
+    w = inputs.DecodeWorkload("long", B=2, Hq=8, Hkv=2, max_blocks=4096, seed=29)
+    out, lse, ref_o, ref_l = _decode(A, w, seqlens=[65536, 3])
+    check_out(out, ref_o, "decode, 65536 keys")
+    check_lse(lse, ref_l, "decode, 65536 keys")
+    assert A.device_status()[0] == 0
+
+
 def test_paged_decode_dominant_keys(A):
     # Two keys per sequence score far above the rest for the first head of
     # each KV group (about 34 and 33.7 in natural-log units) and carry opposite
